@@ -1,0 +1,206 @@
+"""CPU oracle for the VSA hot path -- TEST INFRASTRUCTURE ONLY.
+
+The arithmetic lives in ``vsa_oracle.c`` (plain C, IEEE double); this module
+compiles it with gcc on first use and marshals numpy arrays into it.  Only the
+test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA path
+and imports nothing from it.
+
+Every function takes bf16 data as ``numpy.uint16`` bit patterns, shaped as in
+the CUDA path's C ABI: token rows ``[B, S, heads, D]``.
+
+Parity status of each function (what pins it is in ``tests/test_oracle_*.py``):
+    num_cubes / tile / untile  -- pinned (worked shape example, brute force,
+                                  reshape restatement, inverse identity)
+    pool / coarse              -- pinned (closed forms, einsum+argsort
+                                  restatement, invariances, hand cases)
+    fine                       -- pinned (dense SDPA special case, brute-force
+                                  masked matrix, closed forms, invariances)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "vsa_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_f64 = ctypes.c_double
+_ptr = ctypes.c_void_p
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle shared library with gcc (-O2, no fast-math)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.run(
+            ["gcc", "-O2", "-std=c99", "-D_POSIX_C_SOURCE=200809L", "-fPIC", "-shared",
+             "-pthread", src, "-o", tmp, "-lm"],
+            check=True,
+        )
+        os.replace(tmp, out)
+    return out
+
+
+def load_library(path: str):
+    lib = ctypes.CDLL(path)
+    lib.oracle_num_cubes.restype = _i64
+    lib.oracle_num_cubes.argtypes = [_i64, _i64, _i64]
+    lib.oracle_tile.restype = None
+    lib.oracle_tile.argtypes = [_i64] * 6 + [_ptr, _ptr, _ptr]
+    lib.oracle_untile.restype = None
+    lib.oracle_untile.argtypes = [_i64] * 6 + [_ptr, _ptr]
+    lib.oracle_pool.restype = None
+    lib.oracle_pool.argtypes = [_i64] * 4 + [_ptr, _ptr, _ptr]
+    lib.oracle_coarse.restype = None
+    lib.oracle_coarse.argtypes = [_i64] * 4 + [_ptr, _ptr, _ptr, _i64, _f64, _ptr, _ptr]
+    lib.oracle_fine.restype = _i64
+    lib.oracle_fine.argtypes = ([_i64] * 4 + [_ptr] * 5 + [_i64, _f64, _ptr, _i64, _ptr, _ptr, _i64])
+    lib.oracle_default_threads.restype = _i64
+    lib.oracle_default_threads.argtypes = []
+    return lib
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+class using_library:
+    """Context manager: route every oracle call through another build of the
+    oracle source (the tests use it to run the pins against planted mistakes)."""
+
+    def __init__(self, path: str):
+        self._new = load_library(path)
+        self._old = None
+
+    def __enter__(self):
+        global _lib
+        lib()
+        with _lock:
+            self._old, _lib = _lib, self._new
+        return self._new
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self._old
+        return False
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, "bf16 data is passed as uint16 bit patterns"
+    return a
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def num_cubes(T: int, H: int, W: int) -> int:
+    return int(lib().oracle_num_cubes(T, H, W))
+
+
+def tile(x: np.ndarray, grid):
+    """x: [B, T*H*W, heads, D] uint16 -> (xt [B, N*64, heads, D], vbs [N])."""
+    B, T, H, W = grid
+    x = _u16(x)
+    assert x.shape[:2] == (B, T * H * W)
+    heads, D = x.shape[2], x.shape[3]
+    N = num_cubes(T, H, W)
+    xt = np.empty((B, N * 64, heads, D), np.uint16)
+    vbs = np.empty((N,), np.int32)
+    lib().oracle_tile(B, T, H, W, heads, D, _p(x), _p(xt), _p(vbs))
+    return xt, vbs
+
+
+def untile(yt: np.ndarray, grid) -> np.ndarray:
+    B, T, H, W = grid
+    yt = _u16(yt)
+    heads, D = yt.shape[2], yt.shape[3]
+    N = num_cubes(T, H, W)
+    assert yt.shape[:2] == (B, N * 64)
+    y = np.empty((B, T * H * W, heads, D), np.uint16)
+    lib().oracle_untile(B, T, H, W, heads, D, _p(yt), _p(y))
+    return y
+
+
+def pool(xt: np.ndarray, vbs: np.ndarray) -> np.ndarray:
+    """Cube means: xt [B, N*64, heads, D] -> [B, heads, N, D] float64."""
+    xt = _u16(xt)
+    vbs = _i32(vbs)
+    B, S, heads, D = xt.shape
+    N = S // 64
+    out = np.empty((B, heads, N, D), np.float64)
+    lib().oracle_pool(B, N, heads, D, _p(xt), _p(vbs), _p(out))
+    return out
+
+
+def coarse(qt, kt, vbs, topk: int, sm_scale: float, want_scores: bool = False):
+    """Top-k KV cubes per query cube -> topk_idx [B, heads, N, topk] int32
+    (and the fp64 score matrix [B, heads, N, N] if ``want_scores``)."""
+    qt, kt, vbs = _u16(qt), _u16(kt), _i32(vbs)
+    B, S, heads, D = qt.shape
+    N = S // 64
+    assert 1 <= topk <= N
+    idx = np.empty((B, heads, N, topk), np.int32)
+    scores = np.empty((B, heads, N, N), np.float64) if want_scores else None
+    lib().oracle_coarse(B, N, heads, D, _p(qt), _p(kt), _p(vbs), topk, float(sm_scale),
+                        _p(scores) if scores is not None else None, _p(idx))
+    return (idx, scores) if want_scores else idx
+
+
+def fine(qt, kt, vt, topk_idx, vbs, sm_scale: float, units=None, nthreads: int = 0):
+    """Block-sparse attention over the listed query cubes.
+
+    units: flat indices (b*heads + h)*N + i (default: all).  Returns
+    (out [nunits, 64, D] float64, lse [nunits, 64] float64, threads used).
+    """
+    qt, kt, vt = _u16(qt), _u16(kt), _u16(vt)
+    topk_idx, vbs = _i32(topk_idx), _i32(vbs)
+    B, S, heads, D = qt.shape
+    N = S // 64
+    topk = topk_idx.shape[-1]
+    assert topk_idx.shape == (B, heads, N, topk)
+    if units is None:
+        units = np.arange(B * heads * N, dtype=np.int64)
+    units = np.ascontiguousarray(units, dtype=np.int64)
+    out = np.empty((units.size, 64, D), np.float64)
+    lse = np.empty((units.size, 64), np.float64)
+    used = lib().oracle_fine(B, N, heads, D, _p(qt), _p(kt), _p(vt), _p(topk_idx), _p(vbs),
+                             topk, float(sm_scale), _p(units), units.size, _p(out), _p(lse),
+                             int(nthreads))
+    return out, lse, int(used)
+
+
+def fine_full(qt, kt, vt, topk_idx, vbs, sm_scale: float, nthreads: int = 0):
+    """Fine stage over every query cube, returned in the tiled token layout:
+    (out [B, N*64, heads, D] float64, lse [B, heads, N*64] float64)."""
+    B, S, heads, D = qt.shape
+    N = S // 64
+    out_u, lse_u, _ = fine(qt, kt, vt, topk_idx, vbs, sm_scale, None, nthreads)
+    out = out_u.reshape(B, heads, N * 64, D).transpose(0, 2, 1, 3).copy()
+    lse = lse_u.reshape(B, heads, N * 64).copy()
+    return out, lse
+
+
+def default_threads() -> int:
+    return int(lib().oracle_default_threads())
