@@ -1,0 +1,367 @@
+#!/usr/bin/env python
+"""Benchmark of the VSA hot path on the Wan2.2 attention shape.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+tile q, k, v (21 x 30 x 52 latent grid, 40 heads, D = 128) -> coarse select
+(topk = 78 of 624 cubes) -> block-sparse attention -> untile.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is effective TFLOPS over the whole
+step, using the fine-stage effective FLOP count 4 * S_pad * k * 64 * D * H * B
+(the work the selected blocks need, not the dense work avoided); the fine
+kernel's own time and roofline fraction are reported beside it.  Inputs
+(q, k, v: 3 x 335 MB, plus 1.2 GB of tiled intermediates) exceed the 126 MB
+L2, so no explicit flush is used between steps.
+
+--impl reference times the CPU oracle (the only other implementation there is)
+on a bounded sample of the same workload.  Under torchrun every rank runs its
+own replica (the op shards by heads with no collective; this build runs one
+replica per GPU) and rank 0 reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+if HERE not in sys.path:
+    sys.path.insert(0, HERE)
+
+METRIC = "VSA sparse-attn fwd ms/call and effective TFLOPS; % of GB300 bf16 TC peak"
+UNIT = "TFLOPS (effective)"
+WORKLOAD = "wan"
+KERNELS_PER_STEP = 7  # tile x3, pool sums, score/top-k, sparse attention, untile
+
+
+def load_peaks():
+    path = os.path.join(HERE, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_oracle_sample(wl, inputs, budget_s: float = 15.0, seed: int = 0):
+    """Times the oracle's fine stage (>99.9% of its work) on sampled query
+    cubes of the workload; returns (effective TFLOPS, threads, description)."""
+    import oracle
+    qt, vbs = oracle.tile(inputs["q"], wl.grid)
+    kt, _ = oracle.tile(inputs["k"], wl.grid)
+    vt, _ = oracle.tile(inputs["v"], wl.grid)
+    t0 = time.perf_counter()
+    idx = oracle.coarse(qt, kt, vbs, wl.topk, wl.sm_scale)
+    t_coarse = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    nthreads = oracle.default_threads()
+    units_total = wl.B * wl.heads * wl.ncubes
+    flops_per_unit = wl.fine_flops() / units_total
+    done_units, elapsed, used = 0, 0.0, 0
+    batch = max(nthreads, 8)
+    while elapsed < budget_s and done_units < units_total:
+        units = rng.choice(units_total, size=batch, replace=False).astype(np.int64)
+        t0 = time.perf_counter()
+        _, _, used = oracle.fine(qt, kt, vt, idx, vbs, wl.sm_scale, units)
+        elapsed += time.perf_counter() - t0
+        done_units += batch
+    tflops = done_units * flops_per_unit / elapsed / 1e12
+    desc = (f"fine stage on {done_units} random query cubes of {units_total} "
+            f"({elapsed:.1f} s, {used} threads); full coarse stage took {t_coarse:.1f} s (untimed)")
+    return tflops, used, desc, elapsed / done_units
+
+
+def reference_arm(args, wl, inputs):
+    """--impl reference: the CPU oracle as it stands, one bounded sample per step."""
+    import oracle
+    qt, vbs = oracle.tile(inputs["q"], wl.grid)
+    kt, _ = oracle.tile(inputs["k"], wl.grid)
+    vt, _ = oracle.tile(inputs["v"], wl.grid)
+    idx = oracle.coarse(qt, kt, vbs, wl.topk, wl.sm_scale)
+    nthreads = oracle.default_threads()
+    units_total = wl.B * wl.heads * wl.ncubes
+    per_step = 2 * nthreads
+    rng = np.random.default_rng(1)
+    flops_per_unit = wl.fine_flops() / units_total
+    used = 0
+    for _ in range(args.warmup):
+        _, _, used = oracle.fine(qt, kt, vt, idx, vbs, wl.sm_scale,
+                                 rng.choice(units_total, size=per_step, replace=False))
+    times = []
+    for _ in range(args.steps):
+        units = rng.choice(units_total, size=per_step, replace=False)
+        t0 = time.perf_counter()
+        _, _, used = oracle.fine(qt, kt, vt, idx, vbs, wl.sm_scale, units)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps * per_step * flops_per_unit / total / 1e12
+    desc = f"fine stage on {per_step} random query cubes of {units_total} per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def config_of(wl):
+    return {"workload": f"Wan2.2-shape VSA: grid {wl.T}x{wl.H}x{wl.W}, {wl.heads} heads, D={wl.D}, "
+                        f"topk={wl.topk} of {wl.ncubes} cubes",
+            "B": wl.B, "grid": [wl.T, wl.H, wl.W], "heads": wl.heads, "head_dim": wl.D,
+            "topk": wl.topk, "ncubes": wl.ncubes, "s_padded": wl.s_pad,
+            "fine_flops": wl.fine_flops(), "l2": "inputs (3.2 GB per step) exceed L2; no flush"}
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args, wl, inputs, rank, world, dist):
+    import torch
+
+    import block_sparse_video_vsa_gb300 as vsa
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v = (dev_bf16(inputs[n]) for n in ("q", "k", "v"))
+    grid = wl.grid
+    N = wl.ncubes
+    qt = torch.empty((wl.B, wl.s_pad, wl.heads, wl.D), dtype=torch.bfloat16, device=dev)
+    kt, vt, ot = torch.empty_like(qt), torch.empty_like(qt), torch.empty_like(qt)
+    vbs = torch.empty((N,), dtype=torch.int32, device=dev)
+    vbs2 = torch.empty_like(vbs)
+    idx = torch.empty((wl.B, wl.heads, N, wl.topk), dtype=torch.int32, device=dev)
+    ws = torch.empty((vsa.coarse_workspace_bytes(wl.B, wl.heads, N, wl.D),), dtype=torch.uint8, device=dev)
+    lse = torch.empty((wl.B, wl.heads, wl.s_pad), dtype=torch.float32, device=dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(marks=None):
+        if marks is not None:
+            marks[0].record(stream)
+        vsa.tile(q, grid, out=qt, vbs=vbs)
+        vsa.tile(k, grid, out=kt, vbs=vbs2)
+        vsa.tile(v, grid, out=vt, vbs=vbs2)
+        if marks is not None:
+            marks[1].record(stream)
+        vsa.coarse_select(qt, kt, vbs, wl.topk, wl.sm_scale, workspace=ws, out=idx)
+        if marks is not None:
+            marks[2].record(stream)
+        vsa.sparse_attn_fwd(qt, kt, vt, idx, vbs, wl.sm_scale, out=ot, lse=lse)
+        if marks is not None:
+            marks[3].record(stream)
+        vsa.untile(ot, grid, out=out)
+        if marks is not None:
+            marks[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if vsa.device_error(reset=True):
+        raise RuntimeError("device error word set during warm-up")
+
+    marks = [[ev() for _ in range(5)] for _ in range(args.steps)]
+    start, end = ev(), ev()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record(stream)
+        for s in range(args.steps):
+            step(marks[s])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms_total = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    stage = {name: [marks[s][i].elapsed_time(marks[s][i + 1]) for s in range(args.steps)]
+             for i, name in enumerate(["tile_qkv", "coarse_select", "sparse_attn_fwd", "untile"])}
+    if vsa.device_error(reset=True):
+        raise RuntimeError("device error word set during the timed run")
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    qh, kh, vh = (torch.from_numpy(inputs[n].view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for n in ("q", "k", "v"))
+    oh = torch.empty(qh.shape, dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = 3 * qh.numel() * 2
+    d2h = oh.numel() * 2
+    return ms_step, stage, clk.summary(), e2e_ms, h2d, d2h
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from block_sparse_video_vsa_gb300 import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        inputs = synth.make_inputs(wl)
+        print(json.dumps(reference_arm(args, wl, inputs)), flush=True)
+        return 0
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    from block_sparse_video_vsa_gb300 import build as vbuild
+    if not vbuild.up_to_date() and rank == 0:
+        vbuild.build()
+    if dist:
+        dist.barrier()
+
+    inputs = synth.make_inputs(wl)
+    ms_step, stage, clocks, e2e_ms, h2d, d2h = run_ours(args, wl, inputs, rank, world, dist)
+
+    burst, sustained, hbm, peak_kind = load_peaks()
+    flops = wl.fine_flops()
+    fine_ms = statistics.mean(stage["sparse_attn_fwd"])
+    fine_tflops = flops / (fine_ms * 1e-3) / 1e12
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(wl),
+        "fine_kernel": {
+            "ms_per_call_mean": fine_ms, "ms_per_call_median": statistics.median(stage["sparse_attn_fwd"]),
+            "effective_tflops": fine_tflops, "frac_of_burst_peak": fine_tflops / burst,
+            "frac_of_sustained_peak": fine_tflops / sustained},
+        "stages_ms_median": {k: statistics.median(v) for k, v in stage.items()},
+        "roofline": {"bound": "tensor", "achieved": fine_tflops, "peak": burst, "unit": "TFLOP/s",
+                     "frac": fine_tflops / burst, "traffic": None,
+                     "peak_kind": f"{peak_kind} dense bf16 burst",
+                     "kernel": "fine_fwd_kernel (vsa_sparse_attn_fwd)"},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tflops, cores, desc, _ = cpu_oracle_sample(wl, inputs, args.cpu_budget)
+        result["cpu_baseline"] = {"value": tflops, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

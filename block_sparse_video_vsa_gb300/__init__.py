@@ -1,0 +1,256 @@
+"""GB300-native Video Sparse Attention (VSA) hot path.
+
+Python binding of ``libvsa.so`` (C ABI declared in ``include/vsa.h``).  Every
+function here only marshals arguments: it checks tensor placement, dtype and
+shape, allocates outputs with PyTorch, and calls the C entry point of the same
+name on the current CUDA stream.  All computation runs in the library's
+sm_103a kernels; there is no CPU fallback, and a missing library raises.
+
+    xt, vbs  = tile(x, grid)                       # raster -> cube-major
+    topk_idx = coarse_select(qt, kt, vbs, topk)    # mean-pool + score + top-k
+    o, lse   = sparse_attn_fwd(qt, kt, vt, topk_idx, vbs)
+    y        = untile(o, grid)                     # cube-major -> raster
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Sequence, Tuple
+
+from .build import LIB_PATH
+
+__all__ = [
+    "VsaError", "library", "num_cubes", "tile", "untile", "coarse_workspace_bytes", "coarse_select",
+    "sparse_attn_fwd", "validate_indices", "device_error", "debug_wait_timeout", "pipeline",
+]
+
+_STATUS = {0: "VSA_OK", 1: "VSA_ERR_INVALID_ARG", 2: "VSA_ERR_UNSUPPORTED", 3: "VSA_ERR_ALIGNMENT",
+           4: "VSA_ERR_INDEX_RANGE", 5: "VSA_ERR_TIMEOUT", 6: "VSA_ERR_CUDA"}
+
+
+class VsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_STATUS.get(status, status)}")
+        self.status = status
+
+
+class VsaGrid(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("W", ctypes.c_int32), ("heads", ctypes.c_int32), ("D", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+_p = ctypes.c_void_p
+_i32 = ctypes.c_int32
+
+
+def _declare(lib):
+    lib.vsa_status_string.restype = ctypes.c_char_p
+    lib.vsa_status_string.argtypes = [ctypes.c_int]
+    lib.vsa_num_cubes.restype = ctypes.c_int64
+    lib.vsa_num_cubes.argtypes = [ctypes.POINTER(VsaGrid)]
+    lib.vsa_tile.restype = ctypes.c_int
+    lib.vsa_tile.argtypes = [ctypes.POINTER(VsaGrid), _p, _p, _p, _p]
+    lib.vsa_untile.restype = ctypes.c_int
+    lib.vsa_untile.argtypes = [ctypes.POINTER(VsaGrid), _p, _p, _p]
+    lib.vsa_coarse_workspace_bytes.restype = ctypes.c_size_t
+    lib.vsa_coarse_workspace_bytes.argtypes = [_i32] * 4
+    lib.vsa_coarse_select.restype = ctypes.c_int
+    lib.vsa_coarse_select.argtypes = [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _p, _p, _p]
+    lib.vsa_sparse_attn_fwd.restype = ctypes.c_int
+    lib.vsa_sparse_attn_fwd.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_float,
+                                        _p, _p, _p]
+    lib.vsa_validate_indices.restype = ctypes.c_int
+    lib.vsa_validate_indices.argtypes = [_p, _p, _i32, _i32, _i32, _i32, _p, _p]
+    lib.vsa_device_error.restype = ctypes.c_int
+    lib.vsa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), _i32]
+    lib.vsa_debug_wait_timeout.restype = ctypes.c_int
+    lib.vsa_debug_wait_timeout.argtypes = [ctypes.c_int64, _p, _p]
+    return lib
+
+
+def library():
+    """The loaded libvsa.so (ctypes).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libvsa.so not found at {LIB_PATH}; build it first "
+                    "(python -m block_sparse_video_vsa_gb300.build)")
+            _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise VsaError(status, what)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _grid(grid, heads: int, D: int) -> VsaGrid:
+    B, T, H, W = (int(v) for v in grid)
+    return VsaGrid(B, T, H, W, int(heads), int(D))
+
+
+def num_cubes(grid: Sequence[int]) -> int:
+    """Cubes covering a (B, T, H, W) grid: ceil(T/4) * ceil(H/4) * ceil(W/4)."""
+    _, T, H, W = (int(v) for v in grid)
+    return -(-T // 4) * -(-H // 4) * -(-W // 4)
+
+
+def tile(x, grid, out=None, vbs=None, stream=None):
+    """Raster [B, T*H*W, heads, D] bf16 -> (cube-major [B, 64*N, heads, D], vbs [N] int32)."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x")
+    B, S, heads, D = x.shape
+    g = _grid(grid, heads, D)
+    if (g.B, g.T * g.H * g.W) != (B, S):
+        raise ValueError("x shape does not match the grid")
+    N = num_cubes(grid)
+    if out is None:
+        out = torch.empty((B, 64 * N, heads, D), dtype=torch.bfloat16, device=x.device)
+    if vbs is None:
+        vbs = torch.empty((N,), dtype=torch.int32, device=x.device)
+    _need(out, torch.bfloat16, "out")
+    _need(vbs, torch.int32, "vbs")
+    _check(library().vsa_tile(ctypes.byref(g), x.data_ptr(), out.data_ptr(), vbs.data_ptr(), _stream(stream)),
+           "vsa_tile")
+    return out, vbs
+
+
+def untile(yt, grid, out=None, stream=None):
+    """Cube-major [B, 64*N, heads, D] bf16 -> raster [B, T*H*W, heads, D]."""
+    torch = _torch()
+    _need(yt, torch.bfloat16, "yt")
+    B, S, heads, D = yt.shape
+    g = _grid(grid, heads, D)
+    if S != 64 * num_cubes(grid) or B != g.B:
+        raise ValueError("yt shape does not match the grid")
+    if out is None:
+        out = torch.empty((B, g.T * g.H * g.W, heads, D), dtype=torch.bfloat16, device=yt.device)
+    _need(out, torch.bfloat16, "out")
+    _check(library().vsa_untile(ctypes.byref(g), yt.data_ptr(), out.data_ptr(), _stream(stream)), "vsa_untile")
+    return out
+
+
+def coarse_workspace_bytes(B: int, heads: int, ncubes: int, D: int) -> int:
+    return int(library().vsa_coarse_workspace_bytes(B, heads, ncubes, D))
+
+
+def coarse_select(qt, kt, vbs, topk: int, sm_scale: float = 0.0, workspace=None, out=None, stream=None):
+    """Top-k key cubes per query cube -> int32 [B, heads, N, topk] (ascending cube ids)."""
+    torch = _torch()
+    _need(qt, torch.bfloat16, "qt")
+    _need(kt, torch.bfloat16, "kt")
+    _need(vbs, torch.int32, "vbs")
+    B, S, heads, D = qt.shape
+    if kt.shape != qt.shape or S % 64:
+        raise ValueError("qt/kt must share a tiled [B, 64*N, heads, D] shape")
+    N = S // 64
+    nbytes = coarse_workspace_bytes(B, heads, N, D)
+    if workspace is None:
+        workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=qt.device)
+    _need(workspace, torch.uint8, "workspace")
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    if out is None:
+        out = torch.empty((B, heads, N, int(topk)), dtype=torch.int32, device=qt.device)
+    _need(out, torch.int32, "out")
+    _check(library().vsa_coarse_select(qt.data_ptr(), kt.data_ptr(), vbs.data_ptr(), B, N, heads, D, int(topk),
+                                       float(sm_scale), workspace.data_ptr(), out.data_ptr(), _stream(stream)),
+           "vsa_coarse_select")
+    return out
+
+
+def sparse_attn_fwd(qt, kt, vt, topk_idx, vbs, sm_scale: float = 0.0, out=None, lse=None,
+                    want_lse: bool = True, stream=None):
+    """Block-sparse attention -> (out bf16 [B, 64*N, heads, D], lse fp32 [B, heads, 64*N] or None)."""
+    torch = _torch()
+    for t, n in ((qt, "qt"), (kt, "kt"), (vt, "vt")):
+        _need(t, torch.bfloat16, n)
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(vbs, torch.int32, "vbs")
+    B, S, heads, D = qt.shape
+    if kt.shape != qt.shape or vt.shape != qt.shape or S % 64:
+        raise ValueError("qt/kt/vt must share a tiled [B, 64*N, heads, D] shape")
+    N = S // 64
+    if topk_idx.dim() != 4 or tuple(topk_idx.shape[:3]) != (B, heads, N):
+        raise ValueError("topk_idx must be [B, heads, N, topk]")
+    topk = topk_idx.shape[3]
+    if out is None:
+        out = torch.empty_like(qt)
+    _need(out, torch.bfloat16, "out")
+    if want_lse and lse is None:
+        lse = torch.empty((B, heads, S), dtype=torch.float32, device=qt.device)
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    _check(library().vsa_sparse_attn_fwd(qt.data_ptr(), kt.data_ptr(), vt.data_ptr(), topk_idx.data_ptr(),
+                                         vbs.data_ptr(), B, N, heads, D, topk, float(sm_scale), out.data_ptr(),
+                                         lse.data_ptr() if lse is not None else None, _stream(stream)),
+           "vsa_sparse_attn_fwd")
+    return out, lse
+
+
+def validate_indices(topk_idx, vbs, stream=None) -> int:
+    """Runs the index validator; returns its flag (0 = valid).  Synchronises."""
+    torch = _torch()
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(vbs, torch.int32, "vbs")
+    B, heads, N, topk = topk_idx.shape
+    flag = torch.zeros((1,), dtype=torch.int32, device=topk_idx.device)
+    _check(library().vsa_validate_indices(topk_idx.data_ptr(), vbs.data_ptr(), B, heads, N, topk,
+                                          flag.data_ptr(), _stream(stream)), "vsa_validate_indices")
+    return int(flag.item())
+
+
+def device_error(reset: bool = False) -> int:
+    v = ctypes.c_uint32(0)
+    _check(library().vsa_device_error(ctypes.byref(v), 1 if reset else 0), "vsa_device_error")
+    return int(v.value)
+
+
+def debug_wait_timeout(limit_ns: int, stream=None) -> int:
+    """Runs the bounded-wait self test; returns 1 if the wait ran out."""
+    torch = _torch()
+    res = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _check(library().vsa_debug_wait_timeout(int(limit_ns), res.data_ptr(), _stream(stream)),
+           "vsa_debug_wait_timeout")
+    return int(res.item())
+
+
+def pipeline(q, k, v, grid, topk: int, sm_scale: float = 0.0, stream=None):
+    """Whole hot path on raster inputs: tile -> coarse select -> sparse attention -> untile.
+
+    Returns (out raster bf16, lse fp32 [B, heads, 64*N] in cube-major order, topk_idx)."""
+    qt, vbs = tile(q, grid, stream=stream)
+    kt, _ = tile(k, grid, vbs=_torch().empty_like(vbs), stream=stream)
+    vt, _ = tile(v, grid, vbs=_torch().empty_like(vbs), stream=stream)
+    idx = coarse_select(qt, kt, vbs, topk, sm_scale, stream=stream)
+    ot, lse = sparse_attn_fwd(qt, kt, vt, idx, vbs, sm_scale, stream=stream)
+    return untile(ot, grid, stream=stream), lse, idx

@@ -1,0 +1,214 @@
+// C ABI of the VSA library: argument validation on the host, then dispatch
+// to the kernels of tile.cu, coarse.cu and fine.cu.  See include/vsa.h for
+// the contract of each entry point.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "vsa_common.cuh"
+
+namespace vsa {
+
+cudaError_t launch_tile(const vsa_grid& g, int ncubes, const void* x, void* xt, int32_t* vbs,
+                        cudaStream_t stream);
+cudaError_t launch_untile(const vsa_grid& g, int ncubes, const void* yt, void* y, cudaStream_t stream);
+size_t coarse_workspace_bytes(int B, int heads, int ncubes, int D);
+size_t coarse_smem_bytes(int R, int N, int D);
+int coarse_rows_per_block(int ncubes);
+cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes, int heads,
+                          int D, int topk, float sm_scale, void* workspace, int32_t* topk_idx,
+                          cudaStream_t stream);
+cudaError_t launch_validate(const int32_t* idx, const int32_t* vbs, int rows, int ncubes, int topk,
+                            int32_t* flag, cudaStream_t stream);
+int validate_max_cubes();
+cudaError_t launch_debug_wait(long long limit_ns, int32_t* result, unsigned int* err, cudaStream_t stream);
+int fine_smem_bytes();
+cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                        const int32_t* vbs, int B, int ncubes, int heads, int D, int topk, float sm_scale,
+                        void* out, float* lse, unsigned int* err, int num_sms, cudaStream_t stream);
+
+// Library-wide device error word (one per device that loads the library).
+__device__ unsigned int g_device_error;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_ctx_mu;
+DevCtx g_ctx[kMaxDevices];
+bool g_ctx_ok[kMaxDevices];
+}  // namespace
+
+cudaError_t get_dev_ctx(DevCtx* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_ctx_mu);
+    if (!g_ctx_ok[dev]) {
+        DevCtx c;
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_error);
+        if (e != cudaSuccess) return e;
+        c.err = static_cast<unsigned int*>(p);
+        e = cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&c.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        g_ctx[dev] = c;
+        g_ctx_ok[dev] = true;
+    }
+    *out = g_ctx[dev];
+    return cudaSuccess;
+}
+
+}  // namespace vsa
+
+using namespace vsa;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+vsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? VSA_OK : VSA_ERR_CUDA; }
+
+bool grid_ok(const vsa_grid* g) {
+    return g && g->B > 0 && g->T > 0 && g->H > 0 && g->W > 0 && g->heads > 0 && g->D > 0;
+}
+
+int64_t cubes_of(const vsa_grid* g) {
+    return (int64_t)((g->T + 3) / 4) * ((g->H + 3) / 4) * ((g->W + 3) / 4);
+}
+
+// Element counts that index int32 loops in the kernels must stay below 2^31.
+bool sizes_fit(int64_t B, int64_t rows, int64_t heads, int64_t D) {
+    const int64_t lim = (int64_t)1 << 31;
+    return heads * D < lim / 64 && B * rows < lim && B * heads * rows / 64 < lim;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vsa_status_string(vsa_status s) {
+    switch (s) {
+        case VSA_OK: return "VSA_OK";
+        case VSA_ERR_INVALID_ARG: return "VSA_ERR_INVALID_ARG";
+        case VSA_ERR_UNSUPPORTED: return "VSA_ERR_UNSUPPORTED";
+        case VSA_ERR_ALIGNMENT: return "VSA_ERR_ALIGNMENT";
+        case VSA_ERR_INDEX_RANGE: return "VSA_ERR_INDEX_RANGE";
+        case VSA_ERR_TIMEOUT: return "VSA_ERR_TIMEOUT";
+        case VSA_ERR_CUDA: return "VSA_ERR_CUDA";
+    }
+    return "VSA_ERR_UNKNOWN";
+}
+
+int64_t vsa_num_cubes(const vsa_grid* g) {
+    if (!grid_ok(g)) return -1;
+    return cubes_of(g);
+}
+
+vsa_status vsa_tile(const vsa_grid* g, const void* x, void* xt, int32_t* vbs, vsa_stream_t stream) {
+    if (!grid_ok(g) || !x || !xt) return VSA_ERR_INVALID_ARG;
+    if ((g->heads * (int64_t)g->D) % 8 != 0) return VSA_ERR_UNSUPPORTED;
+    const int64_t N = cubes_of(g);
+    if (!sizes_fit(g->B, N * 64, g->heads, g->D) || (int64_t)g->T * g->H * g->W >= ((int64_t)1 << 31))
+        return VSA_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(xt) || (vbs && (reinterpret_cast<uintptr_t>(vbs) & 3u)))
+        return VSA_ERR_ALIGNMENT;
+    return from_cuda(launch_tile(*g, (int)N, x, xt, vbs, static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status vsa_untile(const vsa_grid* g, const void* yt, void* y, vsa_stream_t stream) {
+    if (!grid_ok(g) || !yt || !y) return VSA_ERR_INVALID_ARG;
+    if ((g->heads * (int64_t)g->D) % 8 != 0) return VSA_ERR_UNSUPPORTED;
+    const int64_t N = cubes_of(g);
+    if (!sizes_fit(g->B, N * 64, g->heads, g->D) || (int64_t)g->T * g->H * g->W >= ((int64_t)1 << 31))
+        return VSA_ERR_UNSUPPORTED;
+    if (!aligned16(yt) || !aligned16(y)) return VSA_ERR_ALIGNMENT;
+    return from_cuda(launch_untile(*g, (int)N, yt, y, static_cast<cudaStream_t>(stream)));
+}
+
+size_t vsa_coarse_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t D) {
+    if (B <= 0 || heads <= 0 || ncubes <= 0 || D <= 0) return 0;
+    return coarse_workspace_bytes(B, heads, ncubes, D);
+}
+
+vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs, int32_t B, int32_t ncubes,
+                             int32_t heads, int32_t D, int32_t topk, float sm_scale, void* workspace,
+                             int32_t* topk_idx, vsa_stream_t stream) {
+    if (!qt || !kt || !vbs || !workspace || !topk_idx) return VSA_ERR_INVALID_ARG;
+    if (B <= 0 || ncubes <= 0 || heads <= 0 || topk <= 0 || topk > ncubes) return VSA_ERR_INVALID_ARG;
+    if (!(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return VSA_ERR_UNSUPPORTED;
+    if (ncubes > 4096 || !sizes_fit(B, (int64_t)ncubes * 64, heads, D)) return VSA_ERR_UNSUPPORTED;
+    if (!aligned16(qt) || !aligned16(kt) || !aligned16(workspace) || !aligned16(vbs) ||
+        (reinterpret_cast<uintptr_t>(topk_idx) & 3u))
+        return VSA_ERR_ALIGNMENT;
+    DevCtx ctx;
+    cudaError_t e = get_dev_ctx(&ctx);
+    if (e != cudaSuccess) return VSA_ERR_CUDA;
+    const size_t smem = coarse_smem_bytes(coarse_rows_per_block(ncubes), ncubes, D);
+    if (smem > (size_t)ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
+    if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
+    return from_cuda(launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, workspace, topk_idx,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                               const int32_t* vbs, int32_t B, int32_t ncubes, int32_t heads, int32_t D,
+                               int32_t topk, float sm_scale, void* out, float* lse, vsa_stream_t stream) {
+    if (!qt || !kt || !vt || !topk_idx || !vbs || !out) return VSA_ERR_INVALID_ARG;
+    if (B <= 0 || ncubes <= 0 || heads <= 0 || topk <= 0 || topk > ncubes) return VSA_ERR_INVALID_ARG;
+    if (!(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return VSA_ERR_UNSUPPORTED;
+    if (!sizes_fit(B, (int64_t)ncubes * 64, heads, D) || (int64_t)B * ncubes * 64 >= ((int64_t)1 << 31) ||
+        (int64_t)B * heads * ncubes >= ((int64_t)1 << 31))
+        return VSA_ERR_UNSUPPORTED;
+    if (heads > 65535) return VSA_ERR_UNSUPPORTED;  // TMA box coordinate range
+    if (!aligned16(qt) || !aligned16(kt) || !aligned16(vt) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(vbs) & 3u) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return VSA_ERR_ALIGNMENT;
+    DevCtx ctx;
+    cudaError_t e = get_dev_ctx(&ctx);
+    if (e != cudaSuccess) return VSA_ERR_CUDA;
+    if (fine_smem_bytes() > ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
+    if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
+    return from_cuda(launch_fine(qt, kt, vt, topk_idx, vbs, B, ncubes, heads, D, topk, sm_scale, out, lse,
+                                 ctx.err, ctx.num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status vsa_validate_indices(const int32_t* topk_idx, const int32_t* vbs, int32_t B, int32_t heads,
+                                int32_t ncubes, int32_t topk, int32_t* dev_flag, vsa_stream_t stream) {
+    if (!topk_idx || !vbs || !dev_flag) return VSA_ERR_INVALID_ARG;
+    if (B <= 0 || heads <= 0 || ncubes <= 0 || topk <= 0) return VSA_ERR_INVALID_ARG;
+    if (ncubes > validate_max_cubes() || (int64_t)B * heads * ncubes >= ((int64_t)1 << 31))
+        return VSA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(vbs) & 3u) ||
+        (reinterpret_cast<uintptr_t>(dev_flag) & 3u))
+        return VSA_ERR_ALIGNMENT;
+    return from_cuda(launch_validate(topk_idx, vbs, B * heads * ncubes, ncubes, topk, dev_flag,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status vsa_device_error(uint32_t* out, int32_t reset) {
+    if (!out) return VSA_ERR_INVALID_ARG;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return VSA_ERR_CUDA;
+    *out = v;
+    if (reset) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &z, sizeof z) != cudaSuccess) return VSA_ERR_CUDA;
+    }
+    return VSA_OK;
+}
+
+vsa_status vsa_debug_wait_timeout(int64_t limit_ns, int32_t* dev_result, vsa_stream_t stream) {
+    if (!dev_result || limit_ns < 1000 || limit_ns > 10000000000ll) return VSA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(dev_result) & 3u) return VSA_ERR_ALIGNMENT;
+    DevCtx ctx;
+    if (get_dev_ctx(&ctx) != cudaSuccess) return VSA_ERR_CUDA;
+    return from_cuda(launch_debug_wait((long long)limit_ns, dev_result, ctx.err, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,201 @@
+/*
+ * vsa.h -- C ABI of the GB300 (sm_103a) Video Sparse Attention hot path.
+ *
+ * The library implements the data path of Video Sparse Attention (VSA):
+ *   1. vsa_tile            cube tiling of a (T, H, W) latent token grid into
+ *                          zero-padded 4x4x4 cubes plus the per-cube real-token
+ *                          count vbs;
+ *   2. vsa_coarse_select   cube mean-pool of Q and K, cube-to-cube scores and
+ *                          the top-k key/value cubes per query cube;
+ *   3. vsa_sparse_attn_fwd non-causal block-sparse attention over the selected
+ *                          cubes, padded tokens masked (bf16 out + fp32 LSE);
+ *   4. vsa_untile          the inverse permutation of step 1.
+ *
+ * Sources (page title, section):
+ *   [VSA-AMD] "VSA: Accelerating Video Diffusion Inference with Sparse
+ *             Attention on AMD GPUs": Two-Stage Architecture, Block-Sparse
+ *             Encoding, Kernel Architecture, Sparse Traversal, Generating
+ *             Sparsity Patterns.
+ *   [WAN-VSA] "Wan2.2 Production Values -- VSA Block-Sparse Attention Inputs +
+ *             Reference": Shapes, Operator contract.
+ *   [STA]     "FastVideo Guide: Sliding Tile Attention": Implementation
+ *             (tile partition and inverse permutation).
+ *
+ * Conventions shared by every entry point
+ *   - Layout: token tensors are BSHD, i.e. [B, S, heads, D] row-major,
+ *     contiguous, bf16 (IEEE bfloat16 bit patterns).  "Tiled" tensors have
+ *     S = S_pad = 64 * ncubes; "raster" tensors have S = T * H * W with token
+ *     n = (t * H + h) * W + w.
+ *   - Cube order is raster over the cube grid: cube c = (ct * nh + ch) * nw + cw
+ *     with nt = ceil(T/4), nh = ceil(H/4), nw = ceil(W/4).  Inside a cube the
+ *     real tokens of its clipped sub-box occupy slots 0 .. vbs[c]-1 in raster
+ *     (t, h, w) order; slots vbs[c] .. 63 are padding.
+ *   - vbs is int32 [ncubes], shared by every batch entry and head.
+ *   - Ownership: the caller allocates and owns every buffer (device memory
+ *     unless stated) and the stream.  The library allocates no memory.
+ *     Every call is asynchronous on `stream`; results are ready when the
+ *     stream reaches that point.
+ *   - Alignment: device pointers must be 16-byte aligned.
+ *   - Errors: argument checks run on the host before any launch and return a
+ *     status without touching memory.  Launch failures return VSA_ERR_CUDA.
+ *     Faults of a launched kernel surface at the caller's next
+ *     synchronisation.  Kernels never trap: a bounded wait that runs out sets
+ *     a device error word (see vsa_device_error) and the kernel returns.
+ *   - In-place operation is not supported (outputs must not alias inputs).
+ *   - Results are bit-reproducible from run to run on the same device.
+ */
+#ifndef VSA_H_
+#define VSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (cudaStream_t / CUstream); NULL = legacy default stream. */
+typedef void* vsa_stream_t;
+
+typedef enum {
+    VSA_OK = 0,
+    VSA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, topk out of range */
+    VSA_ERR_UNSUPPORTED = 2, /* D not in {64, 128}, or a size beyond a stated limit */
+    VSA_ERR_ALIGNMENT = 3,   /* a device pointer is not 16-byte aligned */
+    VSA_ERR_INDEX_RANGE = 4, /* vsa_validate_indices found a bad index or count */
+    VSA_ERR_TIMEOUT = 5,     /* a device-side bounded wait ran out */
+    VSA_ERR_CUDA = 6         /* a CUDA runtime/driver call failed */
+} vsa_status;
+
+/* Latent token grid: batch B, T x H x W tokens, `heads` heads of size D. */
+typedef struct {
+    int32_t B, T, H, W, heads, D;
+} vsa_grid;
+
+/* Device error word bits (vsa_device_error). */
+#define VSA_DEVERR_TIMEOUT 0x1u /* a bounded mbarrier wait in a kernel ran out */
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* vsa_status_string(vsa_status s);
+
+/*
+ * Number of 4x4x4 cubes covering the grid: ceil(T/4) * ceil(H/4) * ceil(W/4)
+ * ([WAN-VSA] Shapes: 624 = 6 x 8 x 13 for 21 x 30 x 52).  Returns -1 for a
+ * NULL or non-positive grid.
+ */
+int64_t vsa_num_cubes(const vsa_grid* g);
+
+/*
+ * Cube tiling ([VSA-AMD] Two-Stage Architecture, Pre-stage and Stage 1 cube
+ * partition; [WAN-VSA] Shapes "cube-major tiled/padded").
+ *   x   : raster bf16 [B, T*H*W, heads, D]              (read)
+ *   xt  : tiled  bf16 [B, 64*ncubes, heads, D]         (written in full;
+ *         padding slots are written as zero)
+ *   vbs : int32 [ncubes] real tokens per cube, or NULL   (written)
+ * Any D >= 8 with heads * D a multiple of 8 is accepted (rows are copied as
+ * 16-byte vectors).
+ */
+vsa_status vsa_tile(const vsa_grid* g, const void* x, void* xt, int32_t* vbs, vsa_stream_t stream);
+
+/*
+ * Inverse of vsa_tile on the real slots ([STA] Implementation, inverse
+ * permutation); padding slots of yt are ignored.
+ *   yt : tiled  bf16 [B, 64*ncubes, heads, D]   (read)
+ *   y  : raster bf16 [B, T*H*W, heads, D]      (written in full)
+ */
+vsa_status vsa_untile(const vsa_grid* g, const void* yt, void* y, vsa_stream_t stream);
+
+/*
+ * Bytes of device workspace vsa_coarse_select needs: 16 * B * heads * ncubes
+ * * D (exact cube sums of Q and K as fp32 hi/lo pairs).  0 for bad sizes.
+ */
+size_t vsa_coarse_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t D);
+
+/*
+ * Coarse selection ([VSA-AMD] Stage 1: Coarse Selection and Generating
+ * Sparsity Patterns).  For every (b, head, query cube i):
+ *   q_mean_i = (1 / vbs[i]) * sum_{s < vbs[i]} qt[b, 64 i + s, head, :]
+ *   k_mean_j likewise from kt,
+ *   score_ij = sm_scale * (q_mean_i . k_mean_j),
+ *   topk_idx[b, head, i, :] = the topk cubes j with the largest score_ij,
+ *   ties broken toward the lower cube index; the row lists them in
+ *   ascending cube index.
+ * A cube with vbs = 0 pools to the zero vector.  Scores are formed in fp32
+ * with a proven error bound; rows whose k-th boundary falls inside that bound
+ * are re-ranked with exact cube sums in fp64, so the selected set equals the
+ * exact-arithmetic top-k except where exact scores tie to ~1e-13 relative.
+ *   qt, kt    : tiled bf16 [B, 64*ncubes, heads, D]
+ *   vbs       : int32 [ncubes], each in [0, 64]
+ *   topk      : 1 <= topk <= ncubes
+ *   sm_scale  : score scale; <= 0 means 1/sqrt(D)
+ *   workspace : device buffer of vsa_coarse_workspace_bytes(...) bytes,
+ *               16-byte aligned; contents need not be initialised
+ *   topk_idx  : int32 [B, heads, ncubes, topk] (written)
+ * Limits: D in {64, 128}; ncubes <= 4096.
+ */
+vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs, int32_t B,
+                             int32_t ncubes, int32_t heads, int32_t D, int32_t topk,
+                             float sm_scale, void* workspace, int32_t* topk_idx,
+                             vsa_stream_t stream);
+
+/*
+ * Fine stage: non-causal block-sparse attention ([WAN-VSA] Operator contract;
+ * [VSA-AMD] Stage 2: Fine Computation, Kernel Architecture, Sparse Traversal).
+ * For every (b, head, query cube i) and each of its 64 rows r (padding rows
+ * included), with the attended keys
+ *   X = { 64 j + s : j in topk_idx[b, head, i, :], s < vbs[j] }:
+ *   s_x   = sm_scale * (q_r . k_x)
+ *   out_r = sum_x softmax(s)_x v_x          (bf16, round to nearest even)
+ *   lse_r = log(sum_x exp(s_x))             (fp32, natural log)
+ * The softmax subtracts a running row maximum, so logits of any finite size
+ * are safe.  A row with no attended key gets out = 0 and lse = -inf.
+ *   qt, kt, vt : tiled bf16 [B, 64*ncubes, heads, D]; padding slots must hold
+ *                finite values (vsa_tile writes zeros)
+ *   topk_idx   : int32 [B, heads, ncubes, topk], entries in [0, ncubes),
+ *                distinct within a row (order is free)
+ *   vbs        : int32 [ncubes], each in [0, 64]
+ *   out        : bf16 [B, 64*ncubes, heads, D] (written in full)
+ *   lse        : fp32 [B, heads, 64*ncubes] (written), or NULL
+ * Limits: D in {64, 128}; 1 <= topk <= ncubes; 64*ncubes*B < 2^31.
+ * Index validity is a precondition (check with vsa_validate_indices).
+ */
+vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt,
+                               const int32_t* topk_idx, const int32_t* vbs, int32_t B,
+                               int32_t ncubes, int32_t heads, int32_t D, int32_t topk,
+                               float sm_scale, void* out, float* lse, vsa_stream_t stream);
+
+/*
+ * Debug aid for the block-sparse encoding ([VSA-AMD] Block-Sparse Encoding):
+ * checks every topk_idx entry is in [0, ncubes), that no row repeats an
+ * index, and that every vbs entry is in [0, 64].  ORs into *dev_flag (device
+ * int32, caller-initialised): 1 = index out of range, 2 = duplicate index,
+ * 4 = vbs out of range.  Read the flag after the stream synchronises;
+ * VSA_ERR_INDEX_RANGE is the status a caller should report for a non-zero
+ * flag.
+ */
+vsa_status vsa_validate_indices(const int32_t* topk_idx, const int32_t* vbs, int32_t B,
+                                int32_t heads, int32_t ncubes, int32_t topk, int32_t* dev_flag,
+                                vsa_stream_t stream);
+
+/*
+ * Reads (and with reset != 0 clears) the library's device error word on the
+ * current device; synchronous.  Bits: VSA_DEVERR_*.  A kernel whose bounded
+ * wait ran out sets VSA_DEVERR_TIMEOUT, stops, and leaves its outputs
+ * unspecified.
+ */
+vsa_status vsa_device_error(uint32_t* out, int32_t reset);
+
+/*
+ * Self-test of the bounded-wait mechanism the kernels use: launches one
+ * block that waits on an mbarrier nobody arrives on, with a limit of
+ * `limit_ns` nanoseconds (1e3 .. 1e10).  When the wait runs out the kernel
+ * sets VSA_DEVERR_TIMEOUT in the device error word and writes 1 to
+ * *dev_result (device int32), else 0.  The kernel then returns normally.
+ */
+vsa_status vsa_debug_wait_timeout(int64_t limit_ns, int32_t* dev_result, vsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VSA_H_ */

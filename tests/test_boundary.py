@@ -1,0 +1,117 @@
+"""Host-only checks of the C ABI boundary (no GPU needed).
+
+- libvsa.so builds for sm_103a, loads, and exports every entry point that
+  include/vsa.h declares;
+- argument validation runs before any CUDA call and returns the documented
+  status codes (NULL pointers, bad sizes, unsupported D, misalignment).
+Only argument combinations that fail validation are passed here: nothing in
+this file launches a kernel.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_video_vsa_gb300 as vsa
+from block_sparse_video_vsa_gb300 import build as vbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "vsa.h")
+OK, INVALID, UNSUPPORTED, ALIGNMENT = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    vbuild.build()
+    return vsa.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vsa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("vsa_tile", "vsa_untile", "vsa_coarse_select", "vsa_sparse_attn_fwd",
+              "vsa_coarse_workspace_bytes", "vsa_num_cubes", "vsa_status_string",
+              "vsa_validate_indices", "vsa_device_error", "vsa_debug_wait_timeout"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["VSA_OK", "VSA_ERR_INVALID_ARG", "VSA_ERR_UNSUPPORTED", "VSA_ERR_ALIGNMENT",
+                                 "VSA_ERR_INDEX_RANGE", "VSA_ERR_TIMEOUT", "VSA_ERR_CUDA"]):
+        assert lib.vsa_status_string(code).decode() == name
+    assert lib.vsa_status_string(99).decode() == "VSA_ERR_UNKNOWN"
+
+
+def test_num_cubes(lib):
+    g = vsa.VsaGrid(1, 21, 30, 52, 40, 128)
+    assert lib.vsa_num_cubes(ctypes.byref(g)) == 624
+    g = vsa.VsaGrid(1, 0, 30, 52, 40, 128)
+    assert lib.vsa_num_cubes(ctypes.byref(g)) == -1
+    assert lib.vsa_num_cubes(None) == -1
+
+
+def test_workspace_bytes(lib):
+    assert lib.vsa_coarse_workspace_bytes(1, 40, 624, 128) == 16 * 40 * 624 * 128
+    assert lib.vsa_coarse_workspace_bytes(0, 40, 624, 128) == 0
+
+
+A = 0x10000   # fake, never dereferenced: every call below fails validation first
+MIS = 0x10008
+
+
+def test_tile_validation(lib):
+    g = vsa.VsaGrid(1, 5, 6, 10, 2, 64)
+    assert lib.vsa_tile(None, A, A, None, None) == INVALID
+    assert lib.vsa_tile(ctypes.byref(g), None, A, None, None) == INVALID
+    assert lib.vsa_tile(ctypes.byref(g), A, MIS, None, None) == ALIGNMENT
+    bad = vsa.VsaGrid(1, 5, 6, 10, 1, 4)  # heads * D not a multiple of 8
+    assert lib.vsa_tile(ctypes.byref(bad), A, A, None, None) == UNSUPPORTED
+    assert lib.vsa_untile(ctypes.byref(g), MIS, A, None) == ALIGNMENT
+    assert lib.vsa_untile(ctypes.byref(g), A, None, None) == INVALID
+
+
+def test_coarse_validation(lib):
+    f = lib.vsa_coarse_select
+    assert f(None, A, A, 1, 12, 2, 64, 3, 0.0, A, A, None) == INVALID
+    assert f(A, A, A, 1, 12, 2, 64, 0, 0.0, A, A, None) == INVALID       # topk = 0
+    assert f(A, A, A, 1, 12, 2, 64, 13, 0.0, A, A, None) == INVALID      # topk > ncubes
+    assert f(A, A, A, 1, 12, 2, 96, 3, 0.0, A, A, None) == UNSUPPORTED   # D = 96
+    assert f(A, A, A, 1, 5000, 2, 64, 3, 0.0, A, A, None) == UNSUPPORTED  # ncubes > 4096
+    assert f(A, MIS, A, 1, 12, 2, 64, 3, 0.0, A, A, None) == ALIGNMENT
+    assert f(A, A, A, 1, 12, 2, 64, 3, float("nan"), A, A, None) == INVALID
+
+
+def test_fine_validation(lib):
+    f = lib.vsa_sparse_attn_fwd
+    assert f(A, A, A, A, A, 1, 12, 2, 64, 3, 0.0, None, None, None) == INVALID
+    assert f(A, A, A, A, A, 1, 12, 2, 64, 0, 0.0, A, None, None) == INVALID
+    assert f(A, A, A, A, A, 1, 12, 2, 64, 13, 0.0, A, None, None) == INVALID
+    assert f(A, A, A, A, A, 0, 12, 2, 64, 3, 0.0, A, None, None) == INVALID
+    assert f(A, A, A, A, A, 1, 12, 2, 256, 3, 0.0, A, None, None) == UNSUPPORTED
+    assert f(A, A, MIS, A, A, 1, 12, 2, 64, 3, 0.0, A, None, None) == ALIGNMENT
+    assert f(A, A, A, A, A, 1, 12, 2, 64, 3, 0.0, A, A + 2, None) == ALIGNMENT  # lse
+
+
+def test_validator_and_debug_validation(lib):
+    assert lib.vsa_validate_indices(None, A, 1, 1, 12, 3, A, None) == INVALID
+    assert lib.vsa_validate_indices(A, A, 1, 1, 100000, 3, A, None) == UNSUPPORTED
+    assert lib.vsa_debug_wait_timeout(10, A, None) == INVALID
+    assert lib.vsa_debug_wait_timeout(10 ** 6, None, None) == INVALID
+    assert lib.vsa_device_error(None, 0) == INVALID
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros((1, 300, 2, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        vsa.tile(x, (1, 5, 6, 10))
