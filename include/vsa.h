@@ -139,6 +139,26 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
                              vsa_stream_t stream);
 
 /*
+ * vsa_coarse_select without a workspace argument, for callers that cannot
+ * allocate device memory: code running inside a host application that owns
+ * every device allocation (e.g. a plugin given a fixed memory plan), or
+ * loops that must avoid cudaMalloc/cudaFree because those can synchronise
+ * the device.  The paper has no counterpart; it is a deployment variant.
+ * Same arguments, results and errors as vsa_coarse_select, except:
+ *   - the scratch is a 64 MiB device array inside the library, reserved on
+ *     every GPU that loads the library until the process exits; problems with
+ *     16 * B * heads * ncubes * D > 64 MiB return VSA_ERR_UNSUPPORTED;
+ *   - the first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture;
+ *   - all calls on a device share the array, so calls whose kernels overlap
+ *     on the GPU race and must be serialised by the caller;
+ *   - no cudaMalloc, cudaFree or other allocating routine is called.
+ */
+vsa_status vsa_coarse_select_noalloc(const void* qt, const void* kt, const int32_t* vbs, int32_t B,
+                                     int32_t ncubes, int32_t heads, int32_t D, int32_t topk,
+                                     float sm_scale, int32_t* topk_idx, vsa_stream_t stream);
+
+/*
  * Fine stage: non-causal block-sparse attention ([WAN-VSA] Operator contract;
  * [VSA-AMD] Stage 2: Fine Computation, Kernel Architecture, Sparse Traversal).
  * For every (b, head, query cube i) and each of its 64 rows r (padding rows
