@@ -24,6 +24,8 @@ cudaError_t launch_validate(const int32_t* idx, const int32_t* vbs, int rows, in
 int validate_max_cubes();
 cudaError_t launch_debug_wait(long long limit_ns, int32_t* result, unsigned int* err, cudaStream_t stream);
 int fine_smem_bytes();
+int fine_max_topk();
+int fine_max_cubes();
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                         const int32_t* vbs, int B, int ncubes, int heads, int D, int topk, float sm_scale,
                         void* out, float* lse, unsigned int* err, int num_sms, cudaStream_t stream);
@@ -165,6 +167,7 @@ vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt, c
         (int64_t)B * heads * ncubes >= ((int64_t)1 << 31))
         return VSA_ERR_UNSUPPORTED;
     if (heads > 65535) return VSA_ERR_UNSUPPORTED;  // TMA box coordinate range
+    if (topk > fine_max_topk() || ncubes > fine_max_cubes()) return VSA_ERR_UNSUPPORTED;
     if (!aligned16(qt) || !aligned16(kt) || !aligned16(vt) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(vbs) & 3u) ||
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))

@@ -9,25 +9,32 @@
 // and Sparse Traversal: walk the query block's K/V block list only).
 //
 // sm_103a design (5th-generation tensor cores, TMEM, TMA):
-//  * Work unit = one (b, head, query cube).  Persistent grid, one CTA per SM,
-//    units dealt round-robin in head-major order so one head's K/V stays in L2.
-//  * A step processes TWO selected key cubes (128 keys) at once in transposed
-//    form, so every MMA is M = 128 with no wasted rows:
-//        S^T[128 keys x 64 q]  = K_pair[128 x D] . Q^T          (tcgen05, TMEM)
-//        O^T[D x 64 q]        += V_pair^T[D x 128] . P^T[128 x 64] (tcgen05, TMEM)
-//    An odd last cube runs as a half step (PV over 64 keys).
-//  * Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer
-//    (also owns TMEM), warps 2..9 = softmax.  Each softmax thread owns one key
-//    row of S^T (its TMEM lane) and 32 of the 64 query columns.
-//  * Softmax per column keeps a running max m in log2 units.  The max is set
-//    exactly from the first step of a unit; later steps only re-reduce (and
-//    rescale O^T and the partial sums) when some logit exceeds m by more than
-//    kRescaleThreshold, so the usual step needs no cross-thread reduction.
-//    exp2 arguments are then <= the threshold: no overflow for logits of any
-//    finite size.
-//  * Padded key slots (slot >= vbs[j]) get probability 0; P^T is written as
-//    bf16 into a 128-byte-swizzled shared-memory tile that is the B operand
-//    of the PV MMA.
+//  * A work unit is a PAIR of query cubes (2p, 2p+1) of one (batch, head):
+//    128 query rows, one per TMEM lane.  It walks the union of the two cubes'
+//    selected key cubes, two key cubes (128 keys) per step:
+//        S[128 q x 128 keys]  = Q_pair . K_pair^T      (A = Q in TMEM)
+//        O[128 q x D]        += P . V_pair            (A = P in TMEM)
+//    Both MMAs are M = 128, N = 128 (full tensor-core rate; an M x 64 MMA runs
+//    at half rate), and only the B operands (K, V) are read from shared
+//    memory, which keeps shared-memory bandwidth to about half of its peak.
+//    Query rows of a cube that did not select a key cube get probability 0
+//    for it, so each row attends exactly its own selection.
+//  * Persistent grid, one CTA per SM, units dealt round-robin in head-major
+//    order so one head's K/V stays in L2.
+//  * Warp roles (384 threads): warp 0 builds each unit's union list (sorted,
+//    with membership bits and vbs) and is the TMA producer of K; warp 1 issues
+//    all MMAs and owns TMEM; warp 2 is the TMA producer of V; warps 4..11 run
+//    the softmax and stage Q into TMEM.  A query row is shared by two threads
+//    (two warps on the same TMEM lane quarter), one per key cube of the step;
+//    they exchange their row maxima through shared memory with a 64-thread
+//    named barrier, so the running max, the sum and the lazy rescale of the
+//    row's O need no wider synchronisation.
+//  * TMEM (512 columns): S double buffer [0,128) [128,256) (P in bf16 is
+//    written over the first 64 columns of its S buffer), O [256, 384), Q double
+//    buffer [384, 448) [448, 512).
+//  * Running max kept in log2 units; O and the sum are rescaled only when a
+//    row's max grows by more than kRescaleThreshold, so exp2 arguments stay
+//    <= the threshold and logits of any finite size are safe.
 //  * Every wait is bounded; a wait that runs out raises a CTA abort flag and
 //    the device error word, and each role winds down without deadlock.
 #include <cuda_bf16.h>
@@ -39,147 +46,249 @@ namespace vsa {
 
 namespace {
 
-constexpr int kStages = 3;            // key/value pair stages in the TMA ring
-constexpr int kThreads = 320;         // 10 warps
+constexpr int kKStages = 3;           // K pair slots (QK operand B)
+constexpr int kVStages = 3;           // V pair slots (PV operand B)
 constexpr int kSoftmaxWarps = 8;
-constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr float kRescaleThreshold = 10.0f;  // log2 units
+constexpr int kFirstSoftmaxWarp = 4;
+constexpr int kThreads = (kFirstSoftmaxWarp + kSoftmaxWarps) * 32;  // 8 warps
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kIdxPerLane = 8;        // producer keeps 256 indices in registers
+constexpr int kMaxTopk = 512;
+constexpr int kMaxUnion = 2 * kMaxTopk;
+constexpr int kMaxCubes = 8192;
+constexpr int kBitmapWords = kMaxCubes / 32;
+
+// TMEM columns.
+constexpr int kTmemS = 0;    // two S buffers of 128 columns
+constexpr int kTmemO = 256;  // O accumulator (D columns)
+constexpr int kTmemQ = 384;  // two Q buffers of 64 columns (bf16 pairs)
 
 // Shared-memory layout (bytes from a 1024-aligned base).
 constexpr int kChunkRows64 = 64 * 128;           // 64 rows x 128 B   = 8 KB
 constexpr int kChunkRows128 = 128 * 128;         // 128 rows x 128 B  = 16 KB
-constexpr int kOffQ = 0;                         // [2 chunks][64 q][128 B]
-constexpr int kOffK = kOffQ + 2 * kChunkRows64;  // [stage][2 chunks][128 keys][128 B]
-constexpr int kStageBytes = 2 * kChunkRows128;   // 32 KB per tensor per stage
-constexpr int kOffV = kOffK + kStages * kStageBytes;
-constexpr int kOffP = kOffV + kStages * kStageBytes;  // [128 keys][128 B]
-constexpr int kOffMisc = kOffP + kChunkRows128;
+constexpr int kPairBytes = 2 * kChunkRows128;    // one tensor for a cube pair: 32 KB
+constexpr int kOffK = 0;                         // [slot][2 chunks][128 keys][128 B]
+constexpr int kOffV = kOffK + kKStages * kPairBytes;
+constexpr int kOffList = kOffV + kVStages * kPairBytes;          // [2][kMaxUnion] packed entries
+constexpr int kOffBitmap = kOffList + 2 * kMaxUnion * 4;         // [2][kBitmapWords]
+constexpr int kOffMisc = kOffBitmap + 2 * kBitmapWords * 4;
+
+// Union-list entry: cube id (bits 0..15), vbs (bits 16..23), membership
+// (bit 24: selected by the first query cube, bit 25: by the second).
+__device__ __forceinline__ int entry_cube(uint32_t e) { return (int)(e & 0xFFFFu); }
+__device__ __forceinline__ int entry_vbs(uint32_t e) { return (int)((e >> 16) & 0xFFu); }
+__device__ __forceinline__ uint32_t entry_mask(uint32_t e) { return (e >> 24) & 3u; }
 
 struct __align__(16) Misc {
-    uint64_t kv_full[kStages];
-    uint64_t kv_empty[kStages];
-    uint64_t q_full;
-    uint64_t q_empty;
+    uint64_t k_full[kKStages];
+    uint64_t k_empty[kKStages];
+    uint64_t v_full[kVStages];
+    uint64_t v_empty[kVStages];
     uint64_t s_full[2];
-    uint64_t p_full;
-    uint64_t o_done;
+    uint64_t p_full[2];
+    uint64_t pv_done[2];
+    uint64_t q_full[2];
+    uint64_t list_full[2];
+    uint64_t list_empty[2];
     uint64_t drain;
-    int4 info[kStages];          // per stage: cube a, vbs a, cube b (-1 = none), vbs b
-    float m[64];                 // running max per query column (log2 units)
-    float mb[64];                // exp base: m, or 0 while m = -inf
-    float alpha[64];             // rescale factor of the last update
-    float red[kSoftmaxWarps][32];
+    int list_count[2];
+    float xmax[2][2][128];        // [step parity][key half][row]: row maxima exchanged by thread pairs
+    float xsum[2][128];           // [key half][row]: partial row sums for the epilogue
     uint32_t tmem_base;
     int abort_flag;
-    int m_neg_inf;               // some column still has m = -inf
 };
 
 constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc);
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
-
 static_assert(kSmemAlloc <= 232448, "fine kernel shared memory exceeds the sm_103a limit");
 
 struct FineParams {
     const int32_t* topk_idx;
     const int32_t* vbs;
-    __nv_bfloat16* out;  // unused type-wise, raw bf16 bits written
+    const uint4* q;      // tiled q rows (for staging Q into TMEM)
+    __nv_bfloat16* out;
     float* lse;
     unsigned int* err;
-    int B, N, heads, D, topk, nsteps;
-    int num_units;
-    float scale_log2;  // sm_scale * log2(e)
+    int B, N, heads, D, topk;
+    int npairs;          // ceil(N / 2)
+    int num_units;       // B * heads * npairs
+    float scale_log2;    // sm_scale * log2(e)
 };
+
+__device__ __forceinline__ void unit_coords(int u, const FineParams& p, int& b, int& h, int& pair) {
+    pair = u % p.npairs;
+    const int bh = u / p.npairs;
+    h = bh % p.heads;
+    b = bh / p.heads;
+}
+
+// Builds the sorted union of the two query cubes' selections (one warp).
+__device__ int build_union(const FineParams& p, int u, uint32_t* list, uint32_t* bm0, uint32_t* bm1, int lane) {
+    int b, h, pair;
+    unit_coords(u, p, b, h, pair);
+    const int N = p.N, k = p.topk;
+    const int nwords = (N + 31) >> 5;
+    const int i0 = 2 * pair, i1 = 2 * pair + 1;
+    for (int w = lane; w < nwords; w += 32) {
+        bm0[w] = 0u;
+        bm1[w] = 0u;
+    }
+    __syncwarp();
+    const int32_t* r0 = p.topk_idx + (((size_t)b * p.heads + h) * N + i0) * (size_t)k;
+    for (int e = lane; e < k; e += 32) {
+        const int j = __ldg(r0 + e);
+        atomicOr(&bm0[j >> 5], 1u << (j & 31));
+    }
+    if (i1 < N) {
+        const int32_t* r1 = r0 + k;
+        for (int e = lane; e < k; e += 32) {
+            const int j = __ldg(r1 + e);
+            atomicOr(&bm1[j >> 5], 1u << (j & 31));
+        }
+    }
+    __syncwarp();
+    int pos = 0;
+    for (int w0 = 0; w0 < nwords; w0 += 32) {
+        const int w = w0 + lane;
+        const uint32_t a0 = w < nwords ? bm0[w] : 0u;
+        const uint32_t a1 = w < nwords ? bm1[w] : 0u;
+        uint32_t bits = a0 | a1;
+        const int c = __popc(bits);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int q = pos + incl - c;
+        while (bits) {
+            const int bt = __ffs(bits) - 1;
+            bits &= bits - 1u;
+            const int j = w * 32 + bt;
+            const uint32_t mask = ((a0 >> bt) & 1u) | (((a1 >> bt) & 1u) << 1);
+            const int vb = min(max(__ldg(p.vbs + j), 0), kCubeTokens);
+            list[q++] = (uint32_t)j | ((uint32_t)vb << 16) | (mask << 24);
+        }
+        pos += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    __syncwarp();
+    return pos;
+}
+
+// Issues the TMA copies of one cube pair (rows of cubes ja and jb; jb < 0:
+// single cube) of tensor `tm` into a 32 KB pair slot.
+__device__ __forceinline__ void load_pair(const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row_a, int row_b,
+                                          int h, int nchunks, int D, uint64_t policy) {
+    mbar_arrive_expect_tx(bar, (uint32_t)((row_b >= 0 ? 2 : 1) * kCubeTokens * D * 2));
+    for (int c = 0; c < nchunks; ++c) tma_load_3d(dst + c * kChunkRows128, tm, bar, c * 64, h, row_a, policy);
+    if (row_b >= 0)
+        for (int c = 0; c < nchunks; ++c)
+            tma_load_3d(dst + c * kChunkRows128 + kChunkRows64, tm, bar, c * 64, h, row_b, policy);
+}
+
+// Waits (bounded) until the last copy issued into each ring slot has landed.
+template <int kSlots>
+__device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t issued, volatile int* abort_flag,
+                                           unsigned int* err) {
+    for (int s = 0; s < kSlots; ++s) {
+        if ((uint32_t)s >= issued) continue;
+        const uint32_t last = issued - 1 - ((issued - 1 - s) % kSlots);  // last step that used slot s
+        mbar_wait_bounded(smem_u32(&full[s]), (last / kSlots) & 1, abort_flag, err, kWaitLimitNs);
+    }
+}
+
+// Softmax threads: copy half `hf` of this thread's Q row (or zeros) into TMEM
+// Q buffer qb (D/2 elements = D/4 32-bit columns; D = 64 has one half only).
+__device__ __forceinline__ void stage_q(const FineParams& p, int u, int row_in_pair, uint32_t t_lane, int qb,
+                                        int hf) {
+    int b, h, pair;
+    unit_coords(u, p, b, h, pair);
+    const int i = 2 * pair + (row_in_pair >> 6);
+    const int D = p.D;
+    const int words = D / 2;  // 32-bit columns of a full row
+    uint32_t w[32];
+    for (int c0 = hf * 32; c0 < words && c0 < hf * 32 + 32; c0 += 32) {
+        if (i < p.N) {
+            const size_t row = (size_t)b * p.N * kCubeTokens + (size_t)i * kCubeTokens + (row_in_pair & 63);
+            const uint4* src = p.q + (row * p.heads + h) * (size_t)(D / 8) + c0 / 4;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint4 x = __ldg(src + v);
+                w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < 32; ++v) w[v] = 0u;
+        }
+        tmem_st32(t_lane + kTmemQ + qb * 64 + c0, w);
+    }
+    tmem_wait_st();
+}
 
 __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
-__device__ __forceinline__ bool named_red_or(int id, int n, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, %2, %3, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
-// Reduce 32 per-thread column values over the 32 lanes of a warp; lane L
-// returns the reduction of column L.
-template <bool kMax>
-__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const bool up = (lane & off) != 0;
-#pragma unroll
-        for (int j = 0; j < off; ++j) {
-            const float send = up ? v[j] : v[j + off];
-            const float keep = up ? v[j + off] : v[j];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-            v[j] = kMax ? fmaxf(keep, recv) : keep + recv;
-        }
-    }
-    return v[0];
-}
-
-__device__ __forceinline__ void unit_coords(int u, int N, int heads, int& b, int& h, int& i) {
-    i = u % N;
-    const int bh = u / N;
-    h = bh % heads;
-    b = bh / heads;
-}
-
+template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
-    fine_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, FineParams p) {
+    fine_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    FineParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
+    uint32_t* lists = reinterpret_cast<uint32_t*>(smem + kOffList);
+    uint32_t* bitmaps = reinterpret_cast<uint32_t*>(smem + kOffBitmap);
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort_flag = &ms.abort_flag;
 
-    const int D = p.D;
+    constexpr int D = kD;
     const int nchunks = D / 64;
     const int s_pad = p.N * kCubeTokens;
+    const int my_units = blockIdx.x < p.num_units ? (p.num_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
     // ---------------------------------------------------------------- setup
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&ms.kv_full[s]), 1);
-            mbar_init(smem_u32(&ms.kv_empty[s]), 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(smem_u32(&ms.k_full[s]), 1);
+            mbar_init(smem_u32(&ms.k_empty[s]), 1);
         }
-        mbar_init(smem_u32(&ms.q_full), 1);
-        mbar_init(smem_u32(&ms.q_empty), 1);
-        mbar_init(smem_u32(&ms.s_full[0]), 1);
-        mbar_init(smem_u32(&ms.s_full[1]), 1);
-        mbar_init(smem_u32(&ms.p_full), kSoftmaxWarps);
-        mbar_init(smem_u32(&ms.o_done), 1);
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(smem_u32(&ms.v_full[s]), 1);
+            mbar_init(smem_u32(&ms.v_empty[s]), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&ms.s_full[s]), 1);
+            mbar_init(smem_u32(&ms.p_full[s]), kSoftmaxWarps);
+            mbar_init(smem_u32(&ms.pv_done[s]), 1);
+            mbar_init(smem_u32(&ms.q_full[s]), kSoftmaxWarps);
+            mbar_init(smem_u32(&ms.list_full[s]), 1);
+            mbar_init(smem_u32(&ms.list_empty[s]), 1 + 1 + kSoftmaxWarps);  // V producer, MMA, softmax warps
+        }
         mbar_init(smem_u32(&ms.drain), 1);
         ms.abort_flag = 0;
-        ms.m_neg_inf = 0;
         fence_barrier_init();
     }
-    // Zero the K/V stages once: half steps read rows no TMA wrote, and for
-    // D = 64 the second V chunk must stay zero.
+    // Zero the K/V rings once: a single-cube step's MMA reads rows no copy wrote.
     {
         int4* z = reinterpret_cast<int4*>(smem + kOffK);
-        const int n16 = 2 * kStages * kStageBytes / 16;
+        const int n16 = (kKStages + kVStages) * kPairBytes / 16;
         for (int e = threadIdx.x; e < n16; e += kThreads) z[e] = make_int4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&ms.tmem_base), 256);
+        tmem_alloc(smem_u32(&ms.tmem_base), 512);
         tmem_relinquish();
     }
     if (threadIdx.x == 0) {
-        tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
     }
@@ -188,370 +297,335 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ms.tmem_base;
 
-    const int nsteps = p.nsteps;
-    const int k = p.topk;
-
     if (warp == 0) {
-        // ============================================================ producer
-        const uint64_t pol_kv = l2_policy_evict_last();
-        const uint64_t pol_q = l2_policy_evict_first();
+        // ================================ union lists + TMA producer of K
+        const uint64_t pol = l2_policy_evict_last();
         uint32_t g = 0;
-        int ucount = 0;
-        uint32_t last_g[kStages];
-        for (int s = 0; s < kStages; ++s) last_g[s] = 0xFFFFFFFFu;
-        bool q_issued = false;
         bool ok = true;
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ucount) {
-            int b, h, i;
-            unit_coords(u, p.N, p.heads, b, h, i);
-            if (ucount > 0) {
-                ok = mbar_wait_bounded(smem_u32(&ms.q_empty), (ucount - 1) & 1, abort_flag, p.err,
+        for (int ul = 0; ul < my_units && ok; ++ul) {
+            const int u = blockIdx.x + ul * gridDim.x;
+            const int lb = ul & 1;
+            if (ul >= 2)
+                ok = mbar_wait_bounded(smem_u32(&ms.list_empty[lb]), ((ul >> 1) + 1) & 1, abort_flag, p.err,
                                        kWaitLimitNs);
-                if (!ok) break;
-            }
-            const int row0 = b * s_pad + i * kCubeTokens;
+            if (!ok) break;
+            uint32_t* list = lists + lb * kMaxUnion;
+            const int count = build_union(p, u, list, bitmaps, bitmaps + kBitmapWords, lane);
             if (lane == 0) {
-                const uint32_t qbar = smem_u32(&ms.q_full);
-                mbar_arrive_expect_tx(qbar, (uint32_t)(kCubeTokens * D * 2));
-                for (int c = 0; c < nchunks; ++c)
-                    tma_load_3d(sbase + kOffQ + c * kChunkRows64, &tm_q, qbar, c * 64, h, row0, pol_q);
+                ms.list_count[lb] = count;
+                mbar_arrive(smem_u32(&ms.list_full[lb]));
             }
-            q_issued = true;
-            const int32_t* idx_row = p.topk_idx + (((size_t)b * p.heads + h) * p.N + i) * (size_t)k;
-            int idx_reg[kIdxPerLane], vbs_reg[kIdxPerLane];
-            for (int t = 0; t < nsteps && ok; ++t) {
-                const int e0 = 2 * t;
-                if ((e0 & (32 * kIdxPerLane - 1)) == 0) {
-                    // (Re)load the next 256 indices of the row and their vbs.
-#pragma unroll
-                    for (int s = 0; s < kIdxPerLane; ++s) {
-                        const int e = e0 + s * 32 + lane;
-                        idx_reg[s] = e < k ? __ldg(idx_row + e) : -1;
-                        vbs_reg[s] = idx_reg[s] >= 0 ? __ldg(p.vbs + idx_reg[s]) : 0;
-                    }
-                }
-                const int stage = g % kStages;
-                if (g >= (uint32_t)kStages) {
-                    ok = mbar_wait_bounded(smem_u32(&ms.kv_empty[stage]), ((g / kStages) + 1) & 1,
-                                           abort_flag, p.err, kWaitLimitNs);
+            int b, h, pair;
+            unit_coords(u, p, b, h, pair);
+            const int nst = (count + 1) >> 1;
+            for (int t = 0; t < nst; ++t, ++g) {
+                const int slot = g % kKStages;
+                if (g >= (uint32_t)kKStages) {
+                    ok = mbar_wait_bounded(smem_u32(&ms.k_empty[slot]), ((g / kKStages) + 1) & 1, abort_flag,
+                                           p.err, kWaitLimitNs);
                     if (!ok) break;
-                }
-                // Fetch entries e0 and e0 + 1 from their owner lanes.
-                int ja = -1, va = 0, jb = -1, vb = 0;
-                {
-                    const int ea = e0 & (32 * kIdxPerLane - 1), eb = ea + 1;
-                    int xa = 0, ya = 0, xb = 0, yb = 0;
-#pragma unroll
-                    for (int s = 0; s < kIdxPerLane; ++s) {
-                        if ((ea >> 5) == s) { xa = idx_reg[s]; ya = vbs_reg[s]; }
-                        if ((eb >> 5) == s) { xb = idx_reg[s]; yb = vbs_reg[s]; }
-                    }
-                    ja = __shfl_sync(0xffffffffu, xa, ea & 31);
-                    va = __shfl_sync(0xffffffffu, ya, ea & 31);
-                    jb = __shfl_sync(0xffffffffu, xb, eb & 31);
-                    vb = __shfl_sync(0xffffffffu, yb, eb & 31);
-                    if (e0 + 1 >= k) { jb = -1; vb = 0; }
                 }
                 if (lane == 0) {
-                    ms.info[stage] = make_int4(ja, va, jb, vb);
-                    const uint32_t fbar = smem_u32(&ms.kv_full[stage]);
-                    const uint32_t bytes = (uint32_t)((jb >= 0 ? 2 : 1) * 2 * kCubeTokens * D * 2);
-                    mbar_arrive_expect_tx(fbar, bytes);
-                    const uint32_t kst = sbase + kOffK + stage * kStageBytes;
-                    const uint32_t vst = sbase + kOffV + stage * kStageBytes;
-                    const int ra = b * s_pad + ja * kCubeTokens;
-                    for (int c = 0; c < nchunks; ++c) {
-                        tma_load_3d(kst + c * kChunkRows128, &tm_k, fbar, c * 64, h, ra, pol_kv);
-                        tma_load_3d(vst + c * kChunkRows128, &tm_v, fbar, c * 64, h, ra, pol_kv);
-                    }
-                    if (jb >= 0) {
-                        const int rb = b * s_pad + jb * kCubeTokens;
-                        for (int c = 0; c < nchunks; ++c) {
-                            tma_load_3d(kst + c * kChunkRows128 + kChunkRows64, &tm_k, fbar, c * 64, h, rb,
-                                        pol_kv);
-                            tma_load_3d(vst + c * kChunkRows128 + kChunkRows64, &tm_v, fbar, c * 64, h, rb,
-                                        pol_kv);
-                        }
-                    }
+                    const int ra = b * s_pad + entry_cube(list[2 * t]) * kCubeTokens;
+                    const int rb = 2 * t + 1 < count ? b * s_pad + entry_cube(list[2 * t + 1]) * kCubeTokens : -1;
+                    load_pair(&tm_k, sbase + kOffK + slot * kPairBytes, smem_u32(&ms.k_full[slot]), ra, rb, h,
+                              nchunks, D, pol);
                 }
-                last_g[stage] = g;
-                ++g;
+                __syncwarp();
             }
         }
-        // Drain: every issued copy must land before the CTA exits.
-        for (int s = 0; s < kStages; ++s)
-            if (last_g[s] != 0xFFFFFFFFu)
-                mbar_wait_bounded(smem_u32(&ms.kv_full[s]), (last_g[s] / kStages) & 1, abort_flag, p.err,
-                                  kWaitLimitNs);
-        if (q_issued)
-            mbar_wait_bounded(smem_u32(&ms.q_full), (ucount - 1) & 1, abort_flag, p.err, kWaitLimitNs);
+        drain_ring<kKStages>(ms.k_full, g, abort_flag, p.err);
+    } else if (warp == 2) {
+        // ========================================== TMA producer of V
+        const uint64_t pol = l2_policy_evict_last();
+        uint32_t g = 0;
+        bool ok = true;
+        for (int ul = 0; ul < my_units && ok; ++ul) {
+            const int u = blockIdx.x + ul * gridDim.x;
+            const int lb = ul & 1;
+            ok = mbar_wait_bounded(smem_u32(&ms.list_full[lb]), (ul >> 1) & 1, abort_flag, p.err, kWaitLimitNs);
+            if (!ok) break;
+            const uint32_t* list = lists + lb * kMaxUnion;
+            const int count = ms.list_count[lb];
+            int b, h, pair;
+            unit_coords(u, p, b, h, pair);
+            const int nst = (count + 1) >> 1;
+            for (int t = 0; t < nst; ++t, ++g) {
+                const int slot = g % kVStages;
+                if (g >= (uint32_t)kVStages) {
+                    ok = mbar_wait_bounded(smem_u32(&ms.v_empty[slot]), ((g / kVStages) + 1) & 1, abort_flag,
+                                           p.err, kWaitLimitNs);
+                    if (!ok) break;
+                }
+                if (lane == 0) {
+                    const int ra = b * s_pad + entry_cube(list[2 * t]) * kCubeTokens;
+                    const int rb = 2 * t + 1 < count ? b * s_pad + entry_cube(list[2 * t + 1]) * kCubeTokens : -1;
+                    load_pair(&tm_v, sbase + kOffV + slot * kPairBytes, smem_u32(&ms.v_full[slot]), ra, rb, h,
+                              nchunks, D, pol);
+                }
+                __syncwarp();
+            }
+            if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[lb]));
+        }
+        drain_ring<kVStages>(ms.v_full, g, abort_flag, p.err);
     } else if (warp == 1) {
         // ============================================================ MMA issuer
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 64, 0, 0);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 64, 1, 1);
-        const uint32_t t_s0 = tmem;          // S^T buffers: columns [0, 64) and [64, 128)
-        const uint32_t t_o = tmem + 128;     // O^T: columns [128, 192)
-        uint32_t g = 0;
-        int ucount = 0;
-        bool ok = true;
-        // Issues QK^T for global step gg (Q resident, K/V of stage landed).
-        // release_q: gg is the last step of its unit, so the Q buffer is free
-        // once this MMA completes.
-        auto issue_qk = [&](uint32_t gg, bool release_q) {
-            const int stage = gg % kStages;
-            const uint32_t kst = sbase + kOffK + stage * kStageBytes;
-            const uint32_t d_tmem = t_s0 + (gg & 1) * 64;
-            if (lane == 0) {
+        // One lane issues every MMA, in the order QK(0), then per step g:
+        // QK(g + 1), PV(g).  QK(g + 2) reuses the TMEM columns that PV(g) reads
+        // P from; MMAs issued by one thread execute in issue order, so the
+        // reuse needs no extra wait.  Descriptors are precomputed; each MMA
+        // adds a constant to the start-address field of the low word (no
+        // carry: shared addresses are below 256 KB).
+        if (lane == 0 && my_units > 0) {
+            const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
+            const uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
+            const uint32_t hi = (uint32_t)(smem_desc_sw128(0, 16, 1024) >> 32);  // SBO, version, swizzle
+            const uint32_t lo_k = (uint32_t)smem_desc_sw128(sbase + kOffK, 16, 1024);
+            const uint32_t lo_v = (uint32_t)smem_desc_sw128(sbase + kOffV, kChunkRows128, 1024);
+            constexpr int ksteps_qk = D / 16;
+            bool ok = true;
+            uint32_t g = 0;    // next PV step (global)
+            uint32_t gq = 0;   // next QK step (global)
+            int ul_q = 0, t_q = 0, cnt_q = 0;  // unit / step cursor of the QK stream
+            int ul_p = 0, t_p = 0, cnt_p = 0;  // unit / step cursor of the PV stream
+            // Count of the list of local unit ul (waits for the list).
+            auto list_count = [&](int ul) -> int {
+                if (!mbar_wait_bounded_1(smem_u32(&ms.list_full[ul & 1]), (ul >> 1) & 1, abort_flag, p.err,
+                                         kWaitLimitNs))
+                    return -1;
+                return ms.list_count[ul & 1];
+            };
+            auto issue_qk = [&]() -> bool {
+                if (t_q == 0) {
+                    cnt_q = list_count(ul_q);
+                    if (cnt_q < 0) return false;
+                    if (!mbar_wait_bounded_1(smem_u32(&ms.q_full[ul_q & 1]), (ul_q >> 1) & 1, abort_flag, p.err,
+                                             kWaitLimitNs))
+                        return false;
+                }
+                const int slot = gq % kKStages;
+                if (!mbar_wait_bounded_1(smem_u32(&ms.k_full[slot]), (gq / kKStages) & 1, abort_flag, p.err,
+                                         kWaitLimitNs))
+                    return false;
+                const uint32_t b0 = lo_k + ((uint32_t)(slot * kPairBytes) >> 4);
+                const uint32_t a0 = tmem + kTmemQ + (ul_q & 1) * 64;
+                const uint32_t d_tmem = tmem + kTmemS + (gq & 1) * 128;
                 tc_fence_after();
-                int n = 0;
-                for (int c = 0; c < nchunks; ++c)
-                    for (int kk = 0; kk < 4; ++kk, ++n) {
-                        const uint64_t a = smem_desc_sw128(kst + c * kChunkRows128 + kk * 32, 16, 1024);
-                        const uint64_t bq = smem_desc_sw128(sbase + kOffQ + c * kChunkRows64 + kk * 32, 16, 1024);
-                        mma_ss(d_tmem, a, bq, idesc_qk, n > 0);
-                    }
-                mma_commit(smem_u32(&ms.s_full[gg & 1]));
-                if (release_q) mma_commit(smem_u32(&ms.q_empty));
-            }
-            __syncwarp();
-        };
-        const int first_u = blockIdx.x;
-        if (first_u < p.num_units) {
-            ok = mbar_wait_bounded(smem_u32(&ms.q_full), 0, abort_flag, p.err, kWaitLimitNs) &&
-                 mbar_wait_bounded(smem_u32(&ms.kv_full[0]), 0, abort_flag, p.err, kWaitLimitNs);
-            if (ok) issue_qk(0, nsteps == 1);
-        }
-        for (int u = first_u; u < p.num_units && ok; u += gridDim.x, ++ucount) {
-            const bool has_next_unit = u + (int)gridDim.x < p.num_units;
-            for (int t = 0; t < nsteps && ok; ++t) {
-                const bool last_in_unit = (t + 1 == nsteps);
-                const bool next_exists = !last_in_unit || has_next_unit;
-                // Within a unit the next QK^T goes first (it feeds the next
-                // softmax step); at a unit boundary the PV goes first.
-                if (next_exists && !last_in_unit) {
-                    const uint32_t gn = g + 1;
-                    ok = mbar_wait_bounded(smem_u32(&ms.kv_full[gn % kStages]), (gn / kStages) & 1,
-                                           abort_flag, p.err, kWaitLimitNs);
-                    if (!ok) break;
-                    issue_qk(gn, t + 2 == nsteps);
+#pragma unroll
+                for (int kk = 0; kk < ksteps_qk; ++kk)
+                    mma_ts_lohi(d_tmem, a0 + kk * 8, b0 + (((kk >> 2) * kChunkRows128 + (kk & 3) * 32) >> 4), hi,
+                                idesc_qk, kk > 0);
+                mma_commit(smem_u32(&ms.s_full[gq & 1]));
+                mma_commit(smem_u32(&ms.k_empty[slot]));
+                ++gq;
+                if (++t_q == (cnt_q + 1) >> 1) {
+                    t_q = 0;
+                    ++ul_q;
                 }
-                ok = mbar_wait_bounded(smem_u32(&ms.p_full), g & 1, abort_flag, p.err, kWaitLimitNs);
-                if (!ok) break;
-                {
-                    const int stage = g % kStages;
-                    const uint32_t vst = sbase + kOffV + stage * kStageBytes;
-                    const bool half = (2 * t + 1 >= k);
-                    const int ksteps = half ? 4 : 8;
-                    if (lane == 0) {
-                        tc_fence_after();
-                        for (int kk = 0; kk < ksteps; ++kk) {
-                            const uint64_t a = smem_desc_sw128(vst + kk * 2048, kChunkRows128, 1024);
-                            const uint64_t bp = smem_desc_sw128(sbase + kOffP + kk * 2048, kChunkRows128, 1024);
-                            mma_ss(t_o, a, bp, idesc_pv, (t > 0 || kk > 0));
-                        }
-                        mma_commit(smem_u32(&ms.o_done));
-                        mma_commit(smem_u32(&ms.kv_empty[stage]));
-                    }
-                    __syncwarp();
+                return true;
+            };
+            auto issue_pv = [&]() -> bool {
+                if (t_p == 0) {
+                    cnt_p = list_count(ul_p);
+                    if (cnt_p < 0) return false;
                 }
-                if (next_exists && last_in_unit) {
-                    const uint32_t gn = g + 1;
-                    ok = mbar_wait_bounded(smem_u32(&ms.q_full), (ucount + 1) & 1, abort_flag, p.err,
-                                           kWaitLimitNs) &&
-                         mbar_wait_bounded(smem_u32(&ms.kv_full[gn % kStages]), (gn / kStages) & 1,
-                                           abort_flag, p.err, kWaitLimitNs);
-                    if (!ok) break;
-                    issue_qk(gn, nsteps == 1);
+                const int slot = g % kVStages;
+                if (!mbar_wait_bounded_1(smem_u32(&ms.p_full[g & 1]), (g >> 1) & 1, abort_flag, p.err,
+                                         kWaitLimitNs) ||
+                    !mbar_wait_bounded_1(smem_u32(&ms.v_full[slot]), (g / kVStages) & 1, abort_flag, p.err,
+                                         kWaitLimitNs))
+                    return false;
+                const uint32_t b0 = lo_v + ((uint32_t)(slot * kPairBytes) >> 4);
+                const uint32_t a0 = tmem + kTmemS + (g & 1) * 128;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts_lohi(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv,
+                                (t_p > 0 || kk > 0));
+                if (2 * t_p + 1 < cnt_p) {  // the second cube of the step (a single-cube step has 64 keys)
+#pragma unroll
+                    for (int kk = 4; kk < 8; ++kk)
+                        mma_ts_lohi(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv, 1u);
+                }
+                mma_commit(smem_u32(&ms.pv_done[g & 1]));
+                mma_commit(smem_u32(&ms.v_empty[slot]));
+                if (++t_p == (cnt_p + 1) >> 1) {
+                    // The MMA side is done with this unit's list.
+                    mbar_arrive(smem_u32(&ms.list_empty[ul_p & 1]));
+                    t_p = 0;
+                    ++ul_p;
                 }
                 ++g;
+                return true;
+            };
+            ok = issue_qk();
+            while (ok && ul_p < my_units) {
+                if (ul_q < my_units) ok = issue_qk();
+                if (ok) ok = issue_pv();
             }
+            // Drain: all issued MMAs complete before TMEM is released.
+            mma_commit(smem_u32(&ms.drain));
+            mbar_wait_bounded_1(smem_u32(&ms.drain), 0, abort_flag, p.err, kWaitLimitNs);
         }
-        // Drain: all issued MMAs complete before TMEM is released.
-        if (lane == 0) mma_commit(smem_u32(&ms.drain));
         __syncwarp();
-        mbar_wait_bounded(smem_u32(&ms.drain), 0, abort_flag, p.err, kWaitLimitNs);
-    } else {
+    } else if (warp >= kFirstSoftmaxWarp) {
         // ============================================================ softmax
-        const int sw = warp - 2;            // 0..7
-        const int quarter = warp & 3;       // TMEM lane quarter this warp may access
-        const int half = sw >> 2;           // query columns [32*half, 32*half + 32)
-        const int key = quarter * 32 + lane;  // S^T row = key slot in the pair (0..127)
-        const int cube_sel = key >> 6;      // 0: first cube of the pair, 1: second
-        const int slot = key & 63;
-        const int col0 = half * 32;
+        const int sw = warp - kFirstSoftmaxWarp;  // 0..7
+        const int quarter = warp & 3;             // TMEM lane quarter
+        const int hf = sw >> 2;                   // key half of the step: cube 2t + hf
+        const int r = quarter * 32 + lane;        // query row of the pair (0..127)
+        const uint32_t my_bit = 1u << (r >> 6);   // membership bit of this row's cube
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int dh = D / 2;                     // O columns this thread owns: [hf * dh, hf * dh + dh)
         const float c2 = p.scale_log2;
         const float ninf = -INFINITY;
         bool ok = true;
         uint32_t g = 0;
-        float lpart[32];
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-            int b, h, i;
-            unit_coords(u, p.N, p.heads, b, h, i);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) lpart[q] = 0.f;
-            for (int t = 0; t < nsteps; ++t, ++g) {
-                const int stage = g % kStages;
-                const uint32_t sbuf = g & 1;
-                if (ok) ok = mbar_wait_bounded(smem_u32(&ms.s_full[sbuf]), (g >> 1) & 1, abort_flag, p.err,
+        if (my_units > 0) {
+            stage_q(p, blockIdx.x, r, t_lane, 0, hf);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ms.q_full[0]));
+        }
+        for (int ul = 0; ul < my_units; ++ul) {
+            const int u = blockIdx.x + ul * gridDim.x;
+            const int lb = ul & 1;
+            if (ok) ok = mbar_wait_bounded(smem_u32(&ms.list_full[lb]), (ul >> 1) & 1, abort_flag, p.err,
+                                           kWaitLimitNs);
+            const uint32_t* list = lists + lb * kMaxUnion;
+            const int count = ok ? ms.list_count[lb] : 0;
+            const int nst = (count + 1) >> 1;
+            float m = ninf, l = 0.f;
+            for (int t = 0; t < nst; ++t, ++g) {
+                const int e = 2 * t + hf;
+                const uint32_t ent = e < count ? list[e] : 0u;
+                const bool mem = (entry_mask(ent) & my_bit) != 0;  // warp-uniform (row cube)
+                const int vb = entry_vbs(ent);
+                const uint32_t sc = kTmemS + (g & 1) * 128;
+                if (ok) ok = mbar_wait_bounded(smem_u32(&ms.s_full[g & 1]), (g >> 1) & 1, abort_flag, p.err,
                                                kWaitLimitNs);
-                if (ok) ok = mbar_wait_bounded(smem_u32(&ms.kv_full[stage]), (g / kStages) & 1, abort_flag,
-                                               p.err, kWaitLimitNs);
                 tc_fence_after();
-                const int4 inf = ms.info[stage];
-                const bool active = (cube_sel == 0) || (inf.z >= 0);  // warp-uniform
-                const int vbm = cube_sel == 0 ? inf.y : inf.w;
-                const bool real = ok && active && slot < vbm;
-                float y[32];
-                if (ok && active) {
-                    uint32_t raw[32];
-                    tmem_ld32(t_lane + sbuf * 64 + col0, raw);
+                float x[64];
+                if (ok && mem) {
+                    tmem_ld32(t_lane + sc + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+                    tmem_ld32(t_lane + sc + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
                     tmem_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) y[q] = __uint_as_float(raw[q]) * c2;  // log2-scaled logit
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) y[q] = 0.f;
                 }
-                if (!real) {
+                // Scaled logits (log2 units); keys past vbs are -inf.  Max by tree.
+                float lmax = ninf;
+                if (ok && mem) {
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) y[q] = ninf;
+                    for (int c = 0; c < 64; ++c) x[c] = c < vb ? x[c] * c2 : ninf;
+                    float mm[22];
+#pragma unroll
+                    for (int j = 0; j < 21; ++j) mm[j] = max3(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
+                    mm[21] = x[63];
+#pragma unroll
+                    for (int j = 0; j < 7; ++j) mm[j] = max3(mm[3 * j], mm[3 * j + 1], mm[3 * j + 2]);
+                    lmax = max3(max3(mm[0], mm[1], mm[2]), max3(mm[3], mm[4], mm[5]), max3(mm[6], mm[21], ninf));
                 }
-                // Does any logit exceed its column base by more than the threshold?
-                float mbr[32];
-#pragma unroll
-                for (int q = 0; q < 32; q += 4) {
-                    const float4 m4 = *reinterpret_cast<const float4*>(&ms.mb[col0 + q]);
-                    mbr[q] = m4.x; mbr[q + 1] = m4.y; mbr[q + 2] = m4.z; mbr[q + 3] = m4.w;
+                // Row max over both key cubes of the step (thread pair exchange).
+                ms.xmax[g & 1][hf][r] = lmax;
+                named_sync(1 + quarter, 64);
+                const float rmax = fmaxf(lmax, ms.xmax[g & 1][hf ^ 1][r]);
+                // Lazy running max: rescale O and l only on a jump > threshold
+                // (both threads of the row take the same decision).
+                float alpha = 1.f;
+                if (rmax > m + kRescaleThreshold) {
+                    alpha = (m == ninf) ? 0.f : ex2_approx(m - rmax);
+                    m = rmax;
+                    l *= alpha;
                 }
-                bool need = (t == 0);
-                if (t > 0) {
-                    float dmax = ninf;
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) dmax = fmaxf(dmax, y[q] - mbr[q]);
-                    bool trig = dmax > kRescaleThreshold || (real && ms.m_neg_inf);
-                    need = named_red_or(1, kSoftmaxThreads, trig);
-                }
-                if (need) {
-                    // Exact column max over the 128 keys of this step.
-                    float v[32];
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] = y[q];
-                    const float cm = transpose_reduce32<true>(v, lane);
-                    ms.red[sw][lane] = cm;
-                    named_sync(1, kSoftmaxThreads);
-                    if (sw == 0 || sw == 4) {
-                        const int col = col0 + lane;
-                        float mx = ms.red[sw][lane];
-#pragma unroll
-                        for (int w = 1; w < 4; ++w) mx = fmaxf(mx, ms.red[sw + w][lane]);
-                        const float m_old = (t == 0) ? ninf : ms.m[col];
-                        const float m_new = fmaxf(m_old, mx);
-                        ms.alpha[col] = (m_old == ninf) ? 0.f : ex2_approx(m_old - m_new);
-                        ms.m[col] = m_new;
-                        ms.mb[col] = (m_new == ninf) ? 0.f : m_new;
-                    }
-                    named_sync(1, kSoftmaxThreads);
-                    if (sw == 0 && lane == 0) {
-                        int any = 0;
-                        for (int c = 0; c < 64; ++c) any |= (ms.m[c] == ninf);
-                        ms.m_neg_inf = any;
-                    }
-                    if (t > 0) {
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) lpart[q] *= ms.alpha[col0 + q];
-                        // Rescale O^T: wait for the previous PV, then scale the columns.
-                        if (ok) ok = mbar_wait_bounded(smem_u32(&ms.o_done), (g - 1) & 1, abort_flag, p.err,
-                                                       kWaitLimitNs);
-                        if (ok) {
-                            tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f) && t > 0) {
+                    // This thread's half of the O row: wait for the previous PV.
+                    const uint32_t gp = g - 1;
+                    if (ok) ok = mbar_wait_bounded(smem_u32(&ms.pv_done[gp & 1]), (gp >> 1) & 1, abort_flag, p.err,
+                                                   kWaitLimitNs);
+                    if (ok) {
+                        tc_fence_after();
+                        for (int c0 = hf * dh; c0 < hf * dh + dh; c0 += 32) {
                             uint32_t o[32];
-                            tmem_ld32(t_lane + 128 + col0, o);
+                            tmem_ld32(t_lane + kTmemO + c0, o);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int q = 0; q < 32; ++q)
-                                o[q] = __float_as_uint(__uint_as_float(o[q]) * ms.alpha[col0 + q]);
-                            tmem_st32(t_lane + 128 + col0, o);
-                            tmem_wait_st();
+                            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+                            tmem_st32(t_lane + kTmemO + c0, o);
                         }
-                    }
-                    named_sync(1, kSoftmaxThreads);  // m_neg_inf published
-#pragma unroll
-                    for (int q = 0; q < 32; q += 4) {
-                        const float4 m4 = *reinterpret_cast<const float4*>(&ms.mb[col0 + q]);
-                        mbr[q] = m4.x; mbr[q + 1] = m4.y; mbr[q + 2] = m4.z; mbr[q + 3] = m4.w;
+                        tmem_wait_st();
                     }
                 }
-                // Probabilities (exp2 relative to the column base) and partial sums.
-                uint32_t pk[16];
+                // P = exp2(x - m) as bf16 pairs into this half's 32 P columns.
+                uint32_t pk[32];
+                if (ok && mem) {
+                    const float mb = (m == ninf) ? 0.f : m;
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-                for (int q = 0; q < 32; q += 2) {
-                    const float p0 = ex2_approx(y[q] - mbr[q]);
-                    const float p1 = ex2_approx(y[q + 1] - mbr[q + 1]);
-                    lpart[q] += p0;
-                    lpart[q + 1] += p1;
-                    pk[q >> 1] = pack_bf16x2(p0, p1);
-                }
-                // The single P^T buffer is free once the previous PV finished.
-                if (g > 0 && ok)
-                    ok = mbar_wait_bounded(smem_u32(&ms.o_done), (g - 1) & 1, abort_flag, p.err, kWaitLimitNs);
-                if (ok && active) {
-                    unsigned char* prow = smem + kOffP + key * 128;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int chunk = (half * 4 + cc) ^ (key & 7);
-                        *reinterpret_cast<uint4*>(prow + chunk * 16) =
-                            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                    for (int c = 0; c < 64; c += 4) {
+                        const float p0 = ex2_approx(x[c] - mb), p1 = ex2_approx(x[c + 1] - mb);
+                        const float p2 = ex2_approx(x[c + 2] - mb), p3 = ex2_approx(x[c + 3] - mb);
+                        s0 += p0; s1 += p1; s2 += p2; s3 += p3;
+                        pk[c >> 1] = pack_bf16x2(p0, p1);
+                        pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
                     }
+                    l += (s0 + s1) + (s2 + s3);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) pk[c] = 0u;
                 }
-                fence_proxy_async_smem();
+                if (ok) {
+                    tmem_st32(t_lane + sc + hf * 32, pk);
+                    tmem_wait_st();
+                }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ms.p_full));
-            }
-            // ------------------------------------------------ unit epilogue
-            {
-                float v[32];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] = lpart[q];
-                const float ls = transpose_reduce32<false>(v, lane);
-                ms.red[sw][lane] = ls;
-                named_sync(1, kSoftmaxThreads);
-                if (sw == 0 || sw == 4) {
-                    const int col = col0 + lane;
-                    float l = ms.red[sw][lane];
-#pragma unroll
-                    for (int w = 1; w < 4; ++w) l += ms.red[sw + w][lane];
-                    ms.alpha[col] = l > 0.f ? 1.f / l : 0.f;  // reused: 1 / l
-                    if (p.lse && ok) {
-                        const float lse = l > 0.f ? (ms.m[col] + __log2f(l)) * 0.69314718055994531f : ninf;
-                        p.lse[((size_t)b * p.heads + h) * s_pad + (size_t)i * kCubeTokens + col] = lse;
-                    }
+                if (lane == 0) mbar_arrive(smem_u32(&ms.p_full[g & 1]));
+                if (t == 0 && ul + 1 < my_units && ok) {
+                    // Stage the next unit's Q (its buffer was last read by a QK of
+                    // unit ul - 1, long complete).
+                    stage_q(p, u + gridDim.x, r, t_lane, (ul + 1) & 1, hf);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ms.q_full[(ul + 1) & 1]));
                 }
-                named_sync(1, kSoftmaxThreads);
-                if (ok) ok = mbar_wait_bounded(smem_u32(&ms.o_done), (g - 1) & 1, abort_flag, p.err, kWaitLimitNs);
-                if (ok) {
-                    tc_fence_after();
+            }
+            if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[lb]));
+            // ------------------------------------------------ unit epilogue
+            int b, h, pair;
+            unit_coords(u, p, b, h, pair);
+            const int i = 2 * pair + (r >> 6);
+            ms.xsum[hf][r] = l;
+            named_sync(1 + quarter, 64);
+            const float lt = l + ms.xsum[hf ^ 1][r];
+            const uint32_t gl = g - 1;  // last step of the unit
+            if (ok) ok = mbar_wait_bounded(smem_u32(&ms.pv_done[gl & 1]), (gl >> 1) & 1, abort_flag, p.err,
+                                           kWaitLimitNs);
+            if (ok) {
+                tc_fence_after();
+                const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+                const size_t row = (size_t)b * s_pad + (size_t)i * kCubeTokens + (r & 63);
+                uint4* dst = reinterpret_cast<uint4*>(p.out) + (row * p.heads + h) * (size_t)(D / 8);
+                for (int c0 = hf * dh; c0 < hf * dh + dh; c0 += 32) {
                     uint32_t o[32];
-                    tmem_ld32(t_lane + 128 + col0, o);
+                    tmem_ld32(t_lane + kTmemO + c0, o);
                     tmem_wait_ld();
-                    const int d = key;  // O^T lane = head-dim index
-                    if (d < D) {
-                        unsigned short* ob = reinterpret_cast<unsigned short*>(p.out);
-                        const size_t rs = (size_t)p.heads * D;
-                        const size_t base = ((size_t)b * s_pad + (size_t)i * kCubeTokens + col0) * rs +
-                                            (size_t)h * D + d;
+                    if (i < p.N) {
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            const float val = __uint_as_float(o[q]) * ms.alpha[col0 + q];
-                            const __nv_bfloat16 bv = __float2bfloat16_rn(val);
-                            __stcs(ob + base + (size_t)q * rs, *reinterpret_cast<const unsigned short*>(&bv));
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+                            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+                            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+                            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+                            __stcs(dst + c0 / 8 + v, w);
                         }
                     }
                 }
-                tc_fence_before();
-                named_sync(1, kSoftmaxThreads);  // 1/l and m are rewritten by the next unit
+                if (p.lse && i < p.N && hf == 0)
+                    p.lse[((size_t)b * p.heads + h) * s_pad + (size_t)i * kCubeTokens + (r & 63)] =
+                        lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : ninf;
             }
+            tc_fence_before();
+            named_sync(1 + quarter, 64);  // xsum is rewritten by the next unit's epilogue
         }
     }
 
@@ -559,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, 256);
+    if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
@@ -598,18 +672,20 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int heads, int 
 }
 
 int fine_smem_bytes() { return kSmemAlloc; }
+int fine_max_topk() { return kMaxTopk; }
+int fine_max_cubes() { return kMaxCubes; }
 
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                         const int32_t* vbs, int B, int ncubes, int heads, int D, int topk, float sm_scale,
                         void* out, float* lse, unsigned int* err, int num_sms, cudaStream_t stream) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mk, mv;
     const int rows = B * ncubes * kCubeTokens;
-    if (!make_map(&mq, qt, rows, heads, D, true) || !make_map(&mk, kt, rows, heads, D, true) ||
-        !make_map(&mv, vt, rows, heads, D, true))
+    if (!make_map(&mk, kt, rows, heads, D, true) || !make_map(&mv, vt, rows, heads, D, true))
         return cudaErrorInvalidValue;
     FineParams p;
     p.topk_idx = topk_idx;
     p.vbs = vbs;
+    p.q = static_cast<const uint4*>(qt);
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;
     p.err = err;
@@ -618,13 +694,14 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     p.heads = heads;
     p.D = D;
     p.topk = topk;
-    p.nsteps = (topk + 1) / 2;
-    p.num_units = B * heads * ncubes;
+    p.npairs = (ncubes + 1) / 2;
+    p.num_units = B * heads * p.npairs;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
-    cudaError_t e = cudaFuncSetAttribute(fine_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    auto kernel = D == 64 ? fine_fwd_kernel<64> : fine_fwd_kernel<128>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     const int grid = p.num_units < num_sms ? p.num_units : num_sms;
-    fine_fwd_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, p);
+    kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, p);
     return cudaGetLastError();
 }
 

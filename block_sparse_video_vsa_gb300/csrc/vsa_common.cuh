@@ -75,31 +75,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false if *abort was raised by another thread or the limit ran out (then it
-// raises *abort and sets the timeout bit).  Called by every lane of a warp;
-// the result is made warp-uniform.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort, unsigned int* err,
-                                                  uint64_t limit_ns) {
-    bool ok = true;
-    if (!mbar_try_wait(bar, parity)) {
-        const uint64_t t0 = globaltimer_ns();
-        for (;;) {
-            if (*abort) { ok = false; break; }
-            if (mbar_try_wait(bar, parity)) break;
-            if (globaltimer_ns() - t0 > limit_ns) {
-                *abort = 1;
-                atomicOr(err, VSA_DEVERR_TIMEOUT);
-                ok = false;
-                break;
-            }
-        }
-    }
-    return __all_sync(0xffffffffu, ok);
+// Non-blocking probe: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
-// Single-thread variant (no warp vote), for code run by one elected lane.
+// Single-thread bounded wait for the phase with the given parity to
+// complete.  Returns false if *abort was raised by another thread or the
+// limit ran out (then it raises *abort and sets the timeout bit).
 __device__ __forceinline__ bool mbar_wait_bounded_1(uint32_t bar, uint32_t parity,
                                                     volatile int* abort, unsigned int* err,
                                                     uint64_t limit_ns) {
@@ -114,6 +105,19 @@ __device__ __forceinline__ bool mbar_wait_bounded_1(uint32_t bar, uint32_t parit
             return false;
         }
     }
+}
+
+// Warp-wide bounded wait: lane 0 polls the barrier (one shared-memory access
+// stream instead of 32), the result is broadcast, and __syncwarp orders the
+// other lanes' later accesses after lane 0's acquire.  Called by every lane.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort, unsigned int* err,
+                                                  uint64_t limit_ns) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded_1(bar, parity, abort, err, limit_ns) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
 }
 
 // ------------------------------------------------------------------- TMA
@@ -200,6 +204,33 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// Same MMA with the descriptors given as (lo, hi) 32-bit halves, so a caller
+// can step through K by adding to the low word only.
+__device__ __forceinline__ void mma_ss_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                           uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem] (A operand read from tensor memory: M rows in
+// lanes, K along columns, two bf16 per 32-bit column, lower k in the low half).
+__device__ __forceinline__ void mma_ts_lohi(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // The mbarrier tracks completion of every tcgen05 op this thread issued so far.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -228,6 +259,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
         : "memory");
 }
 

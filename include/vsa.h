@@ -176,7 +176,8 @@ vsa_status vsa_coarse_select_noalloc(const void* qt, const void* kt, const int32
  *   vbs        : int32 [ncubes], each in [0, 64]
  *   out        : bf16 [B, 64*ncubes, heads, D] (written in full)
  *   lse        : fp32 [B, heads, 64*ncubes] (written), or NULL
- * Limits: D in {64, 128}; 1 <= topk <= ncubes; 64*ncubes*B < 2^31.
+ * Limits: D in {64, 128}; 1 <= topk <= min(ncubes, 512); ncubes <= 8192;
+ * 64*ncubes*B < 2^31.
  * Index validity is a precondition (check with vsa_validate_indices).
  */
 vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt,
