@@ -22,6 +22,7 @@ replica per GPU) and rank 0 reports the aggregate.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -62,13 +63,14 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []        # (host monotonic time, csv line)
+        self.window = None     # (t0, t1) of the timed region, host monotonic time
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:
@@ -77,7 +79,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -89,9 +91,21 @@ class ClockSampler:
         return False
 
     def summary(self):
+        """Clocks seen inside the timed window; if the sampler produced no
+        sample there (a very short timed region), the samples taken while the
+        warm-up and timed steps ran, marked as such."""
+        lines = self.lines
+        where = "timed region"
+        if self.window is not None:
+            t0, t1 = self.window
+            inside = [(t, ln) for t, ln in lines if t0 <= t <= t1 + 0.05]
+            if inside:
+                lines = inside
+            else:
+                where = "warm-up and timed steps (timed region shorter than the sampling period)"
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for _, ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -106,7 +120,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sampled_over": where}
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -178,7 +192,16 @@ def config_of(wl):
                         f"topk={wl.topk} of {wl.ncubes} cubes",
             "B": wl.B, "grid": [wl.T, wl.H, wl.W], "heads": wl.heads, "head_dim": wl.D,
             "topk": wl.topk, "ncubes": wl.ncubes, "s_padded": wl.s_pad,
-            "fine_flops": wl.fine_flops(), "l2": "inputs (3.2 GB per step) exceed L2; no flush"}
+            "fine_flops": wl.fine_flops(),
+            "l2": f"inputs and intermediates ({step_bytes(wl) / 1e9:.2f} GB touched per step) exceed the "
+                  f"126 MB L2; no flush"}
+
+
+def step_bytes(wl):
+    """Bytes of the step's big tensors: q, k, v and out untiled; q, k, v and out tiled."""
+    untiled = wl.B * wl.T * wl.H * wl.W * wl.heads * wl.D * 2
+    tiled = wl.B * wl.s_pad * wl.heads * wl.D * 2
+    return 4 * untiled + 4 * tiled
 
 
 # ------------------------------------------------------------------ ours
@@ -224,23 +247,26 @@ def run_ours(args, wl, inputs, rank, world, dist):
         if marks is not None:
             marks[4].record(stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if vsa.device_error(reset=True):
-        raise RuntimeError("device error word set during warm-up")
+    clk = ClockSampler(torch.cuda.current_device())
+    with clk:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        if vsa.device_error(reset=True):
+            raise RuntimeError("device error word set during warm-up")
 
-    marks = [[ev() for _ in range(5)] for _ in range(args.steps)]
-    start, end = ev(), ev()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
+        marks = [[ev() for _ in range(5)] for _ in range(args.steps)]
+        start, end = ev(), ev()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.monotonic()
         start.record(stream)
         for s in range(args.steps):
             step(marks[s])
         end.record(stream)
         torch.cuda.synchronize()
+        clk.window = (t0, time.monotonic())
     if dist:
         dist.barrier()
     ms_total = start.elapsed_time(end)
@@ -254,6 +280,8 @@ def run_ours(args, wl, inputs, rank, world, dist):
     if vsa.device_error(reset=True):
         raise RuntimeError("device error word set during the timed run")
 
+    if args.no_e2e:
+        return ms_step, stage, clk.summary(), None, 0, 0
     # ---- end to end through host buffers (pinned), copies inside the timed region
     qh, kh, vh = (torch.from_numpy(inputs[n].view(np.int16)).view(torch.bfloat16).pin_memory()
                   for n in ("q", "k", "v"))
@@ -296,6 +324,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) leg")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="profiling only: run the Wan grid with this many heads instead of 40")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -305,6 +336,8 @@ def main():
 
     from block_sparse_video_vsa_gb300 import synth
     wl = synth.WORKLOADS[WORKLOAD]
+    if args.heads > 0:
+        wl = dataclasses.replace(wl, heads=args.heads)
 
     if args.impl == "reference":
         if rank != 0:
@@ -347,8 +380,9 @@ def main():
                      "frac": fine_tflops / burst, "traffic": None,
                      "peak_kind": f"{peak_kind} dense bf16 burst",
                      "kernel": "fine_fwd_kernel (vsa_sparse_attn_fwd)"},
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": None if e2e_ms is None else {
+            "value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clocks,
     }

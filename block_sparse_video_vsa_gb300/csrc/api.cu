@@ -10,26 +10,6 @@
 
 namespace vsa {
 
-cudaError_t launch_tile(const vsa_grid& g, int ncubes, const void* x, void* xt, int32_t* vbs,
-                        cudaStream_t stream);
-cudaError_t launch_untile(const vsa_grid& g, int ncubes, const void* yt, void* y, cudaStream_t stream);
-size_t coarse_workspace_bytes(int B, int heads, int ncubes, int D);
-size_t coarse_smem_bytes(int R, int N, int D);
-int coarse_rows_per_block(int ncubes);
-cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes, int heads,
-                          int D, int topk, float sm_scale, void* workspace, int32_t* topk_idx,
-                          cudaStream_t stream);
-cudaError_t launch_validate(const int32_t* idx, const int32_t* vbs, int rows, int ncubes, int topk,
-                            int32_t* flag, cudaStream_t stream);
-int validate_max_cubes();
-cudaError_t launch_debug_wait(long long limit_ns, int32_t* result, unsigned int* err, cudaStream_t stream);
-int fine_smem_bytes();
-int fine_max_topk();
-int fine_max_cubes();
-cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
-                        const int32_t* vbs, int B, int ncubes, int heads, int D, int topk, float sm_scale,
-                        void* out, float* lse, unsigned int* err, int num_sms, cudaStream_t stream);
-
 // Library-wide device error word (one per device that loads the library).
 __device__ unsigned int g_device_error;
 
@@ -149,7 +129,7 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
     DevCtx ctx;
     cudaError_t e = get_dev_ctx(&ctx);
     if (e != cudaSuccess) return VSA_ERR_CUDA;
-    const size_t smem = coarse_smem_bytes(coarse_rows_per_block(ncubes), ncubes, D);
+    const size_t smem = coarse_smem_bytes(coarse_rows_per_block(ncubes, D), ncubes, D);
     if (smem > (size_t)ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
     return from_cuda(launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, workspace, topk_idx,

@@ -7,15 +7,21 @@
 // top-k over the last axis) with the score scaled by sm_scale.
 //
 // Pipeline (two kernels):
-//  1. pool_sums_kernel -- exact per-cube channel sums of q and k as fp32
-//     (hi, lo) pairs (error-free TwoSum accumulation over the vbs real
-//     tokens).  HBM bound: reads each tiled tensor once.
+//  1. pool_kernel -- per (batch, cube, q|k): channel sums over the vbs real
+//     tokens, accumulated error-free as fp32 (hi, lo) pairs (TwoSum), stored
+//     as the fp32 mean m = fl(fl(hi + lo) / vbs) and the fp32 residual
+//     r = (hi + lo) - m * vbs (TwoProduct, exact up to one rounding), plus the
+//     fp32 norm of every cube's mean vector per head.  HBM bound: reads each
+//     tiled tensor once.
 //  2. score_topk_kernel -- per (batch, head, block of R query cubes): fp32
-//     scores against every key cube (FFMA, shared-memory tiled), then per row
-//     a bitwise radix select of the k-th largest score.  Scores within a
-//     proven fp32 error bound of that boundary are re-ranked with exact cube
-//     sums in fp64, so the set matches exact-arithmetic top-k.
+//     scores against every key cube (FFMA; key means streamed into shared
+//     memory by asynchronous copies, double buffered), then per row a bitwise radix
+//     select of the k-th largest score.  Scores within a proven fp32 error
+//     bound of that boundary are re-ranked in fp64 with the exact cube sums
+//     m * vbs + r, so the set matches exact-arithmetic top-k.
 #include <float.h>
+
+#include <type_traits>
 
 #include "vsa_common.cuh"
 
@@ -33,58 +39,92 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// grid: (B * ncubes, 2 [q, k]); threads stride over 8-channel vectors of a
-// token row (heads * D / 8 of them).  ws layout: [2][B][heads][ncubes][D] for
-// hi, then the same for lo.
-__global__ void __launch_bounds__(256) pool_sums_kernel(const uint4* __restrict__ qt,
-                                                        const uint4* __restrict__ kt,
-                                                        const int32_t* __restrict__ vbs,
-                                                        float* __restrict__ ws_hi,
-                                                        float* __restrict__ ws_lo, int B,
-                                                        int ncubes, int heads, int D) {
+__device__ __forceinline__ void accumulate8(const uint4 w, float (&hi)[8], float (&lo)[8]) {
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float s, err;
+        two_sum(hi[2 * e], bf16_lo(ww[e]), s, err);
+        hi[2 * e] = s;
+        lo[2 * e] += err;
+        two_sum(hi[2 * e + 1], bf16_hi(ww[e]), s, err);
+        hi[2 * e + 1] = s;
+        lo[2 * e + 1] += err;
+    }
+}
+
+// Workspace planes (floats): mean [2][B][heads][ncubes][D] (q then k),
+// residual likewise, then norm [2][B][heads][ncubes].
+struct PoolOut {
+    float* mean;
+    float* resid;
+    float* norm;
+};
+
+// grid: (B * ncubes, 2 [q, k]); threads stride over the 8-channel vectors of
+// a token row (heads * D / 8 of them); D / 8 consecutive threads hold one
+// head's row, so the norm is a reduction over that lane group.
+__global__ void __launch_bounds__(256) pool_kernel(const uint4* __restrict__ qt, const uint4* __restrict__ kt,
+                                                   const int32_t* __restrict__ vbs, PoolOut o, int B,
+                                                   int ncubes, int heads, int D) {
     const int c = blockIdx.x % ncubes;
     const int b = blockIdx.x / ncubes;
     const int which = blockIdx.y;
     const uint4* src = which == 0 ? qt : kt;
     const int row_vecs = heads * D / 8;
+    const int gsz = D / 8;
     const int vb = min(max(vbs[c], 0), kCubeTokens);
+    const float fv = (float)vb;
     const size_t s_pad = (size_t)ncubes * kCubeTokens;
     const uint4* base = src + ((size_t)b * s_pad + (size_t)c * kCubeTokens) * row_vecs;
     for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) {
         float hi[8], lo[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) hi[e] = lo[e] = 0.f;
-        for (int r = 0; r < vb; ++r) {
-            const uint4 w = __ldcs(base + (size_t)r * row_vecs + v);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        int r = 0;
+        for (; r + 8 <= vb; r += 8) {  // eight loads in flight, summed in token order
+            uint4 w[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float s, err;
-                two_sum(hi[2 * e], bf16_lo(ww[e]), s, err);
-                hi[2 * e] = s;
-                lo[2 * e] += err;
-                two_sum(hi[2 * e + 1], bf16_hi(ww[e]), s, err);
-                hi[2 * e + 1] = s;
-                lo[2 * e + 1] += err;
+            for (int u = 0; u < 8; ++u) w[u] = __ldcs(base + (size_t)(r + u) * row_vecs + v);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) accumulate8(w[u], hi, lo);
+        }
+        for (; r < vb; ++r) accumulate8(__ldcs(base + (size_t)r * row_vecs + v), hi, lo);
+        float m[8], rr[8];
+        float s2 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (vb > 0) {
+                m[e] = (hi[e] + lo[e]) / fv;
+                const float p = m[e] * fv;
+                const float pe = fmaf(m[e], fv, -p);  // m * vb = p + pe exactly
+                rr[e] = (hi[e] - p) + (lo[e] - pe);
+            } else {
+                m[e] = rr[e] = 0.f;
             }
+            s2 = fmaf(m[e], m[e], s2);
         }
         const int ch = v * 8;
         const int h = ch / D;
         const int d = ch - h * D;
-        const size_t o = ((((size_t)which * B + b) * heads + h) * ncubes + c) * D + d;
-#pragma unroll
-        for (int e = 0; e < 8; e += 4) {
-            *reinterpret_cast<float4*>(ws_hi + o + e) = make_float4(hi[e], hi[e + 1], hi[e + 2], hi[e + 3]);
-            *reinterpret_cast<float4*>(ws_lo + o + e) = make_float4(lo[e], lo[e + 1], lo[e + 2], lo[e + 3]);
-        }
+        const size_t row = (((size_t)which * B + b) * heads + h) * ncubes + c;
+        const size_t off = row * D + d;
+        *reinterpret_cast<float4*>(o.mean + off) = make_float4(m[0], m[1], m[2], m[3]);
+        *reinterpret_cast<float4*>(o.mean + off + 4) = make_float4(m[4], m[5], m[6], m[7]);
+        *reinterpret_cast<float4*>(o.resid + off) = make_float4(rr[0], rr[1], rr[2], rr[3]);
+        *reinterpret_cast<float4*>(o.resid + off + 4) = make_float4(rr[4], rr[5], rr[6], rr[7]);
+        // Whole lane groups are active together (row_vecs and blockDim are
+        // multiples of gsz), so the xor partners below are always active.
+        const unsigned act = __activemask();
+        for (int x = 1; x < gsz; x <<= 1) s2 += __shfl_xor_sync(act, s2, x);
+        if ((v & (gsz - 1)) == 0) o.norm[row] = sqrtf(s2);
     }
 }
 
 // ------------------------------------------------------------ score + top-k
-constexpr int kScoreThreads = 256;
-constexpr int kWarps = kScoreThreads / 32;
-constexpr int kTileJ = 32;       // key cubes per shared-memory tile
+constexpr int kTileJ = 64;       // key cubes per shared-memory tile (two per lane)
 constexpr int kCandCap = 128;    // stored candidates per warp for re-ranking
+constexpr size_t kSmemCap = 232448;  // 227 KB opt-in shared memory per block
 
 // Monotone map from float to uint32 (larger float -> larger key).
 __device__ __forceinline__ uint32_t f2key(float f) {
@@ -99,49 +139,116 @@ __device__ __forceinline__ unsigned long long d2key(double f) {
     return (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
 }
 
+// Key of the k-th largest score of a row (warp-wide): the largest T with
+// count(key >= T) >= k, found bit by bit from the top.  The row's keys are
+// held in registers (KPL per lane, N <= 32 * KPL); slots past N hold 0,
+// which no candidate threshold (>= 1) counts.
+template <int KPL>
+__device__ __forceinline__ uint32_t kth_key(const float* row, int N, int k, int lane) {
+    uint32_t key[KPL];
+#pragma unroll
+    for (int q = 0; q < KPL; ++q) {
+        const int j = lane + 32 * q;
+        key[q] = j < N ? f2key(row[j]) : 0u;
+    }
+    uint32_t T = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = T | (1u << bit);
+        int cnt[4] = {0, 0, 0, 0};  // four independent chains (latency)
+#pragma unroll
+        for (int q = 0; q < KPL; ++q) cnt[q & 3] += key[q] >= cand;
+        const int c = __reduce_add_sync(0xffffffffu, (cnt[0] + cnt[1]) + (cnt[2] + cnt[3]));
+        if (c >= k) T = cand;
+    }
+    return T;
+}
+// Same search reading the row from shared memory on every pass (long rows).
+__device__ __noinline__ uint32_t kth_key_smem(const float* row, int N, int k, int lane) {
+    uint32_t T = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = T | (1u << bit);
+        int cnt = 0;
+        for (int j = lane; j < N; j += 32) cnt += f2key(row[j]) >= cand;
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        if (cnt >= k) T = cand;
+    }
+    return T;
+}
+
+// Byte offsets of the score kernel's shared-memory regions.
+struct ScoreLayout {
+    size_t qs, kb, sc, qnorm, red, qsum, cand_s, cand_j, total;
+};
+__host__ __device__ inline size_t take(size_t& o, size_t bytes, size_t align) {
+    o = (o + align - 1) / align * align;
+    const size_t r = o;
+    o += bytes;
+    return r;
+}
+__host__ __device__ inline ScoreLayout score_layout(int R, int N, int D, int warps) {
+    const size_t LD = (size_t)D + 4;  // padded row (floats): conflict-free float4 reads
+    ScoreLayout L;
+    size_t o = 0;
+    L.qs = take(o, (size_t)R * LD * 4, 16);
+    L.kb = take(o, 2 * (size_t)kTileJ * LD * 4, 16);
+    L.sc = take(o, (size_t)R * N * 4, 16);
+    L.qnorm = take(o, (size_t)R * 4, 4);
+    L.red = take(o, (size_t)warps * 4, 4);
+    L.qsum = take(o, (size_t)warps * D * 8, 8);
+    L.cand_s = take(o, (size_t)warps * kCandCap * 8, 8);
+    L.cand_j = take(o, (size_t)warps * kCandCap * 4, 4);
+    L.total = o;
+    return L;
+}
+
 struct ScoreArgs {
-    const float* qh;  // [B][heads][N][D] exact sums, hi part
-    const float* ql;
-    const float* kh;
-    const float* kl;
+    const float* qm;  // [B][heads][N][D] means
+    const float* qr;  //                  residuals
+    const float* km;
+    const float* kr;
+    const float* qn;  // [B][heads][N] norms of the means
+    const float* kn;
     const int32_t* vbs;
     int32_t* topk_idx;
     int B, N, heads, topk, R;
     float sm_scale;
 };
 
-// Exact (to ~1e-16) score of cube pair (i, j) from the hi/lo cube sums:
-// sm_scale * (Q_i . K_j) / (vbs_i * vbs_j), evaluated in fp64.
+__device__ __forceinline__ int clamp_vbs(int v) { return min(max(v, 0), kCubeTokens); }
+
+// Exact (to ~1e-16) score of cube pair (i, j): sm_scale * (S_i . S_j) /
+// (vbs_i * vbs_j) in fp64, with the channel sums S = m * vbs + r.
 template <int D>
-__device__ double precise_score(const double* __restrict__ qsum, const ScoreArgs& a, size_t krow,
-                                int j, double inv_vq) {
-    const float* kh = a.kh + krow + (size_t)j * D;
-    const float* kl = a.kl + krow + (size_t)j * D;
+__device__ double precise_score(const double* __restrict__ qsum, const ScoreArgs& a, size_t hrow, int j,
+                                double inv_vq) {
+    const int vk = clamp_vbs(a.vbs[j]);
+    if (vk <= 0) return 0.0;
+    const float* km = a.km + hrow + (size_t)j * D;
+    const float* kr = a.kr + hrow + (size_t)j * D;
     double acc = 0.0;
 #pragma unroll 4
-    for (int d = 0; d < D; ++d) {
-        const double kd = (double)kh[d] + (double)kl[d];
-        acc = fma(qsum[d], kd, acc);
-    }
-    const int vk = a.vbs[j];
-    if (vk <= 0) return 0.0;
+    for (int d = 0; d < D; ++d) acc = fma(qsum[d], fma((double)km[d], (double)vk, (double)kr[d]), acc);
     return (double)a.sm_scale * acc * inv_vq / (double)vk;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kScoreThreads) score_topk_kernel(ScoreArgs a) {
-    constexpr int LD = D + 4;  // padded row (floats): conflict-free float4 reads
+// WARPS warps; each thread scores RT query rows (R = WARPS * RT rows per block).
+template <int D, int RT, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) score_topk_kernel(ScoreArgs a) {
+    constexpr int kWarps = WARPS;
+    constexpr int kScoreThreads = WARPS * 32;
+    constexpr int LD = D + 4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int R = a.R;
     const int N = a.N;
-    float* qs = reinterpret_cast<float*>(smem_raw);                    // [R][LD]
-    float* ks = qs + R * LD;                                          // [kTileJ][LD]
-    float* sc = ks + kTileJ * LD;                                     // [R][N]
-    float* qnorm = sc + (size_t)R * N;                                // [R]
-    float* kmax_s = qnorm + R;                                        // [kWarps]
-    double* qsum_w = reinterpret_cast<double*>(kmax_s + kWarps + (kWarps & 1 ? 1 : 0));  // [kWarps][D]
-    double* cand_s = qsum_w + kWarps * D;                             // [kWarps][kCandCap]
-    int* cand_j = reinterpret_cast<int*>(cand_s + kWarps * kCandCap); // [kWarps][kCandCap]
+    const ScoreLayout L = score_layout(R, N, D, WARPS);
+    float* qs = reinterpret_cast<float*>(smem_raw + L.qs);        // [R][LD]
+    float* kb = reinterpret_cast<float*>(smem_raw + L.kb);        // [2][kTileJ][LD]
+    float* sc = reinterpret_cast<float*>(smem_raw + L.sc);        // [R][N]
+    float* qnorm = reinterpret_cast<float*>(smem_raw + L.qnorm);  // [R]
+    float* red = reinterpret_cast<float*>(smem_raw + L.red);      // [kWarps]
+    double* qsum_w = reinterpret_cast<double*>(smem_raw + L.qsum);  // [kWarps][D]
+    double* cand_s = reinterpret_cast<double*>(smem_raw + L.cand_s);
+    int* cand_j = reinterpret_cast<int*>(smem_raw + L.cand_j);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -149,85 +256,90 @@ __global__ void __launch_bounds__(kScoreThreads) score_topk_kernel(ScoreArgs a) 
     const int i0 = blockIdx.x * R;
     const int h = blockIdx.y;
     const int b = blockIdx.z;
-    const size_t hrow = ((size_t)b * a.heads + h) * (size_t)N * D;
+    const size_t bh = (size_t)b * a.heads + h;
+    const size_t hrow = bh * (size_t)N * D;  // element offset of this (b, head) in a [B][heads][N][D] plane
+    const int ntiles = (N + kTileJ - 1) / kTileJ;
 
-    // Stage the fp32 query means of this block's rows.
-    for (int e = tid; e < R * D; e += kScoreThreads) {
-        const int r = e / D, d = e - r * D;
+    // Copy key-mean tile t (rows j0 .. j0 + 63, 16-byte pieces into the
+    // padded layout) into buffer t & 1 with asynchronous copies.
+    auto issue_tile = [&](int t) {
+        const int j0 = t * kTileJ;
+        const int rows = min(kTileJ, N - j0);
+        float* dst = kb + (size_t)(t & 1) * kTileJ * LD;
+        const float* src = a.km + hrow + (size_t)j0 * D;
+        for (int e = tid; e < rows * (D / 4); e += kScoreThreads) {
+            const int r = e / (D / 4), c = e - r * (D / 4);
+            cp_async16(smem_u32(dst + r * LD + 4 * c), src + (size_t)r * D + 4 * c);
+        }
+        cp_async_commit();
+    };
+    issue_tile(0);
+
+    // Stage the query means of this block's rows and their norms.
+    for (int e = tid; e < R * (D / 4); e += kScoreThreads) {
+        const int r = e / (D / 4), d4 = e - r * (D / 4);
         const int i = i0 + r;
-        float v = 0.f;
-        if (i < N) {
-            const int vq = a.vbs[i];
-            const size_t o = hrow + (size_t)i * D + d;
-            v = vq > 0 ? (a.qh[o] + a.ql[o]) / (float)vq : 0.f;
-        }
-        qs[r * LD + d] = v;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < N) v = *reinterpret_cast<const float4*>(a.qm + hrow + (size_t)i * D + d4 * 4);
+        *reinterpret_cast<float4*>(qs + r * LD + d4 * 4) = v;
     }
-    __syncthreads();
-    for (int r = warp; r < R; r += kWarps) {
-        float s2 = 0.f;
-        for (int d = lane; d < D; d += 32) s2 = fmaf(qs[r * LD + d], qs[r * LD + d], s2);
+    for (int r = tid; r < R; r += kScoreThreads) qnorm[r] = (i0 + r < N) ? a.qn[bh * N + i0 + r] : 0.f;
+    float kmax = 0.f;  // largest key-mean norm of this head
+    for (int j = tid; j < N; j += kScoreThreads) kmax = fmaxf(kmax, a.kn[bh * N + j]);
 #pragma unroll
-        for (int o = 16; o; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-        if (lane == 0) qnorm[r] = sqrtf(s2);
-    }
-
-    // fp32 scores: thread (row group, column) -> R/8 rows x 1 column per tile.
-    const int col = tid & 31;
-    const int rg = tid >> 5;  // rows rg, rg + 8, ...
-    const int rows_per = R / kWarps;
-    float kmax = 0.f;
-    for (int j0 = 0; j0 < N; j0 += kTileJ) {
-        __syncthreads();
-        for (int e = tid; e < kTileJ * D; e += kScoreThreads) {
-            const int r = e / D, d = e - r * D;
-            const int j = j0 + r;
-            float v = 0.f;
-            if (j < N) {
-                const int vk = a.vbs[j];
-                const size_t o = hrow + (size_t)j * D + d;
-                v = vk > 0 ? (a.kh[o] + a.kl[o]) / (float)vk : 0.f;
-            }
-            ks[r * LD + d] = v;
-        }
-        __syncthreads();
-        {   // running max of key-mean norms (warp w handles tile rows w*4 .. w*4+3)
-            for (int r = warp * 4; r < warp * 4 + 4; ++r) {
-                float s2 = 0.f;
-                for (int d = lane; d < D; d += 32) s2 = fmaf(ks[r * LD + d], ks[r * LD + d], s2);
-#pragma unroll
-                for (int o = 16; o; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-                kmax = fmaxf(kmax, sqrtf(s2));
-            }
-        }
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const float* kp = ks + col * LD;
-#pragma unroll 4
-        for (int d = 0; d < D; d += 4) {
-            const float4 kv = *reinterpret_cast<const float4*>(kp + d);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                if (t < rows_per) {
-                    const float4 qv = *reinterpret_cast<const float4*>(qs + (rg + kWarps * t) * LD + d);
-                    acc[t] = fmaf(qv.x, kv.x, acc[t]);
-                    acc[t] = fmaf(qv.y, kv.y, acc[t]);
-                    acc[t] = fmaf(qv.z, kv.z, acc[t]);
-                    acc[t] = fmaf(qv.w, kv.w, acc[t]);
-                }
-            }
-        }
-        const int j = j0 + col;
-        if (j < N) {
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-                if (t < rows_per) sc[(size_t)(rg + kWarps * t) * N + j] = a.sm_scale * acc[t];
-        }
-    }
-    if (lane == 0) kmax_s[warp] = kmax;
+    for (int o = 16; o; o >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    if (lane == 0) red[warp] = kmax;
     __syncthreads();
     float kmax_all = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) kmax_all = fmaxf(kmax_all, kmax_s[w]);
+    for (int w = 0; w < kWarps; ++w) kmax_all = fmaxf(kmax_all, red[w]);
+
+    // fp32 scores: thread (warp, lane) -> rows warp + 8u (u < R / 8) x key
+    // columns lane and lane + 32 of each tile.
+    constexpr int rt = RT;  // = R / kWarps
+    for (int t = 0; t < ntiles; ++t) {
+        if (t + 1 < ntiles) {
+            issue_tile(t + 1);  // buffer (t+1)&1 was released at the end of t-1
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();  // tile t visible to every thread
+        const float* k0 = kb + (size_t)(t & 1) * kTileJ * LD + lane * LD;
+        const float* k1 = k0 + 32 * LD;
+        float acc[rt][2];
+#pragma unroll
+        for (int u = 0; u < rt; ++u) acc[u][0] = acc[u][1] = 0.f;
+#pragma unroll 8
+        for (int d = 0; d < D; d += 4) {
+            const float4 x0 = *reinterpret_cast<const float4*>(k0 + d);
+            const float4 x1 = *reinterpret_cast<const float4*>(k1 + d);
+#pragma unroll
+            for (int u = 0; u < rt; ++u) {
+                {
+                    const float4 q = *reinterpret_cast<const float4*>(qs + (warp + kWarps * u) * LD + d);
+                    acc[u][0] = fmaf(q.x, x0.x, acc[u][0]);
+                    acc[u][0] = fmaf(q.y, x0.y, acc[u][0]);
+                    acc[u][0] = fmaf(q.z, x0.z, acc[u][0]);
+                    acc[u][0] = fmaf(q.w, x0.w, acc[u][0]);
+                    acc[u][1] = fmaf(q.x, x1.x, acc[u][1]);
+                    acc[u][1] = fmaf(q.y, x1.y, acc[u][1]);
+                    acc[u][1] = fmaf(q.z, x1.z, acc[u][1]);
+                    acc[u][1] = fmaf(q.w, x1.w, acc[u][1]);
+                }
+            }
+        }
+        const int j0 = t * kTileJ + lane;
+#pragma unroll
+        for (int u = 0; u < rt; ++u) {
+            {
+                float* row = sc + (size_t)(warp + kWarps * u) * N;
+                if (j0 < N) row[j0] = a.sm_scale * acc[u][0];
+                if (j0 + 32 < N) row[j0 + 32] = a.sm_scale * acc[u][1];
+            }
+        }
+        __syncthreads();  // releases buffer t & 1 for tile t + 2
+    }
 
     // Selection: one warp per row.
     const int k = a.topk;
@@ -236,13 +348,17 @@ __global__ void __launch_bounds__(kScoreThreads) score_topk_kernel(ScoreArgs a) 
         if (i >= N) break;
         float* row = sc + (size_t)r * N;
         // k-th largest key by bitwise search: largest T with count(key >= T) >= k.
-        uint32_t T = 0;
-        for (int bit = 31; bit >= 0; --bit) {
-            const uint32_t cand = T | (1u << bit);
-            int cnt = 0;
-            for (int j = lane; j < N; j += 32) cnt += f2key(row[j]) >= cand;
-            cnt = __reduce_add_sync(0xffffffffu, cnt);
-            if (cnt >= k) T = cand;
+        uint32_t T;
+        switch ((N + 127) / 128) {  // register slots per lane: N / 32 rounded up to a multiple of 4
+            case 1: T = kth_key<4>(row, N, k, lane); break;
+            case 2: T = kth_key<8>(row, N, k, lane); break;
+            case 3: T = kth_key<12>(row, N, k, lane); break;
+            case 4: T = kth_key<16>(row, N, k, lane); break;
+            case 5: T = kth_key<20>(row, N, k, lane); break;
+            case 6: T = kth_key<24>(row, N, k, lane); break;
+            case 7: T = kth_key<28>(row, N, k, lane); break;
+            case 8: T = kth_key<32>(row, N, k, lane); break;
+            default: T = kth_key_smem(row, N, k, lane); break;
         }
         const float tau = key2f(T);
         // Error bound of an fp32 score against the exact one (dot of rounded
@@ -265,24 +381,24 @@ __global__ void __launch_bounds__(kScoreThreads) score_topk_kernel(ScoreArgs a) 
             // Re-rank the boundary band with exact cube sums in fp64.
             double* qsum = qsum_w + warp * D;
             const size_t qrow = hrow + (size_t)i * D;
-            for (int d = lane; d < D; d += 32) qsum[d] = (double)a.qh[qrow + d] + (double)a.ql[qrow + d];
+            const int vq = clamp_vbs(a.vbs[i]);
+            for (int d = lane; d < D; d += 32)
+                qsum[d] = fma((double)a.qm[qrow + d], (double)vq, (double)a.qr[qrow + d]);
             __syncwarp();
-            const int vq = a.vbs[i];
             const double inv_vq = vq > 0 ? 1.0 / (double)vq : 0.0;
             if (cC <= kCandCap) {
                 double* cs = cand_s + warp * kCandCap;
                 int* cj = cand_j + warp * kCandCap;
                 int pos = 0;
-                for (int j0 = 0; j0 < N; j0 += 32) {
-                    const int j = j0 + lane;
+                for (int j0b = 0; j0b < N; j0b += 32) {
+                    const int j = j0b + lane;
                     const bool inC = j < N && row[j] >= lo && row[j] <= hi;
                     const unsigned m = __ballot_sync(0xffffffffu, inC);
                     if (inC) cj[pos + __popc(m & ((1u << lane) - 1u))] = j;
                     pos += __popc(m);
                 }
                 __syncwarp();
-                for (int c = lane; c < cC; c += 32)
-                    cs[c] = precise_score<D>(qsum, a, hrow, cj[c], inv_vq);
+                for (int c = lane; c < cC; c += 32) cs[c] = precise_score<D>(qsum, a, hrow, cj[c], inv_vq);
                 __syncwarp();
                 // rank among candidates: (score desc, index asc); chosen if rank < need.
                 for (int c = lane; c < cC; c += 32) {
@@ -315,8 +431,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_topk_kernel(ScoreArgs a) 
                         greater += d2key(precise_score<D>(qsum, a, hrow, j, inv_vq)) > T2;
                 greater = __reduce_add_sync(0xffffffffu, greater);
                 int eq_left = need - greater;  // equal-to-T2 members to take, lowest index first
-                for (int j0 = 0; j0 < N; j0 += 32) {
-                    const int j = j0 + lane;
+                for (int j0b = 0; j0b < N; j0b += 32) {
+                    const int j = j0b + lane;
                     bool inC = j < N && row[j] >= lo && row[j] <= hi;
                     unsigned long long kk = 0;
                     if (inC) kk = d2key(precise_score<D>(qsum, a, hrow, j, inv_vq));
@@ -331,14 +447,23 @@ __global__ void __launch_bounds__(kScoreThreads) score_topk_kernel(ScoreArgs a) 
         }
         // Emit the selected set in ascending cube index.  After re-ranking the
         // band members hold +inf (chosen) or -inf (not chosen).
-        int32_t* out = a.topk_idx + (((size_t)b * a.heads + h) * N + i) * (size_t)k;
+        int32_t* out = a.topk_idx + (bh * N + i) * (size_t)k;
         int pos = 0;
-        for (int j0 = 0; j0 < N; j0 += 32) {
-            const int j = j0 + lane;
-            const bool sel = j < N && (row[j] > hi || (take_band && row[j] >= lo));
-            const unsigned m = __ballot_sync(0xffffffffu, sel);
-            if (sel) out[pos + __popc(m & ((1u << lane) - 1u))] = j;
-            pos += __popc(m);
+        const unsigned below = (1u << lane) - 1u;
+        for (int j0b = 0; j0b < N; j0b += 128) {  // four 32-wide slices per pass: loads batched
+            bool sel[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = j0b + 32 * q + lane;
+                const float x = j < N ? row[j] : -INFINITY;
+                sel[q] = j < N && (x > hi || (take_band && x >= lo));
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const unsigned m = __ballot_sync(0xffffffffu, sel[q]);
+                if (sel[q]) out[pos + __popc(m & below)] = j0b + 32 * q + lane;
+                pos += __popc(m);
+            }
         }
     }
 }
@@ -395,66 +520,64 @@ __global__ void debug_wait_kernel(long long limit_ns, int32_t* result, unsigned 
 }  // namespace
 
 size_t coarse_workspace_bytes(int B, int heads, int ncubes, int D) {
-    return (size_t)16 * B * heads * ncubes * D;
+    return (size_t)16 * B * heads * ncubes * D + (size_t)8 * B * heads * ncubes;
 }
 
-int coarse_rows_per_block(int ncubes) {
-    if (ncubes <= 1024) return 32;
-    if (ncubes <= 2048) return 16;
+// Score-block shapes: R rows per block on 16 warps (R = 32: two rows per
+// thread; R = 16: one) or on 8 warps (R = 8).
+static int score_warps(int R) { return R >= 16 ? 16 : 8; }
+
+// Rows per score block: the largest of 32, 16, 8 whose shared memory fits.
+int coarse_rows_per_block(int ncubes, int D) {
+    for (int R = 32; R > 8; R >>= 1)
+        if (score_layout(R, ncubes, D, score_warps(R)).total <= kSmemCap) return R;
     return 8;
 }
 
-size_t coarse_smem_bytes(int R, int N, int D) {
-    const size_t LD = D + 4;
-    size_t f = (size_t)R * LD + (size_t)kTileJ * LD + (size_t)R * N + R + kWarps + 1;
-    size_t bytes = f * 4;
-    bytes = (bytes + 7) & ~(size_t)7;
-    bytes += (size_t)kWarps * D * 8 + (size_t)kWarps * kCandCap * 8 + (size_t)kWarps * kCandCap * 4;
-    return bytes;
-}
+size_t coarse_smem_bytes(int R, int N, int D) { return score_layout(R, N, D, score_warps(R)).total; }
 
 cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes,
                           int heads, int D, int topk, float sm_scale, void* workspace,
                           int32_t* topk_idx, cudaStream_t stream) {
     float* ws = static_cast<float*>(workspace);
-    const size_t plane = (size_t)2 * B * heads * ncubes * D;  // q then k
-    float* hi = ws;
-    float* lo = ws + plane;
+    const size_t half = (size_t)B * heads * ncubes * D;  // one [B][heads][N][D] plane
+    PoolOut po;
+    po.mean = ws;                  // q, then k
+    po.resid = ws + 2 * half;      // q, then k
+    po.norm = ws + 4 * half;       // q [B][heads][N], then k
     const int row_vecs = heads * D / 8;
     dim3 pg(B * ncubes, 2);
-    pool_sums_kernel<<<pg, row_vecs < 256 ? ((row_vecs + 31) / 32) * 32 : 256, 0, stream>>>(
-        static_cast<const uint4*>(qt), static_cast<const uint4*>(kt), vbs, hi, lo, B, ncubes,
-        heads, D);
+    pool_kernel<<<pg, row_vecs < 256 ? ((row_vecs + 31) / 32) * 32 : 256, 0, stream>>>(
+        static_cast<const uint4*>(qt), static_cast<const uint4*>(kt), vbs, po, B, ncubes, heads, D);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     ScoreArgs a;
-    const size_t half = (size_t)B * heads * ncubes * D;
-    a.qh = hi;
-    a.kh = hi + half;
-    a.ql = lo;
-    a.kl = lo + half;
+    a.qm = po.mean;
+    a.km = po.mean + half;
+    a.qr = po.resid;
+    a.kr = po.resid + half;
+    a.qn = po.norm;
+    a.kn = po.norm + (size_t)B * heads * ncubes;
     a.vbs = vbs;
     a.topk_idx = topk_idx;
     a.B = B;
     a.N = ncubes;
     a.heads = heads;
     a.topk = topk;
-    a.R = coarse_rows_per_block(ncubes);
+    a.R = coarse_rows_per_block(ncubes, D);
     a.sm_scale = sm_scale;
     const size_t smem = coarse_smem_bytes(a.R, ncubes, D);
     dim3 grid((ncubes + a.R - 1) / a.R, heads, B);
-    if (D == 128) {
-        e = cudaFuncSetAttribute(score_topk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        score_topk_kernel<128><<<grid, kScoreThreads, smem, stream>>>(a);
-    } else {
-        e = cudaFuncSetAttribute(score_topk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        score_topk_kernel<64><<<grid, kScoreThreads, smem, stream>>>(a);
-    }
+    auto pick = [&](auto d) {
+        constexpr int DD = decltype(d)::value;
+        return a.R == 32 ? score_topk_kernel<DD, 2, 16>
+                         : a.R == 16 ? score_topk_kernel<DD, 1, 16> : score_topk_kernel<DD, 1, 8>;
+    };
+    auto kernel = D == 128 ? pick(std::integral_constant<int, 128>()) : pick(std::integral_constant<int, 64>());
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, score_warps(a.R) * 32, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

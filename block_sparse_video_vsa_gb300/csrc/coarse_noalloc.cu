@@ -29,13 +29,6 @@ static __device__ __align__(256) unsigned char g_coarse_scratch[(size_t)64 << 20
 
 namespace vsa {
 
-size_t coarse_workspace_bytes(int B, int heads, int ncubes, int D);
-size_t coarse_smem_bytes(int R, int N, int D);
-int coarse_rows_per_block(int ncubes);
-cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes, int heads,
-                          int D, int topk, float sm_scale, void* workspace, int32_t* topk_idx,
-                          cudaStream_t stream);
-
 namespace {
 
 constexpr size_t kScratchBytes = sizeof(g_coarse_scratch);  // 64 MiB
@@ -82,7 +75,7 @@ extern "C" vsa_status vsa_coarse_select_noalloc(const void* qt, const void* kt, 
         return VSA_ERR_ALIGNMENT;
     DevCtx ctx;
     if (get_dev_ctx(&ctx) != cudaSuccess) return VSA_ERR_CUDA;
-    if (coarse_smem_bytes(coarse_rows_per_block(ncubes), ncubes, D) > (size_t)ctx.max_smem_optin)
+    if (coarse_smem_bytes(coarse_rows_per_block(ncubes, D), ncubes, D) > (size_t)ctx.max_smem_optin)
         return VSA_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return VSA_ERR_CUDA;

@@ -12,6 +12,7 @@
 #include <stdint.h>
 
 #include "../../include/vsa.h"
+#include "vsa_launch.h"
 
 namespace vsa {
 
@@ -143,6 +144,17 @@ __device__ __forceinline__ void tma_store_3d(const void* desc, uint32_t src, int
             desc),
         "r"(src), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte
+// aligned), tracked by commit groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's commit groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");

@@ -1,0 +1,38 @@
+// Host-side launchers shared between the kernel files and the C ABI layer
+// (internal; not part of the public interface).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/vsa.h"
+
+namespace vsa {
+
+// tile.cu
+cudaError_t launch_tile(const vsa_grid& g, int ncubes, const void* x, void* xt, int32_t* vbs,
+                        cudaStream_t stream);
+cudaError_t launch_untile(const vsa_grid& g, int ncubes, const void* yt, void* y, cudaStream_t stream);
+
+// coarse.cu
+size_t coarse_workspace_bytes(int B, int heads, int ncubes, int D);
+size_t coarse_smem_bytes(int R, int N, int D);
+int coarse_rows_per_block(int ncubes, int D);
+cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes, int heads,
+                          int D, int topk, float sm_scale, void* workspace, int32_t* topk_idx,
+                          cudaStream_t stream);
+cudaError_t launch_validate(const int32_t* idx, const int32_t* vbs, int rows, int ncubes, int topk,
+                            int32_t* flag, cudaStream_t stream);
+int validate_max_cubes();
+cudaError_t launch_debug_wait(long long limit_ns, int32_t* result, unsigned int* err, cudaStream_t stream);
+
+// fine.cu
+int fine_smem_bytes();
+int fine_max_topk();
+int fine_max_cubes();
+cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                        const int32_t* vbs, int B, int ncubes, int heads, int D, int topk, float sm_scale,
+                        void* out, float* lse, unsigned int* err, int num_sms, cudaStream_t stream);
+
+}  // namespace vsa

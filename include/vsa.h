@@ -107,7 +107,9 @@ vsa_status vsa_untile(const vsa_grid* g, const void* yt, void* y, vsa_stream_t s
 
 /*
  * Bytes of device workspace vsa_coarse_select needs: 16 * B * heads * ncubes
- * * D (exact cube sums of Q and K as fp32 hi/lo pairs).  0 for bad sizes.
+ * * D + 8 * B * heads * ncubes (per cube and head: the fp32 mean of Q and K,
+ * an fp32 residual that makes the channel sums exact to ~2^-48, and the norm
+ * of each mean).  0 for bad sizes.
  */
 size_t vsa_coarse_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t D);
 
@@ -146,8 +148,9 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
  * the device.  The paper has no counterpart; it is a deployment variant.
  * Same arguments, results and errors as vsa_coarse_select, except:
  *   - the scratch is a 64 MiB device array inside the library, reserved on
- *     every GPU that loads the library until the process exits; problems with
- *     16 * B * heads * ncubes * D > 64 MiB return VSA_ERR_UNSUPPORTED;
+ *     every GPU that loads the library until the process exits; problems
+ *     whose vsa_coarse_workspace_bytes exceeds 64 MiB return
+ *     VSA_ERR_UNSUPPORTED;
  *   - the first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture;
  *   - all calls on a device share the array, so calls whose kernels overlap

@@ -61,7 +61,7 @@ def test_num_cubes(lib):
 
 
 def test_workspace_bytes(lib):
-    assert lib.vsa_coarse_workspace_bytes(1, 40, 624, 128) == 16 * 40 * 624 * 128
+    assert lib.vsa_coarse_workspace_bytes(1, 40, 624, 128) == 16 * 40 * 624 * 128 + 8 * 40 * 624
     assert lib.vsa_coarse_workspace_bytes(0, 40, 624, 128) == 0
 
 
