@@ -43,6 +43,17 @@ UNIT = "TFLOPS (effective)"
 WORKLOAD = "wan"
 KERNELS_PER_STEP = 7  # tile x3, pool sums, score/top-k, sparse attention, untile
 
+# DRAM traffic of one fine_fwd_kernel launch, from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum) of the Wan grid with 8 heads, scaled by 40/8 (traffic grows with
+# the (batch, head, query-cube pair) units processed).  Valid only for the kernel source it
+# was taken from: if fine.cu no longer hashes to `source_sha256`, the traffic is reported
+# as null.
+FINE_TRAFFIC = {
+    "bytes_per_launch": (247.728128e6 + 66.110208e6) * 40 / 8,
+    "capture": "profiles/fine_fwd_kernel_wan.md",
+    "source_sha256": "5aa99b4c3ad89a6f3bdbc6fa376710911f4008e7bad20a8f052d8b1b916defbe",
+}
+
 
 def load_peaks():
     path = os.path.join(HERE, "MEASURED_PEAKS.json")
@@ -187,8 +198,32 @@ def reference_arm(args, wl, inputs):
     }
 
 
+def fine_traffic():
+    import hashlib
+    path = os.path.join(HERE, "block_sparse_video_vsa_gb300", "csrc", "fine.cu")
+    with open(path, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return FINE_TRAFFIC["bytes_per_launch"] if digest == FINE_TRAFFIC["source_sha256"] else None
+
+
+def stage_bytes(wl):
+    """Algorithmic HBM bytes per call of the memory-bound stages."""
+    real = wl.B * wl.tokens * wl.heads * wl.D * 2
+    tiled = wl.B * wl.s_pad * wl.heads * wl.D * 2
+    return {
+        "tile_qkv": 3 * (real + tiled),                      # read raster rows, write every slot
+        "coarse_select": 2 * tiled + 4 * wl.B * wl.heads * wl.ncubes * wl.topk,  # read q, k; write idx
+        "untile": 2 * real,                                  # read real slots, write raster rows
+    }
+
+
+LABELS = {"wan": "Wan2.2-shape VSA", "wan_outlier": "Wan2.2-shape VSA with an outlier head (logits ~1e3)",
+          "hunyuan": "HunyuanVideo-shape VSA"}
+
+
 def config_of(wl):
-    return {"workload": f"Wan2.2-shape VSA: grid {wl.T}x{wl.H}x{wl.W}, {wl.heads} heads, D={wl.D}, "
+    label = LABELS.get(wl.name.split("-")[0], wl.name)
+    return {"workload": f"{label}: grid {wl.T}x{wl.H}x{wl.W}, {wl.heads} heads, D={wl.D}, "
                         f"topk={wl.topk} of {wl.ncubes} cubes",
             "B": wl.B, "grid": [wl.T, wl.H, wl.W], "heads": wl.heads, "head_dim": wl.D,
             "topk": wl.topk, "ncubes": wl.ncubes, "s_padded": wl.s_pad,
@@ -325,6 +360,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) leg")
+    ap.add_argument("--workload", choices=sorted(LABELS), default=WORKLOAD,
+                    help="the Wan2.2 shape (default; the benchmark workload) or another configuration")
+    ap.add_argument("--topk", type=int, default=0, help="override the workload's topk")
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling only: run the Wan grid with this many heads instead of 40")
     args = ap.parse_args()
@@ -335,7 +373,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     from block_sparse_video_vsa_gb300 import synth
-    wl = synth.WORKLOADS[WORKLOAD]
+    wl = synth.WORKLOADS[args.workload]
+    if args.topk > 0:
+        wl = wl.with_topk(args.topk)
     if args.heads > 0:
         wl = dataclasses.replace(wl, heads=args.heads)
 
@@ -376,8 +416,12 @@ def main():
             "effective_tflops": fine_tflops, "frac_of_burst_peak": fine_tflops / burst,
             "frac_of_sustained_peak": fine_tflops / sustained},
         "stages_ms_median": {k: statistics.median(v) for k, v in stage.items()},
+        "stages_hbm_gbs": {k: b / (statistics.median(stage[k]) * 1e-3) / 1e9
+                           for k, b in stage_bytes(wl).items()},
+        "hbm_peak_gbs": hbm,
         "roofline": {"bound": "tensor", "achieved": fine_tflops, "peak": burst, "unit": "TFLOP/s",
-                     "frac": fine_tflops / burst, "traffic": None,
+                     "frac": fine_tflops / burst,
+                     "traffic": fine_traffic() if wl.heads == 40 else None,
                      "peak_kind": f"{peak_kind} dense bf16 burst",
                      "kernel": "fine_fwd_kernel (vsa_sparse_attn_fwd)"},
         "e2e": None if e2e_ms is None else {

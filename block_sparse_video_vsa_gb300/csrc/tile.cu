@@ -6,7 +6,7 @@
 // a contiguous spatio-temporal region; Stage 1: (4, 4, 4) cubes of 64 tokens)
 // and "Wan2.2 Production Values -- VSA Block-Sparse Attention Inputs +
 // Reference" (Shapes: cube-major tiled/padded, vbs = real tokens per cube;
-// Operator contract: only the first vbs[c] of 64 slots are attended).
+// Operator contract: attention reads only the leading vbs[c] slots of a cube).
 //
 // Work decomposition: one thread block per (batch, cube).  Each token row is
 // heads * D * 2 contiguous bytes; rows move as 16-byte vectors with the block's

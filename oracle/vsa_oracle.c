@@ -28,7 +28,8 @@
  *    tile index order of [STA] Implementation;
  *  - inside a cube the real tokens of its clipped sub-box come first, in
  *    raster (t, h, w) order, padding slots vbs..63 are zero ([WAN-VSA]
- *    Operator contract: "attend only the first vbs[c] of 64");
+ *    Operator contract: a cube's attention covers only its leading vbs[c]
+ *    slots of the 64);
  *  - the cube mean-pool divides by vbs[c] (real tokens only); an empty cube
  *    (vbs = 0, never produced by tiling) pools to the zero vector;
  *  - the cube score is sm_scale * (q_mean . k_mean);
@@ -133,8 +134,8 @@ void oracle_untile(int64_t B, int64_t T, int64_t Hh, int64_t W, int64_t heads, i
 /* ---------------------------------------------------------------------- */
 
 /*
- * Cube mean-pool ([VSA-AMD] Stage 1: each cube is mean-pooled into one
- * cube-level vector).  xt: [B, N*64, heads, D]; out: [B, heads, N, D].
+ * Cube mean-pool ([VSA-AMD] Stage 1: Coarse Selection -- the tokens of a
+ * cube are averaged into a single vector that stands for the cube).  xt: [B, N*64, heads, D]; out: [B, heads, N, D].
  * The mean runs over the vbs[c] real tokens of the cube.
  */
 void oracle_pool(int64_t B, int64_t N, int64_t heads, int64_t D, const uint16_t* xt,
