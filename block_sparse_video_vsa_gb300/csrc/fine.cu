@@ -29,9 +29,11 @@
 //    they exchange their row maxima through shared memory with a 64-thread
 //    named barrier, so the running max, the sum and the lazy rescale of the
 //    row's O need no wider synchronisation.
-//  * TMEM (512 columns): S double buffer [0,128) [128,256) (P in bf16 is
-//    written over the first 64 columns of its S buffer), O [256, 384), Q double
-//    buffer [384, 448) [448, 512).
+//  * TMEM (512 columns): S double buffer [0,128) [128,256); P of the current
+//    step (bf16 pairs) [256,320); Q of the current unit [320,384); O
+//    [384,512).  The softmax releases an S buffer as soon as it has loaded
+//    it, so QK runs two steps ahead of PV; P has its own columns, rewritten
+//    for step g + 1 only after PV(g) completes.
 //  * Running max kept in log2 units; O and the sum are rescaled only when a
 //    row's max grows by more than kRescaleThreshold, so exp2 arguments stay
 //    <= the threshold and logits of any finite size are safe.
@@ -50,7 +52,7 @@ constexpr int kKStages = 3;           // K pair slots (QK operand B)
 constexpr int kVStages = 3;           // V pair slots (PV operand B)
 constexpr int kSoftmaxWarps = 8;
 constexpr int kFirstSoftmaxWarp = 4;
-constexpr int kThreads = (kFirstSoftmaxWarp + kSoftmaxWarps) * 32;  // 8 warps
+constexpr int kThreads = (kFirstSoftmaxWarp + kSoftmaxWarps) * 32;  // 12 warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kMaxTopk = 512;
@@ -60,8 +62,9 @@ constexpr int kBitmapWords = kMaxCubes / 32;
 
 // TMEM columns.
 constexpr int kTmemS = 0;    // two S buffers of 128 columns
-constexpr int kTmemO = 256;  // O accumulator (D columns)
-constexpr int kTmemQ = 384;  // two Q buffers of 64 columns (bf16 pairs)
+constexpr int kTmemP = 256;  // P of the current step: 128 keys as 64 columns of bf16 pairs
+constexpr int kTmemQ = 320;  // Q of the current unit: D bf16 as D/2 columns of pairs
+constexpr int kTmemO = 384;  // O accumulator (D columns)
 
 // Shared-memory layout (bytes from a 1024-aligned base).
 constexpr int kChunkRows64 = 64 * 128;           // 64 rows x 128 B   = 8 KB
@@ -85,9 +88,11 @@ struct __align__(16) Misc {
     uint64_t v_full[kVStages];
     uint64_t v_empty[kVStages];
     uint64_t s_full[2];
-    uint64_t p_full[2];
-    uint64_t pv_done[2];
-    uint64_t q_full[2];
+    uint64_t s_free[2];
+    uint64_t p_full;
+    uint64_t pv_done;
+    uint64_t q_full;
+    uint64_t q_empty;
     uint64_t list_full[2];
     uint64_t list_empty[2];
     uint64_t drain;
@@ -186,21 +191,20 @@ __device__ __forceinline__ void load_pair(const CUtensorMap* tm, uint32_t dst, u
             tma_load_3d(dst + c * kChunkRows128 + kChunkRows64, tm, bar, c * 64, h, row_b, policy);
 }
 
-// Waits (bounded) until the last copy issued into each ring slot has landed.
+// Waits (bounded, also after an abort) until the last copy issued into each
+// ring slot has landed.  Called by lane 0 of the producer warp.
 template <int kSlots>
-__device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t issued, volatile int* abort_flag,
-                                           unsigned int* err) {
+__device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t issued, unsigned int* err) {
     for (int s = 0; s < kSlots; ++s) {
         if ((uint32_t)s >= issued) continue;
         const uint32_t last = issued - 1 - ((issued - 1 - s) % kSlots);  // last step that used slot s
-        mbar_wait_bounded(smem_u32(&full[s]), (last / kSlots) & 1, abort_flag, err, kWaitLimitNs);
+        mbar_wait_drain_1(smem_u32(&full[s]), (last / kSlots) & 1, err, kWaitLimitNs);
     }
 }
 
 // Softmax threads: copy half `hf` of this thread's Q row (or zeros) into TMEM
 // Q buffer qb (D/2 elements = D/4 32-bit columns; D = 64 has one half only).
-__device__ __forceinline__ void stage_q(const FineParams& p, int u, int row_in_pair, uint32_t t_lane, int qb,
-                                        int hf) {
+__device__ __forceinline__ void stage_q(const FineParams& p, int u, int row_in_pair, uint32_t t_lane, int hf) {
     int b, h, pair;
     unit_coords(u, p, b, h, pair);
     const int i = 2 * pair + (row_in_pair >> 6);
@@ -220,7 +224,7 @@ __device__ __forceinline__ void stage_q(const FineParams& p, int u, int row_in_p
 #pragma unroll
             for (int v = 0; v < 32; ++v) w[v] = 0u;
         }
-        tmem_st32(t_lane + kTmemQ + qb * 64 + c0, w);
+        tmem_st32(t_lane + kTmemQ + c0, w);
     }
     tmem_wait_st();
 }
@@ -267,12 +271,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&ms.s_full[s]), 1);
-            mbar_init(smem_u32(&ms.p_full[s]), kSoftmaxWarps);
-            mbar_init(smem_u32(&ms.pv_done[s]), 1);
-            mbar_init(smem_u32(&ms.q_full[s]), kSoftmaxWarps);
+            mbar_init(smem_u32(&ms.s_free[s]), kSoftmaxWarps);
             mbar_init(smem_u32(&ms.list_full[s]), 1);
             mbar_init(smem_u32(&ms.list_empty[s]), 1 + 1 + kSoftmaxWarps);  // V producer, MMA, softmax warps
         }
+        mbar_init(smem_u32(&ms.p_full), kSoftmaxWarps);
+        mbar_init(smem_u32(&ms.pv_done), 1);
+        mbar_init(smem_u32(&ms.q_full), kSoftmaxWarps);
+        mbar_init(smem_u32(&ms.q_empty), 1);
         mbar_init(smem_u32(&ms.drain), 1);
         ms.abort_flag = 0;
         fence_barrier_init();
@@ -334,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
         }
-        drain_ring<kKStages>(ms.k_full, g, abort_flag, p.err);
+        if (lane == 0) drain_ring<kKStages>(ms.k_full, g, p.err);
+        __syncwarp();
     } else if (warp == 2) {
         // ========================================== TMA producer of V
         const uint64_t pol = l2_policy_evict_last();
@@ -367,16 +374,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[lb]));
         }
-        drain_ring<kVStages>(ms.v_full, g, abort_flag, p.err);
+        if (lane == 0) drain_ring<kVStages>(ms.v_full, g, p.err);
+        __syncwarp();
     } else if (warp == 1) {
         // ============================================================ MMA issuer
-        // One lane issues every MMA, in the order QK(0), then per step g:
-        // QK(g + 1), PV(g).  QK(g + 2) reuses the TMEM columns that PV(g) reads
-        // P from; MMAs issued by one thread execute in issue order, so the
-        // reuse needs no extra wait.  Descriptors are precomputed; each MMA
-        // adds a constant to the start-address field of the low word (no
-        // carry: shared addresses are below 256 KB).
-        if (lane == 0 && my_units > 0) {
+        // The whole warp walks the schedule with warp-uniform values; lane 0
+        // issues every MMA and commit.  QK(g) writes S buffer g & 1 once the
+        // softmax has loaded S(g - 2) from it, so QK runs two steps ahead of
+        // PV; the order is QK(0), QK(1), then per step g: PV(g), QK(g + 2).
+        // PV(g) reads P from its own TMEM columns, which the softmax rewrites
+        // for step g + 1 only after PV(g) completes.  Descriptors are
+        // precomputed; each MMA adds a constant to the start-address field of
+        // the low word (no carry: shared addresses are below 256 KB).
+        if (my_units > 0) {
             const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
             const uint32_t hi = (uint32_t)(smem_desc_sw128(0, 16, 1024) >> 32);  // SBO, version, swizzle
@@ -388,37 +398,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t gq = 0;   // next QK step (global)
             int ul_q = 0, t_q = 0, cnt_q = 0;  // unit / step cursor of the QK stream
             int ul_p = 0, t_p = 0, cnt_p = 0;  // unit / step cursor of the PV stream
-            // Count of the list of local unit ul (waits for the list).
+            // Count of the list of local unit ul (waits for the list), warp-uniform.
             auto list_count = [&](int ul) -> int {
-                if (!mbar_wait_bounded_1(smem_u32(&ms.list_full[ul & 1]), (ul >> 1) & 1, abort_flag, p.err,
-                                         kWaitLimitNs))
+                if (!mbar_wait_bounded(smem_u32(&ms.list_full[ul & 1]), (ul >> 1) & 1, abort_flag, p.err,
+                                       kWaitLimitNs))
                     return -1;
-                return ms.list_count[ul & 1];
+                return __shfl_sync(0xffffffffu, ms.list_count[ul & 1], 0);
             };
             auto issue_qk = [&]() -> bool {
                 if (t_q == 0) {
                     cnt_q = list_count(ul_q);
                     if (cnt_q < 0) return false;
-                    if (!mbar_wait_bounded_1(smem_u32(&ms.q_full[ul_q & 1]), (ul_q >> 1) & 1, abort_flag, p.err,
-                                             kWaitLimitNs))
+                    if (!mbar_wait_bounded(smem_u32(&ms.q_full), ul_q & 1, abort_flag, p.err, kWaitLimitNs))
                         return false;
                 }
+                if (gq >= 2 && !mbar_wait_bounded(smem_u32(&ms.s_free[gq & 1]), ((gq >> 1) + 1) & 1, abort_flag,
+                                                  p.err, kWaitLimitNs))
+                    return false;
                 const int slot = gq % kKStages;
-                if (!mbar_wait_bounded_1(smem_u32(&ms.k_full[slot]), (gq / kKStages) & 1, abort_flag, p.err,
-                                         kWaitLimitNs))
+                if (!mbar_wait_bounded(smem_u32(&ms.k_full[slot]), (gq / kKStages) & 1, abort_flag, p.err,
+                                       kWaitLimitNs))
                     return false;
                 const uint32_t b0 = lo_k + ((uint32_t)(slot * kPairBytes) >> 4);
-                const uint32_t a0 = tmem + kTmemQ + (ul_q & 1) * 64;
+                const uint32_t a0 = tmem + kTmemQ;
                 const uint32_t d_tmem = tmem + kTmemS + (gq & 1) * 128;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < ksteps_qk; ++kk)
-                    mma_ts_lohi(d_tmem, a0 + kk * 8, b0 + (((kk >> 2) * kChunkRows128 + (kk & 3) * 32) >> 4), hi,
+                    mma_ts_warp(d_tmem, a0 + kk * 8, b0 + (((kk >> 2) * kChunkRows128 + (kk & 3) * 32) >> 4), hi,
                                 idesc_qk, kk > 0);
-                mma_commit(smem_u32(&ms.s_full[gq & 1]));
-                mma_commit(smem_u32(&ms.k_empty[slot]));
+                mma_commit_warp(smem_u32(&ms.s_full[gq & 1]));
+                mma_commit_warp(smem_u32(&ms.k_empty[slot]));
                 ++gq;
                 if (++t_q == (cnt_q + 1) >> 1) {
+                    mma_commit_warp(smem_u32(&ms.q_empty));  // the unit's Q is no longer read
                     t_q = 0;
                     ++ul_q;
                 }
@@ -430,28 +443,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (cnt_p < 0) return false;
                 }
                 const int slot = g % kVStages;
-                if (!mbar_wait_bounded_1(smem_u32(&ms.p_full[g & 1]), (g >> 1) & 1, abort_flag, p.err,
-                                         kWaitLimitNs) ||
-                    !mbar_wait_bounded_1(smem_u32(&ms.v_full[slot]), (g / kVStages) & 1, abort_flag, p.err,
-                                         kWaitLimitNs))
+                if (!mbar_wait_bounded(smem_u32(&ms.p_full), g & 1, abort_flag, p.err, kWaitLimitNs) ||
+                    !mbar_wait_bounded(smem_u32(&ms.v_full[slot]), (g / kVStages) & 1, abort_flag, p.err,
+                                       kWaitLimitNs))
                     return false;
                 const uint32_t b0 = lo_v + ((uint32_t)(slot * kPairBytes) >> 4);
-                const uint32_t a0 = tmem + kTmemS + (g & 1) * 128;
+                const uint32_t a0 = tmem + kTmemP;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_lohi(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv,
+                    mma_ts_warp(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv,
                                 (t_p > 0 || kk > 0));
                 if (2 * t_p + 1 < cnt_p) {  // the second cube of the step (a single-cube step has 64 keys)
 #pragma unroll
                     for (int kk = 4; kk < 8; ++kk)
-                        mma_ts_lohi(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv, 1u);
+                        mma_ts_warp(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv, 1u);
                 }
-                mma_commit(smem_u32(&ms.pv_done[g & 1]));
-                mma_commit(smem_u32(&ms.v_empty[slot]));
+                mma_commit_warp(smem_u32(&ms.pv_done));
+                mma_commit_warp(smem_u32(&ms.v_empty[slot]));
                 if (++t_p == (cnt_p + 1) >> 1) {
                     // The MMA side is done with this unit's list.
-                    mbar_arrive(smem_u32(&ms.list_empty[ul_p & 1]));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[ul_p & 1]));
                     t_p = 0;
                     ++ul_p;
                 }
@@ -459,13 +472,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             ok = issue_qk();
+            if (ok && ul_q < my_units) ok = issue_qk();
             while (ok && ul_p < my_units) {
-                if (ul_q < my_units) ok = issue_qk();
-                if (ok) ok = issue_pv();
+                // PV(g) first: the softmax writes P(g + 1) once PV(g) completes, so
+                // PV(g) goes to the tensor pipe ahead of QK(g + 2).
+                ok = issue_pv();
+                if (ok && ul_q < my_units) ok = issue_qk();
             }
             // Drain: all issued MMAs complete before TMEM is released.
-            mma_commit(smem_u32(&ms.drain));
-            mbar_wait_bounded_1(smem_u32(&ms.drain), 0, abort_flag, p.err, kWaitLimitNs);
+            mma_commit_warp(smem_u32(&ms.drain));
+            if (lane == 0) mbar_wait_drain_1(smem_u32(&ms.drain), 0, p.err, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp >= kFirstSoftmaxWarp) {
@@ -482,10 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         uint32_t g = 0;
         if (my_units > 0) {
-            stage_q(p, blockIdx.x, r, t_lane, 0, hf);
+            stage_q(p, blockIdx.x, r, t_lane, hf);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ms.q_full[0]));
+            if (lane == 0) mbar_arrive(smem_u32(&ms.q_full));
         }
         for (int ul = 0; ul < my_units; ++ul) {
             const int u = blockIdx.x + ul * gridDim.x;
@@ -505,24 +521,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) ok = mbar_wait_bounded(smem_u32(&ms.s_full[g & 1]), (g >> 1) & 1, abort_flag, p.err,
                                                kWaitLimitNs);
                 tc_fence_after();
+                if (t + 1 == nst && ul + 1 < my_units && ok) {
+                    // Last step of the unit: its Q is no longer read (the unit's last
+                    // QK has completed with S(g)), so stage the next unit's Q now.
+                    ok = mbar_wait_bounded(smem_u32(&ms.q_empty), ul & 1, abort_flag, p.err, kWaitLimitNs);
+                    if (ok) {
+                        tc_fence_after();
+                        stage_q(p, u + gridDim.x, r, t_lane, hf);
+                        tc_fence_before();
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ms.q_full));
+                }
                 float x[64];
                 if (ok && mem) {
                     tmem_ld32(t_lane + sc + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
                     tmem_ld32(t_lane + sc + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
                     tmem_wait_ld();
                 }
-                // Scaled logits (log2 units); keys past vbs are -inf.  Max by tree.
+                // S(g) is in registers: its buffer may take S(g + 2).
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ms.s_free[g & 1]));
+                // Raw row maximum of this half (keys past vbs are -inf), then log2 units.
                 float lmax = ninf;
                 if (ok && mem) {
+                    if (vb < kCubeTokens) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) x[c] = c < vb ? x[c] * c2 : ninf;
+                        for (int c = 0; c < 64; ++c) x[c] = c < vb ? x[c] : ninf;
+                    }
                     float mm[22];
 #pragma unroll
                     for (int j = 0; j < 21; ++j) mm[j] = max3(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
                     mm[21] = x[63];
 #pragma unroll
                     for (int j = 0; j < 7; ++j) mm[j] = max3(mm[3 * j], mm[3 * j + 1], mm[3 * j + 2]);
-                    lmax = max3(max3(mm[0], mm[1], mm[2]), max3(mm[3], mm[4], mm[5]), max3(mm[6], mm[21], ninf));
+                    lmax = c2 * max3(max3(mm[0], mm[1], mm[2]), max3(mm[3], mm[4], mm[5]), fmaxf(mm[6], mm[21]));
                 }
                 // Row max over both key cubes of the step (thread pair exchange).
                 ms.xmax[g & 1][hf][r] = lmax;
@@ -536,33 +570,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m = rmax;
                     l *= alpha;
                 }
-                if (__any_sync(0xffffffffu, alpha != 1.f) && t > 0) {
-                    // This thread's half of the O row: wait for the previous PV.
-                    const uint32_t gp = g - 1;
-                    if (ok) ok = mbar_wait_bounded(smem_u32(&ms.pv_done[gp & 1]), (gp >> 1) & 1, abort_flag, p.err,
-                                                   kWaitLimitNs);
-                    if (ok) {
-                        tc_fence_after();
-                        for (int c0 = hf * dh; c0 < hf * dh + dh; c0 += 32) {
-                            uint32_t o[32];
-                            tmem_ld32(t_lane + kTmemO + c0, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
-                            tmem_st32(t_lane + kTmemO + c0, o);
-                        }
-                        tmem_wait_st();
-                    }
-                }
-                // P = exp2(x - m) as bf16 pairs into this half's 32 P columns.
+                // P = exp2(x c2 - m) as bf16 pairs (this half's 32 P columns).
                 uint32_t pk[32];
                 if (ok && mem) {
                     const float mb = (m == ninf) ? 0.f : m;
                     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                     for (int c = 0; c < 64; c += 4) {
-                        const float p0 = ex2_approx(x[c] - mb), p1 = ex2_approx(x[c + 1] - mb);
-                        const float p2 = ex2_approx(x[c + 2] - mb), p3 = ex2_approx(x[c + 3] - mb);
+                        const float p0 = ex2_approx(fmaf(x[c], c2, -mb)), p1 = ex2_approx(fmaf(x[c + 1], c2, -mb));
+                        const float p2 = ex2_approx(fmaf(x[c + 2], c2, -mb)), p3 = ex2_approx(fmaf(x[c + 3], c2, -mb));
                         s0 += p0; s1 += p1; s2 += p2; s3 += p3;
                         pk[c >> 1] = pack_bf16x2(p0, p1);
                         pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
@@ -572,21 +588,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 32; ++c) pk[c] = 0u;
                 }
-                if (ok) {
-                    tmem_st32(t_lane + sc + hf * 32, pk);
-                    tmem_wait_st();
+                // PV(g - 1) has read the P columns and finished adding into O.
+                if (g > 0 && ok)
+                    ok = mbar_wait_bounded(smem_u32(&ms.pv_done), (g - 1) & 1, abort_flag, p.err, kWaitLimitNs);
+                tc_fence_after();
+                if (ok) tmem_st32(t_lane + kTmemP + hf * 32, pk);
+                if (ok && t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    // Rescale this thread's half of the O row.
+#pragma unroll 1
+                    for (int c0 = hf * dh; c0 < hf * dh + dh; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(t_lane + kTmemO + c0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+                        tmem_st32(t_lane + kTmemO + c0, o);
+                    }
                 }
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ms.p_full[g & 1]));
-                if (t == 0 && ul + 1 < my_units && ok) {
-                    // Stage the next unit's Q (its buffer was last read by a QK of
-                    // unit ul - 1, long complete).
-                    stage_q(p, u + gridDim.x, r, t_lane, (ul + 1) & 1, hf);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ms.q_full[(ul + 1) & 1]));
-                }
+                if (lane == 0) mbar_arrive(smem_u32(&ms.p_full));
             }
             if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[lb]));
             // ------------------------------------------------ unit epilogue
@@ -597,8 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(1 + quarter, 64);
             const float lt = l + ms.xsum[hf ^ 1][r];
             const uint32_t gl = g - 1;  // last step of the unit
-            if (ok) ok = mbar_wait_bounded(smem_u32(&ms.pv_done[gl & 1]), (gl >> 1) & 1, abort_flag, p.err,
-                                           kWaitLimitNs);
+            if (ok) ok = mbar_wait_bounded(smem_u32(&ms.pv_done), gl & 1, abort_flag, p.err, kWaitLimitNs);
             if (ok) {
                 tc_fence_after();
                 const float inv_l = lt > 0.f ? 1.f / lt : 0.f;

@@ -108,15 +108,37 @@ __device__ __forceinline__ bool mbar_wait_bounded_1(uint32_t bar, uint32_t parit
     }
 }
 
-// Warp-wide bounded wait: lane 0 polls the barrier (one shared-memory access
-// stream instead of 32), the result is broadcast, and __syncwarp orders the
-// other lanes' later accesses after lane 0's acquire.  Called by every lane.
+// Bounded wait used when a role winds down: it ignores the abort flag (the
+// copies or MMAs it waits for were issued and will complete), so shared
+// memory and TMEM are not released under them; it still gives up after the
+// limit and then sets the timeout bit.
+__device__ __forceinline__ bool mbar_wait_drain_1(uint32_t bar, uint32_t parity, unsigned int* err,
+                                                  uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(err, VSA_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Warp-wide bounded wait, called by every lane of a converged warp.  Fast
+// path: each lane tests the barrier itself (one shared-memory access for the
+// warp, and each lane gets its own acquire); a vote keeps the lanes together.  Slow path: lane 0 polls with
+// the time limit, the result is broadcast, and the other lanes then take
+// their own acquire with one more test (the phase stays complete: no
+// protocol here lets a barrier run two phases ahead of a waiter).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort, unsigned int* err,
                                                   uint64_t limit_ns) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     int ok = 1;
     if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded_1(bar, parity, abort, err, limit_ns) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok && (threadIdx.x & 31) != 0) mbar_try_wait(bar, parity);
     __syncwarp();
     return ok != 0;
 }
@@ -240,6 +262,48 @@ __device__ __forceinline__ void mma_ts_lohi(uint32_t d_tmem, uint32_t a_tmem, ui
         "setp.ne.b32 p, %5, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Warp-wide forms of mma_ss_lohi / mma_ts_lohi: called by all 32 lanes with
+// the same (warp-uniform) operands; lane 0 issues the MMA (always the same
+// lane, so its tcgen05.commit covers every MMA of the warp).  Keeping the
+// issuing code warp-uniform lets the compiler hold descriptors in uniform
+// registers, which keeps the issue rate up when other warps on the same
+// scheduler are busy.
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                            uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t.reg .b32 t;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "mov.u32 t, %%laneid;\n\t"
+        "setp.eq.u32 e, t, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\t.reg .b32 t;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.u32 t, %%laneid;\n\t"
+        "setp.eq.u32 e, t, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Warp-wide tcgen05.commit: lane 0 arrives on the mbarrier once the MMAs it
+// issued so far complete.
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 t;\n\t"
+        "mov.u32 t, %%laneid;\n\t"
+        "setp.eq.u32 e, t, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
         : "memory");
 }
 
