@@ -95,7 +95,7 @@ struct __align__(16) Misc {
     uint64_t q_empty;
     uint64_t list_full[2];
     uint64_t list_empty[2];
-    uint64_t drain;
+    uint64_t drain[2];  // per MMA-issuing warp
     int list_count[2];
     float xmax[2][2][128];        // [step parity][key half][row]: row maxima exchanged by thread pairs
     float xsum[2][128];           // [key half][row]: partial row sums for the epilogue
@@ -279,7 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&ms.pv_done), 1);
         mbar_init(smem_u32(&ms.q_full), kSoftmaxWarps);
         mbar_init(smem_u32(&ms.q_empty), 1);
-        mbar_init(smem_u32(&ms.drain), 1);
+        mbar_init(smem_u32(&ms.drain[0]), 1);
+        mbar_init(smem_u32(&ms.drain[1]), 1);
         ms.abort_flag = 0;
         fence_barrier_init();
     }
@@ -376,28 +377,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) drain_ring<kVStages>(ms.v_full, g, p.err);
         __syncwarp();
-    } else if (warp == 1) {
-        // ============================================================ MMA issuer
-        // The whole warp walks the schedule with warp-uniform values; lane 0
-        // issues every MMA and commit.  QK(g) writes S buffer g & 1 once the
-        // softmax has loaded S(g - 2) from it, so QK runs two steps ahead of
-        // PV; the order is QK(0), QK(1), then per step g: PV(g), QK(g + 2).
-        // PV(g) reads P from its own TMEM columns, which the softmax rewrites
-        // for step g + 1 only after PV(g) completes.  Descriptors are
-        // precomputed; each MMA adds a constant to the start-address field of
-        // the low word (no carry: shared addresses are below 256 KB).
+    } else if (warp == 1 || warp == 3) {
+        // ============================================================ MMA issuers
+        // Two warps issue MMAs, each warp-wide with lane 0 issuing and
+        // committing: warp 1 the QK stream, warp 3 the PV stream.  The streams
+        // touch disjoint TMEM (S vs P and O) and are ordered only through the
+        // softmax: QK(g) writes S buffer g & 1 once the softmax has loaded
+        // S(g - 2) from it (so QK runs up to two steps ahead of the softmax),
+        // and PV(g) reads P(g), which the softmax writes once PV(g - 1) has
+        // completed.  Descriptors are precomputed; each MMA adds a constant to
+        // the start-address field of the low word (no carry: shared addresses
+        // are below 256 KB).
         if (my_units > 0) {
-            const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
-            const uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
             const uint32_t hi = (uint32_t)(smem_desc_sw128(0, 16, 1024) >> 32);  // SBO, version, swizzle
-            const uint32_t lo_k = (uint32_t)smem_desc_sw128(sbase + kOffK, 16, 1024);
-            const uint32_t lo_v = (uint32_t)smem_desc_sw128(sbase + kOffV, kChunkRows128, 1024);
-            constexpr int ksteps_qk = D / 16;
             bool ok = true;
-            uint32_t g = 0;    // next PV step (global)
-            uint32_t gq = 0;   // next QK step (global)
-            int ul_q = 0, t_q = 0, cnt_q = 0;  // unit / step cursor of the QK stream
-            int ul_p = 0, t_p = 0, cnt_p = 0;  // unit / step cursor of the PV stream
             // Count of the list of local unit ul (waits for the list), warp-uniform.
             auto list_count = [&](int ul) -> int {
                 if (!mbar_wait_bounded(smem_u32(&ms.list_full[ul & 1]), (ul >> 1) & 1, abort_flag, p.err,
@@ -405,83 +398,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return -1;
                 return __shfl_sync(0xffffffffu, ms.list_count[ul & 1], 0);
             };
-            auto issue_qk = [&]() -> bool {
-                if (t_q == 0) {
-                    cnt_q = list_count(ul_q);
-                    if (cnt_q < 0) return false;
-                    if (!mbar_wait_bounded(smem_u32(&ms.q_full), ul_q & 1, abort_flag, p.err, kWaitLimitNs))
-                        return false;
-                }
-                if (gq >= 2 && !mbar_wait_bounded(smem_u32(&ms.s_free[gq & 1]), ((gq >> 1) + 1) & 1, abort_flag,
-                                                  p.err, kWaitLimitNs))
-                    return false;
-                const int slot = gq % kKStages;
-                if (!mbar_wait_bounded(smem_u32(&ms.k_full[slot]), (gq / kKStages) & 1, abort_flag, p.err,
-                                       kWaitLimitNs))
-                    return false;
-                const uint32_t b0 = lo_k + ((uint32_t)(slot * kPairBytes) >> 4);
-                const uint32_t a0 = tmem + kTmemQ;
-                const uint32_t d_tmem = tmem + kTmemS + (gq & 1) * 128;
-                tc_fence_after();
+            if (warp == 1) {
+                const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
+                const uint32_t lo_k = (uint32_t)smem_desc_sw128(sbase + kOffK, 16, 1024);
+                constexpr int ksteps_qk = D / 16;
+                uint32_t gq = 0;  // QK step (global)
+                for (int ul = 0; ul < my_units && ok; ++ul) {
+                    const int cnt = list_count(ul);
+                    if (cnt < 0) break;
+                    const int nst = (cnt + 1) >> 1;
+                    ok = mbar_wait_bounded(smem_u32(&ms.q_full), ul & 1, abort_flag, p.err, kWaitLimitNs);
+                    for (int t = 0; t < nst && ok; ++t, ++gq) {
+                        if (gq >= 2)
+                            ok = mbar_wait_bounded(smem_u32(&ms.s_free[gq & 1]), ((gq >> 1) + 1) & 1, abort_flag,
+                                                   p.err, kWaitLimitNs);
+                        const int slot = gq % kKStages;
+                        if (ok)
+                            ok = mbar_wait_bounded(smem_u32(&ms.k_full[slot]), (gq / kKStages) & 1, abort_flag,
+                                                   p.err, kWaitLimitNs);
+                        if (!ok) break;
+                        const uint32_t b0 = lo_k + ((uint32_t)(slot * kPairBytes) >> 4);
+                        const uint32_t a0 = tmem + kTmemQ;
+                        const uint32_t d_tmem = tmem + kTmemS + (gq & 1) * 128;
+                        tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < ksteps_qk; ++kk)
-                    mma_ts_warp(d_tmem, a0 + kk * 8, b0 + (((kk >> 2) * kChunkRows128 + (kk & 3) * 32) >> 4), hi,
-                                idesc_qk, kk > 0);
-                mma_commit_warp(smem_u32(&ms.s_full[gq & 1]));
-                mma_commit_warp(smem_u32(&ms.k_empty[slot]));
-                ++gq;
-                if (++t_q == (cnt_q + 1) >> 1) {
-                    mma_commit_warp(smem_u32(&ms.q_empty));  // the unit's Q is no longer read
-                    t_q = 0;
-                    ++ul_q;
+                        for (int kk = 0; kk < ksteps_qk; ++kk)
+                            mma_ts_warp(d_tmem, a0 + kk * 8,
+                                        b0 + (((kk >> 2) * kChunkRows128 + (kk & 3) * 32) >> 4), hi, idesc_qk,
+                                        kk > 0);
+                        mma_commit_warp(smem_u32(&ms.s_full[gq & 1]));
+                        mma_commit_warp(smem_u32(&ms.k_empty[slot]));
+                    }
+                    if (ok) mma_commit_warp(smem_u32(&ms.q_empty));  // the unit's Q is no longer read
                 }
-                return true;
-            };
-            auto issue_pv = [&]() -> bool {
-                if (t_p == 0) {
-                    cnt_p = list_count(ul_p);
-                    if (cnt_p < 0) return false;
-                }
-                const int slot = g % kVStages;
-                if (!mbar_wait_bounded(smem_u32(&ms.p_full), g & 1, abort_flag, p.err, kWaitLimitNs) ||
-                    !mbar_wait_bounded(smem_u32(&ms.v_full[slot]), (g / kVStages) & 1, abort_flag, p.err,
-                                       kWaitLimitNs))
-                    return false;
-                const uint32_t b0 = lo_v + ((uint32_t)(slot * kPairBytes) >> 4);
-                const uint32_t a0 = tmem + kTmemP;
-                tc_fence_after();
+            } else {
+                const uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
+                const uint32_t lo_v = (uint32_t)smem_desc_sw128(sbase + kOffV, kChunkRows128, 1024);
+                uint32_t g = 0;  // PV step (global)
+                for (int ul = 0; ul < my_units && ok; ++ul) {
+                    const int cnt = list_count(ul);
+                    if (cnt < 0) break;
+                    const int nst = (cnt + 1) >> 1;
+                    for (int t = 0; t < nst && ok; ++t, ++g) {
+                        const int slot = g % kVStages;
+                        ok = mbar_wait_bounded(smem_u32(&ms.p_full), g & 1, abort_flag, p.err, kWaitLimitNs) &&
+                             mbar_wait_bounded(smem_u32(&ms.v_full[slot]), (g / kVStages) & 1, abort_flag, p.err,
+                                               kWaitLimitNs);
+                        if (!ok) break;
+                        const uint32_t b0 = lo_v + ((uint32_t)(slot * kPairBytes) >> 4);
+                        const uint32_t a0 = tmem + kTmemP;
+                        tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_warp(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv,
-                                (t_p > 0 || kk > 0));
-                if (2 * t_p + 1 < cnt_p) {  // the second cube of the step (a single-cube step has 64 keys)
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ts_warp(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv,
+                                        (t > 0 || kk > 0));
+                        if (2 * t + 1 < cnt) {  // the second cube of the step (a single-cube step has 64 keys)
 #pragma unroll
-                    for (int kk = 4; kk < 8; ++kk)
-                        mma_ts_warp(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv, 1u);
-                }
-                mma_commit_warp(smem_u32(&ms.pv_done));
-                mma_commit_warp(smem_u32(&ms.v_empty[slot]));
-                if (++t_p == (cnt_p + 1) >> 1) {
-                    // The MMA side is done with this unit's list.
+                            for (int kk = 4; kk < 8; ++kk)
+                                mma_ts_warp(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv, 1u);
+                        }
+                        mma_commit_warp(smem_u32(&ms.pv_done));
+                        mma_commit_warp(smem_u32(&ms.v_empty[slot]));
+                    }
+                    // This issuer is done with the unit's list.
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[ul_p & 1]));
-                    t_p = 0;
-                    ++ul_p;
+                    if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[ul & 1]));
                 }
-                ++g;
-                return true;
-            };
-            ok = issue_qk();
-            if (ok && ul_q < my_units) ok = issue_qk();
-            while (ok && ul_p < my_units) {
-                // PV(g) first: the softmax writes P(g + 1) once PV(g) completes, so
-                // PV(g) goes to the tensor pipe ahead of QK(g + 2).
-                ok = issue_pv();
-                if (ok && ul_q < my_units) ok = issue_qk();
             }
-            // Drain: all issued MMAs complete before TMEM is released.
-            mma_commit_warp(smem_u32(&ms.drain));
-            if (lane == 0) mbar_wait_drain_1(smem_u32(&ms.drain), 0, p.err, kWaitLimitNs);
+            // Drain: every MMA this warp issued completes before TMEM is released.
+            mma_commit_warp(smem_u32(&ms.drain[warp == 1 ? 0 : 1]));
+            if (lane == 0) mbar_wait_drain_1(smem_u32(&ms.drain[warp == 1 ? 0 : 1]), 0, p.err, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp >= kFirstSoftmaxWarp) {
