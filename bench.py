@@ -49,9 +49,9 @@ KERNELS_PER_STEP = 7  # tile x3, pool sums, score/top-k, sparse attention, until
 # was taken from: if fine.cu no longer hashes to `source_sha256`, the traffic is reported
 # as null.
 FINE_TRAFFIC = {
-    "bytes_per_launch": (247.728128e6 + 66.110208e6) * 40 / 8,
+    "bytes_per_launch": (247.233792e6 + 67.947264e6) * 40 / 8,
     "capture": "profiles/fine_fwd_kernel_wan.md",
-    "source_sha256": "5aa99b4c3ad89a6f3bdbc6fa376710911f4008e7bad20a8f052d8b1b916defbe",
+    "source_sha256": "cb88cefd773f05c9fd830549513351fef64369c2c8c8d620ab48214210351242",
 }
 
 

@@ -22,13 +22,15 @@
 //  * Persistent grid, one CTA per SM, units dealt round-robin in head-major
 //    order so one head's K/V stays in L2.
 //  * Warp roles (384 threads): warp 0 builds each unit's union list (sorted,
-//    with membership bits and vbs) and is the TMA producer of K; warp 1 issues
-//    all MMAs and owns TMEM; warp 2 is the TMA producer of V; warps 4..11 run
-//    the softmax and stage Q into TMEM.  A query row is shared by two threads
-//    (two warps on the same TMEM lane quarter), one per key cube of the step;
-//    they exchange their row maxima through shared memory with a 64-thread
-//    named barrier, so the running max, the sum and the lazy rescale of the
-//    row's O need no wider synchronisation.
+//    with membership bits and vbs) and is the TMA producer of K; warp 1 owns
+//    TMEM and issues the Q.K^T MMAs; warp 2 is the TMA producer of V; warp 3
+//    issues the P.V MMAs; warps 4..11 run the softmax and stage Q into TMEM.
+//    Each MMA-issuing warp runs its loop as a whole warp and lets lane 0
+//    issue, so its waits and loop state stay warp-uniform.  A query row is
+//    shared by two threads (two warps on the same TMEM lane quarter), one per
+//    key cube of the step; they exchange their row maxima through shared
+//    memory with a 64-thread named barrier, so the running max, the sum and
+//    the lazy rescale of the row's O need no wider synchronisation.
 //  * TMEM (512 columns): S double buffer [0,128) [128,256); P of the current
 //    step (bf16 pairs) [256,320); Q of the current unit [320,384); O
 //    [384,512).  The softmax releases an S buffer as soon as it has loaded
