@@ -41,7 +41,7 @@ if HERE not in sys.path:
 METRIC = "VSA sparse-attn fwd ms/call and effective TFLOPS; % of GB300 bf16 TC peak"
 UNIT = "TFLOPS (effective)"
 WORKLOAD = "wan"
-KERNELS_PER_STEP = 7  # tile x3, pool sums, score/top-k, sparse attention, untile
+KERNELS_PER_STEP = 10  # tile x3, pool sums, score/top-k, pairing x3, sparse attention, untile
 
 # DRAM traffic of one fine_fwd_kernel launch, from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum) of the Wan grid with 8 heads, scaled by 40/8 (traffic grows with
@@ -211,7 +211,8 @@ def stage_bytes(wl):
     real = wl.B * wl.tokens * wl.heads * wl.D * 2
     tiled = wl.B * wl.s_pad * wl.heads * wl.D * 2
     return {
-        "tile_qkv": 3 * (real + tiled),                      # read raster rows, write every slot
+        "tile_qk": 2 * (real + tiled),                       # read raster rows, write every slot
+        "tile_v": real + tiled,                              # side stream, beside the pairing
         "coarse_select": 2 * tiled + 4 * wl.B * wl.heads * wl.ncubes * wl.topk,  # read q, k; write idx
         "untile": 2 * real,                                  # read real slots, write raster rows
     }
@@ -260,27 +261,50 @@ def run_ours(args, wl, inputs, rank, world, dist):
     idx = torch.empty((wl.B, wl.heads, N, wl.topk), dtype=torch.int32, device=dev)
     ws = torch.empty((vsa.coarse_workspace_bytes(wl.B, wl.heads, N, wl.D),), dtype=torch.uint8, device=dev)
     lse = torch.empty((wl.B, wl.heads, wl.s_pad), dtype=torch.float32, device=dev)
+    pws = torch.empty((vsa.pair_workspace_bytes(wl.B, wl.heads, N, wl.topk),), dtype=torch.uint8, device=dev)
+    pairs = torch.empty((wl.B, wl.heads, (N + 1) // 2), dtype=torch.int32, device=dev)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
-    def step(marks=None):
+    # Tiling v needs neither the coarse selection nor the pairing, so it runs on
+    # a side stream while the pairing kernels (one CTA per head) run.
+    side = torch.cuda.Stream()
+    ev_coarse, ev_v = torch.cuda.Event(), torch.cuda.Event()
+
+    def step(marks=None, qin=None, kin=None, vin=None, oout=None):
+        qin = q if qin is None else qin
+        kin = k if kin is None else kin
+        vin = v if vin is None else vin
+        oout = out if oout is None else oout
         if marks is not None:
             marks[0].record(stream)
-        vsa.tile(q, grid, out=qt, vbs=vbs)
-        vsa.tile(k, grid, out=kt, vbs=vbs2)
-        vsa.tile(v, grid, out=vt, vbs=vbs2)
+        vsa.tile(qin, grid, out=qt, vbs=vbs)
+        vsa.tile(kin, grid, out=kt, vbs=vbs2)
         if marks is not None:
             marks[1].record(stream)
         vsa.coarse_select(qt, kt, vbs, wl.topk, wl.sm_scale, workspace=ws, out=idx)
+        ev_coarse.record(stream)
         if marks is not None:
             marks[2].record(stream)
-        vsa.sparse_attn_fwd(qt, kt, vt, idx, vbs, wl.sm_scale, out=ot, lse=lse)
+        side.wait_event(ev_coarse)
+        with torch.cuda.stream(side):
+            if marks is not None:
+                marks[6].record(side)
+            vsa.tile(vin, grid, out=vt, vbs=vbs2)
+            if marks is not None:
+                marks[7].record(side)
+            ev_v.record(side)
+        vsa.pair_cubes(idx, workspace=pws, out=pairs)
         if marks is not None:
             marks[3].record(stream)
-        vsa.untile(ot, grid, out=out)
+        stream.wait_event(ev_v)
+        vsa.sparse_attn_fwd(qt, kt, vt, idx, vbs, wl.sm_scale, out=ot, lse=lse, pairs=pairs)
         if marks is not None:
             marks[4].record(stream)
+        vsa.untile(ot, grid, out=oout)
+        if marks is not None:
+            marks[5].record(stream)
 
     clk = ClockSampler(torch.cuda.current_device())
     with clk:
@@ -290,7 +314,7 @@ def run_ours(args, wl, inputs, rank, world, dist):
         if vsa.device_error(reset=True):
             raise RuntimeError("device error word set during warm-up")
 
-        marks = [[ev() for _ in range(5)] for _ in range(args.steps)]
+        marks = [[ev() for _ in range(8)] for _ in range(args.steps)]
         start, end = ev(), ev()
         if dist:
             dist.barrier()
@@ -311,7 +335,8 @@ def run_ours(args, wl, inputs, rank, world, dist):
         ms_total = float(t.item())
     ms_step = ms_total / args.steps
     stage = {name: [marks[s][i].elapsed_time(marks[s][i + 1]) for s in range(args.steps)]
-             for i, name in enumerate(["tile_qkv", "coarse_select", "sparse_attn_fwd", "untile"])}
+             for i, name in enumerate(["tile_qk", "coarse_select", "pair_cubes", "sparse_attn_fwd", "untile"])}
+    stage["tile_v"] = [marks[s][6].elapsed_time(marks[s][7]) for s in range(args.steps)]  # side stream
     if vsa.device_error(reset=True):
         raise RuntimeError("device error word set during the timed run")
 
@@ -349,12 +374,7 @@ def run_ours(args, wl, inputs, rank, world, dist):
             stream.wait_event(up[bb])
             if i >= 2:
                 stream.wait_event(down[bb])  # the read-back of step i - 2 has left this output set
-            vsa.tile(dq[bb], grid, out=qt, vbs=vbs)
-            vsa.tile(dk[bb], grid, out=kt, vbs=vbs2)
-            vsa.tile(dv[bb], grid, out=vt, vbs=vbs2)
-            vsa.coarse_select(qt, kt, vbs, wl.topk, wl.sm_scale, workspace=ws, out=idx)
-            vsa.sparse_attn_fwd(qt, kt, vt, idx, vbs, wl.sm_scale, out=ot, lse=lse)
-            vsa.untile(ot, grid, out=douts[bb])
+            step(qin=dq[bb], kin=dk[bb], vin=dv[bb], oout=douts[bb])
             done[bb].record(stream)
             s_down.wait_event(done[bb])
             with torch.cuda.stream(s_down):

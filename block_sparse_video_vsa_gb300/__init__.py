@@ -63,6 +63,13 @@ def _declare(lib):
     lib.vsa_sparse_attn_fwd.restype = ctypes.c_int
     lib.vsa_sparse_attn_fwd.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_float,
                                         _p, _p, _p]
+    lib.vsa_sparse_attn_fwd_paired.restype = ctypes.c_int
+    lib.vsa_sparse_attn_fwd_paired.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32,
+                                               ctypes.c_float, _p, _p, _p]
+    lib.vsa_pair_workspace_bytes.restype = ctypes.c_size_t
+    lib.vsa_pair_workspace_bytes.argtypes = [_i32] * 4
+    lib.vsa_pair_cubes.restype = ctypes.c_int
+    lib.vsa_pair_cubes.argtypes = [_p, _i32, _i32, _i32, _i32, _p, _p, _p]
     lib.vsa_validate_indices.restype = ctypes.c_int
     lib.vsa_validate_indices.argtypes = [_p, _p, _i32, _i32, _i32, _i32, _p, _p]
     lib.vsa_device_error.restype = ctypes.c_int
@@ -188,9 +195,42 @@ def coarse_select(qt, kt, vbs, topk: int, sm_scale: float = 0.0, workspace=None,
     return out
 
 
+def pair_workspace_bytes(B: int, heads: int, ncubes: int, topk: int) -> int:
+    return int(library().vsa_pair_workspace_bytes(B, heads, ncubes, topk))
+
+
+def pair_cubes(topk_idx, workspace=None, out=None, stream=None):
+    """Query-cube pairing for the fine stage -> int32 [B, heads, (N + 1) // 2].
+
+    Each entry holds the uint32 bit pattern i | (j << 16) (j = 0xFFFF: single
+    cube); see vsa_pair_cubes."""
+    torch = _torch()
+    _need(topk_idx, torch.int32, "topk_idx")
+    if topk_idx.dim() != 4:
+        raise ValueError("topk_idx must be [B, heads, N, topk]")
+    B, heads, N, topk = topk_idx.shape
+    nbytes = pair_workspace_bytes(B, heads, N, topk)
+    if workspace is None:
+        workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=topk_idx.device)
+    _need(workspace, torch.uint8, "workspace")
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    if out is None:
+        out = torch.empty((B, heads, (N + 1) // 2), dtype=torch.int32, device=topk_idx.device)
+    _need(out, torch.int32, "out")
+    if tuple(out.shape) != (B, heads, (N + 1) // 2):
+        raise ValueError("out must be [B, heads, (N + 1) // 2]")
+    _check(library().vsa_pair_cubes(topk_idx.data_ptr(), B, N, heads, topk, workspace.data_ptr(),
+                                    out.data_ptr(), _stream(stream)), "vsa_pair_cubes")
+    return out
+
+
 def sparse_attn_fwd(qt, kt, vt, topk_idx, vbs, sm_scale: float = 0.0, out=None, lse=None,
-                    want_lse: bool = True, stream=None):
-    """Block-sparse attention -> (out bf16 [B, 64*N, heads, D], lse fp32 [B, heads, 64*N] or None)."""
+                    want_lse: bool = True, pairs=None, stream=None):
+    """Block-sparse attention -> (out bf16 [B, 64*N, heads, D], lse fp32 [B, heads, 64*N] or None).
+
+    `pairs` (from pair_cubes) sets which query cubes share a tile; None pairs
+    cubes (2u, 2u + 1).  The results do not depend on it beyond rounding."""
     torch = _torch()
     for t, n in ((qt, "qt"), (kt, "kt"), (vt, "vt")):
         _need(t, torch.bfloat16, n)
@@ -210,9 +250,14 @@ def sparse_attn_fwd(qt, kt, vt, topk_idx, vbs, sm_scale: float = 0.0, out=None, 
         lse = torch.empty((B, heads, S), dtype=torch.float32, device=qt.device)
     if lse is not None:
         _need(lse, torch.float32, "lse")
-    _check(library().vsa_sparse_attn_fwd(qt.data_ptr(), kt.data_ptr(), vt.data_ptr(), topk_idx.data_ptr(),
-                                         vbs.data_ptr(), B, N, heads, D, topk, float(sm_scale), out.data_ptr(),
-                                         lse.data_ptr() if lse is not None else None, _stream(stream)),
+    if pairs is not None:
+        _need(pairs, torch.int32, "pairs")
+        if tuple(pairs.shape) != (B, heads, (N + 1) // 2):
+            raise ValueError("pairs must be [B, heads, (N + 1) // 2]")
+    _check(library().vsa_sparse_attn_fwd_paired(qt.data_ptr(), kt.data_ptr(), vt.data_ptr(), topk_idx.data_ptr(),
+                                                vbs.data_ptr(), pairs.data_ptr() if pairs is not None else None,
+                                                B, N, heads, D, topk, float(sm_scale), out.data_ptr(),
+                                                lse.data_ptr() if lse is not None else None, _stream(stream)),
            "vsa_sparse_attn_fwd")
     return out, lse
 
@@ -245,12 +290,13 @@ def debug_wait_timeout(limit_ns: int, stream=None) -> int:
 
 
 def pipeline(q, k, v, grid, topk: int, sm_scale: float = 0.0, stream=None):
-    """Whole hot path on raster inputs: tile -> coarse select -> sparse attention -> untile.
+    """Whole hot path on raster inputs: tile -> coarse select -> (pairing) -> sparse attention -> untile.
 
     Returns (out raster bf16, lse fp32 [B, heads, 64*N] in cube-major order, topk_idx)."""
     qt, vbs = tile(q, grid, stream=stream)
     kt, _ = tile(k, grid, vbs=_torch().empty_like(vbs), stream=stream)
     vt, _ = tile(v, grid, vbs=_torch().empty_like(vbs), stream=stream)
     idx = coarse_select(qt, kt, vbs, topk, sm_scale, stream=stream)
-    ot, lse = sparse_attn_fwd(qt, kt, vt, idx, vbs, sm_scale, stream=stream)
+    pairs = pair_cubes(idx, stream=stream)
+    ot, lse = sparse_attn_fwd(qt, kt, vt, idx, vbs, sm_scale, pairs=pairs, stream=stream)
     return untile(ot, grid, stream=stream), lse, idx

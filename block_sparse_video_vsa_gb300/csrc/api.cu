@@ -136,9 +136,10 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
                                    static_cast<cudaStream_t>(stream)));
 }
 
-vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
-                               const int32_t* vbs, int32_t B, int32_t ncubes, int32_t heads, int32_t D,
-                               int32_t topk, float sm_scale, void* out, float* lse, vsa_stream_t stream) {
+vsa_status vsa_sparse_attn_fwd_paired(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                                      const int32_t* vbs, const uint32_t* pairs, int32_t B, int32_t ncubes,
+                                      int32_t heads, int32_t D, int32_t topk, float sm_scale, void* out, float* lse,
+                                      vsa_stream_t stream) {
     if (!qt || !kt || !vt || !topk_idx || !vbs || !out) return VSA_ERR_INVALID_ARG;
     if (B <= 0 || ncubes <= 0 || heads <= 0 || topk <= 0 || topk > ncubes) return VSA_ERR_INVALID_ARG;
     if (!(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
@@ -150,15 +151,43 @@ vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt, c
     if (topk > fine_max_topk() || ncubes > fine_max_cubes()) return VSA_ERR_UNSUPPORTED;
     if (!aligned16(qt) || !aligned16(kt) || !aligned16(vt) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(vbs) & 3u) ||
-        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        (reinterpret_cast<uintptr_t>(pairs) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return VSA_ERR_ALIGNMENT;
     DevCtx ctx;
     cudaError_t e = get_dev_ctx(&ctx);
     if (e != cudaSuccess) return VSA_ERR_CUDA;
     if (fine_smem_bytes() > ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
-    return from_cuda(launch_fine(qt, kt, vt, topk_idx, vbs, B, ncubes, heads, D, topk, sm_scale, out, lse,
-                                 ctx.err, ctx.num_sms, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_fine(qt, kt, vt, topk_idx, vbs, pairs, B, ncubes, heads, D, topk, sm_scale, out,
+                                 lse, ctx.err, ctx.num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                               const int32_t* vbs, int32_t B, int32_t ncubes, int32_t heads, int32_t D,
+                               int32_t topk, float sm_scale, void* out, float* lse, vsa_stream_t stream) {
+    return vsa_sparse_attn_fwd_paired(qt, kt, vt, topk_idx, vbs, nullptr, B, ncubes, heads, D, topk, sm_scale,
+                                      out, lse, stream);
+}
+
+size_t vsa_pair_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t topk) {
+    if (B <= 0 || heads <= 0 || ncubes <= 0 || topk <= 0) return 0;
+    return pair_workspace_bytes(B, heads, ncubes, topk);
+}
+
+vsa_status vsa_pair_cubes(const int32_t* topk_idx, int32_t B, int32_t ncubes, int32_t heads, int32_t topk,
+                          void* workspace, uint32_t* pairs, vsa_stream_t stream) {
+    if (!topk_idx || !workspace || !pairs) return VSA_ERR_INVALID_ARG;
+    if (B <= 0 || ncubes <= 0 || heads <= 0 || topk <= 0 || topk > ncubes) return VSA_ERR_INVALID_ARG;
+    if (ncubes > pair_max_cubes() || topk > pair_max_topk() || (int64_t)B * heads * ncubes >= ((int64_t)1 << 31) ||
+        (int64_t)B * heads * ncubes * topk >= ((int64_t)1 << 40))
+        return VSA_ERR_UNSUPPORTED;
+    if (!aligned16(workspace) || (reinterpret_cast<uintptr_t>(topk_idx) & 3u) ||
+        (reinterpret_cast<uintptr_t>(pairs) & 3u))
+        return VSA_ERR_ALIGNMENT;
+    DevCtx ctx;
+    if (get_dev_ctx(&ctx) != cudaSuccess) return VSA_ERR_CUDA;
+    return from_cuda(launch_pair(topk_idx, B, ncubes, heads, topk, workspace, pairs, ctx.num_sms,
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 vsa_status vsa_validate_indices(const int32_t* topk_idx, const int32_t* vbs, int32_t B, int32_t heads,

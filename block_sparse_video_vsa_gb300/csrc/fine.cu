@@ -112,6 +112,7 @@ static_assert(kSmemAlloc <= 232448, "fine kernel shared memory exceeds the sm_10
 struct FineParams {
     const int32_t* topk_idx;
     const int32_t* vbs;
+    const uint32_t* pairs;  // [B * heads][npairs]: i | (j << 16), j = 0xFFFF single; or null: (2u, 2u + 1)
     const uint4* q;      // tiled q rows (for staging Q into TMEM)
     __nv_bfloat16* out;
     float* lse;
@@ -129,25 +130,43 @@ __device__ __forceinline__ void unit_coords(int u, const FineParams& p, int& b, 
     b = bh / p.heads;
 }
 
+// Query cubes of unit `pair` of (b, h); -1 for none.
+__device__ __forceinline__ void unit_cubes(const FineParams& p, int b, int h, int pair, int& i0, int& i1) {
+    if (p.pairs) {
+        const uint32_t e = __ldg(p.pairs + ((size_t)b * p.heads + h) * p.npairs + pair);
+        i0 = (int)(e & 0xFFFFu);
+        i1 = (int)(e >> 16);
+    } else {
+        i0 = 2 * pair;
+        i1 = 2 * pair + 1;
+    }
+    if (i0 >= p.N) i0 = -1;
+    if (i1 >= p.N) i1 = -1;
+}
+
 // Builds the sorted union of the two query cubes' selections (one warp).
 __device__ int build_union(const FineParams& p, int u, uint32_t* list, uint32_t* bm0, uint32_t* bm1, int lane) {
     int b, h, pair;
     unit_coords(u, p, b, h, pair);
     const int N = p.N, k = p.topk;
     const int nwords = (N + 31) >> 5;
-    const int i0 = 2 * pair, i1 = 2 * pair + 1;
+    int i0, i1;
+    unit_cubes(p, b, h, pair, i0, i1);
     for (int w = lane; w < nwords; w += 32) {
         bm0[w] = 0u;
         bm1[w] = 0u;
     }
     __syncwarp();
-    const int32_t* r0 = p.topk_idx + (((size_t)b * p.heads + h) * N + i0) * (size_t)k;
-    for (int e = lane; e < k; e += 32) {
-        const int j = __ldg(r0 + e);
-        atomicOr(&bm0[j >> 5], 1u << (j & 31));
+    const int32_t* rows = p.topk_idx + ((size_t)b * p.heads + h) * N * (size_t)k;
+    if (i0 >= 0) {
+        const int32_t* r0 = rows + (size_t)i0 * k;
+        for (int e = lane; e < k; e += 32) {
+            const int j = __ldg(r0 + e);
+            atomicOr(&bm0[j >> 5], 1u << (j & 31));
+        }
     }
-    if (i1 < N) {
-        const int32_t* r1 = r0 + k;
+    if (i1 >= 0) {
+        const int32_t* r1 = rows + (size_t)i1 * k;
         for (int e = lane; e < k; e += 32) {
             const int j = __ldg(r1 + e);
             atomicOr(&bm1[j >> 5], 1u << (j & 31));
@@ -209,12 +228,14 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t issued, unsi
 __device__ __forceinline__ void stage_q(const FineParams& p, int u, int row_in_pair, uint32_t t_lane, int hf) {
     int b, h, pair;
     unit_coords(u, p, b, h, pair);
-    const int i = 2 * pair + (row_in_pair >> 6);
+    int i0, i1;
+    unit_cubes(p, b, h, pair, i0, i1);
+    const int i = (row_in_pair >> 6) ? i1 : i0;
     const int D = p.D;
     const int words = D / 2;  // 32-bit columns of a full row
     uint32_t w[32];
     for (int c0 = hf * 32; c0 < words && c0 < hf * 32 + 32; c0 += 32) {
-        if (i < p.N) {
+        if (i >= 0) {
             const size_t row = (size_t)b * p.N * kCubeTokens + (size_t)i * kCubeTokens + (row_in_pair & 63);
             const uint4* src = p.q + (row * p.heads + h) * (size_t)(D / 8) + c0 / 4;
 #pragma unroll
@@ -602,7 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------------ unit epilogue
             int b, h, pair;
             unit_coords(u, p, b, h, pair);
-            const int i = 2 * pair + (r >> 6);
+            int i0, i1;
+            unit_cubes(p, b, h, pair, i0, i1);
+            const int i = (r >> 6) ? i1 : i0;
             ms.xsum[hf][r] = l;
             named_sync(1 + quarter, 64);
             const float lt = l + ms.xsum[hf ^ 1][r];
@@ -617,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t o[32];
                     tmem_ld32(t_lane + kTmemO + c0, o);
                     tmem_wait_ld();
-                    if (i < p.N) {
+                    if (i >= 0) {
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint4 w;
@@ -629,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (p.lse && i < p.N && hf == 0)
+                if (p.lse && i >= 0 && hf == 0)
                     p.lse[((size_t)b * p.heads + h) * s_pad + (size_t)i * kCubeTokens + (r & 63)] =
                         lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : ninf;
             }
@@ -685,8 +708,9 @@ int fine_max_topk() { return kMaxTopk; }
 int fine_max_cubes() { return kMaxCubes; }
 
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
-                        const int32_t* vbs, int B, int ncubes, int heads, int D, int topk, float sm_scale,
-                        void* out, float* lse, unsigned int* err, int num_sms, cudaStream_t stream) {
+                        const int32_t* vbs, const uint32_t* pairs, int B, int ncubes, int heads, int D, int topk,
+                        float sm_scale, void* out, float* lse, unsigned int* err, int num_sms,
+                        cudaStream_t stream) {
     CUtensorMap mk, mv;
     const int rows = B * ncubes * kCubeTokens;
     if (!make_map(&mk, kt, rows, heads, D, true) || !make_map(&mv, vt, rows, heads, D, true))
@@ -694,6 +718,7 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     FineParams p;
     p.topk_idx = topk_idx;
     p.vbs = vbs;
+    p.pairs = pairs;
     p.q = static_cast<const uint4*>(qt);
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;

@@ -32,7 +32,16 @@ int fine_smem_bytes();
 int fine_max_topk();
 int fine_max_cubes();
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
-                        const int32_t* vbs, int B, int ncubes, int heads, int D, int topk, float sm_scale,
-                        void* out, float* lse, unsigned int* err, int num_sms, cudaStream_t stream);
+                        const int32_t* vbs, const uint32_t* pairs, int B, int ncubes, int heads, int D, int topk,
+                        float sm_scale, void* out, float* lse, unsigned int* err, int num_sms,
+                        cudaStream_t stream);
+
+// pair.cu
+int pair_words(int ncubes);
+size_t pair_workspace_bytes(int B, int heads, int ncubes, int topk);
+int pair_max_cubes();
+int pair_max_topk();
+cudaError_t launch_pair(const int32_t* topk_idx, int B, int ncubes, int heads, int topk, void* workspace,
+                        uint32_t* pairs, int num_sms, cudaStream_t stream);
 
 }  // namespace vsa

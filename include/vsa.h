@@ -9,6 +9,8 @@
  *                          the top-k key/value cubes per query cube;
  *   3. vsa_sparse_attn_fwd non-causal block-sparse attention over the selected
  *                          cubes, padded tokens masked (bf16 out + fp32 LSE);
+ *      (vsa_pair_cubes     optional schedule for step 3: which query cubes
+ *                          share a tensor-core tile; results are unchanged)
  *   4. vsa_untile          the inverse permutation of step 1.
  *
  * Sources (page title, section):
@@ -187,6 +189,42 @@ vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt,
                                const int32_t* topk_idx, const int32_t* vbs, int32_t B,
                                int32_t ncubes, int32_t heads, int32_t D, int32_t topk,
                                float sm_scale, void* out, float* lse, vsa_stream_t stream);
+
+/*
+ * Schedule for the fine stage (no counterpart in the pages: a GB300 tiling
+ * choice that leaves every result unchanged).  The fine kernel processes
+ * query cubes in pairs, one 128-row tensor-core tile per pair, walking the
+ * union of the two cubes' selections; a pair costs ceil(|sel(i) u sel(j)| / 2)
+ * steps.  vsa_pair_cubes chooses, per (b, head), a pairing with large
+ * selection overlaps: mutual-best matching over each cube's own selection,
+ * then over a window of the unpaired cubes, the rest in index order
+ * (deterministic, integer only).
+ *   topk_idx  : int32 [B, heads, ncubes, topk], as for vsa_sparse_attn_fwd
+ *   workspace : device buffer of vsa_pair_workspace_bytes(...) bytes,
+ *               16-byte aligned, overwritten
+ *   pairs     : uint32 [B, heads, (ncubes + 1) / 2] (written): unit u holds
+ *               cubes i | (j << 16), i < j, j = 0xFFFF for a single cube;
+ *               units in increasing i; every cube appears exactly once
+ * Limits: ncubes <= 8192, topk <= 512.  Entries of topk_idx outside
+ * [0, ncubes) are ignored.
+ */
+size_t vsa_pair_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t topk);
+vsa_status vsa_pair_cubes(const int32_t* topk_idx, int32_t B, int32_t ncubes, int32_t heads,
+                          int32_t topk, void* workspace, uint32_t* pairs, vsa_stream_t stream);
+
+/*
+ * vsa_sparse_attn_fwd with the query-cube pairing given: `pairs` as written
+ * by vsa_pair_cubes (uint32 [B, heads, (ncubes + 1) / 2]), or NULL for the
+ * pairs (2u, 2u + 1).  A pairing must list every cube exactly once (cube
+ * indices >= ncubes mean "none"); the results are those of
+ * vsa_sparse_attn_fwd up to the order of floating-point accumulation.
+ * Same arguments, limits and errors otherwise.
+ */
+vsa_status vsa_sparse_attn_fwd_paired(const void* qt, const void* kt, const void* vt,
+                                      const int32_t* topk_idx, const int32_t* vbs,
+                                      const uint32_t* pairs, int32_t B, int32_t ncubes,
+                                      int32_t heads, int32_t D, int32_t topk, float sm_scale,
+                                      void* out, float* lse, vsa_stream_t stream);
 
 /*
  * Debug aid for the block-sparse encoding ([VSA-AMD] Block-Sparse Encoding):

@@ -36,7 +36,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("vsa_tile", "vsa_untile", "vsa_coarse_select", "vsa_sparse_attn_fwd",
               "vsa_coarse_workspace_bytes", "vsa_num_cubes", "vsa_status_string",
-              "vsa_validate_indices", "vsa_device_error", "vsa_debug_wait_timeout"):
+              "vsa_validate_indices", "vsa_device_error", "vsa_debug_wait_timeout",
+              "vsa_pair_cubes", "vsa_pair_workspace_bytes", "vsa_sparse_attn_fwd_paired"):
         assert n in names
 
 
@@ -100,6 +101,23 @@ def test_fine_validation(lib):
     assert f(A, A, A, A, A, 1, 12, 2, 256, 3, 0.0, A, None, None) == UNSUPPORTED
     assert f(A, A, MIS, A, A, 1, 12, 2, 64, 3, 0.0, A, None, None) == ALIGNMENT
     assert f(A, A, A, A, A, 1, 12, 2, 64, 3, 0.0, A, A + 2, None) == ALIGNMENT  # lse
+
+
+def test_pairing_validation(lib):
+    f = lib.vsa_pair_cubes
+    assert f(None, 1, 12, 2, 3, A, A, None) == INVALID
+    assert f(A, 1, 12, 2, 0, A, A, None) == INVALID       # topk = 0
+    assert f(A, 1, 12, 2, 13, A, A, None) == INVALID      # topk > ncubes
+    assert f(A, 1, 9000, 2, 3, A, A, None) == UNSUPPORTED  # ncubes > 8192
+    assert f(A, 1, 12, 2, 3, MIS, A, None) == ALIGNMENT   # workspace
+    assert f(A, 1, 12, 2, 3, A, A + 2, None) == ALIGNMENT  # pairs
+    # bitmaps: 4-word rows (12 cubes -> 1 word, rounded up to 4), then uint16 overlaps
+    assert lib.vsa_pair_workspace_bytes(1, 2, 12, 3) == 512 + 256  # 2*12*4*4 B -> 512, 2*12*3*2 B -> 256
+    wan = 40 * 624 * 20 * 4
+    assert lib.vsa_pair_workspace_bytes(1, 40, 624, 78) == (wan + 255) // 256 * 256 + (40 * 624 * 78 * 2 + 255) // 256 * 256
+    g = lib.vsa_sparse_attn_fwd_paired
+    assert g(A, A, A, A, A, A + 2, 1, 12, 2, 64, 3, 0.0, A, None, None) == ALIGNMENT  # pairs
+    assert g(A, A, A, A, A, None, 1, 12, 2, 64, 0, 0.0, A, None, None) == INVALID
 
 
 def test_validator_and_debug_validation(lib):

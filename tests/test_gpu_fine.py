@@ -2,9 +2,11 @@
 
 Both sides take the same topk_idx (the oracle's coarse selection, or a
 structured pattern).  Small workloads are compared element by element over
-every output; the full-size Wan2.2 and HunyuanVideo shapes run in the launch
-configuration the benchmark times and are compared on sampled query cubes
-(all 64 rows, every channel) plus whole-output finiteness.
+every output (unpaired schedule: cubes 2u, 2u + 1 share a tile); the
+full-size Wan2.2 and HunyuanVideo shapes run in the launch configuration the
+benchmark times (vsa_pair_cubes, then the paired fine stage) and are compared
+on sampled query cubes (all 64 rows, every channel) plus whole-output
+finiteness.
 """
 import numpy as np
 import pytest
@@ -19,8 +21,10 @@ from gpu_util import (assert_lse_close, assert_scoring_rule, i32_dev, score_outp
 pytestmark = pytest.mark.gpu
 
 
-def gpu_fine(qt, kt, vt, idx, vbs, sm):
-    o, lse = vsa.sparse_attn_fwd(to_dev(qt), to_dev(kt), to_dev(vt), i32_dev(idx), i32_dev(vbs), sm)
+def gpu_fine(qt, kt, vt, idx, vbs, sm, paired=False):
+    idx_d = i32_dev(idx)
+    pairs = vsa.pair_cubes(idx_d) if paired else None
+    o, lse = vsa.sparse_attn_fwd(to_dev(qt), to_dev(kt), to_dev(vt), idx_d, i32_dev(vbs), sm, pairs=pairs)
     torch.cuda.synchronize()
     assert vsa.device_error(reset=True) == 0
     return to_bits(o), lse.cpu().numpy()
@@ -136,7 +140,8 @@ def sample_units(wl, n, seed, heads=None):
 
 
 def sampled_compare(wl, qt, kt, vt, vbs, idx, units):
-    got, got_lse = gpu_fine(qt, kt, vt, idx, vbs, wl.sm_scale)
+    # the launch configuration the benchmark times: pairing, then the paired fine stage
+    got, got_lse = gpu_fine(qt, kt, vt, idx, vbs, wl.sm_scale, paired=True)
     assert np.isfinite(synth.bf16_to_f32(got)).all()
     ref_u, ref_lse_u, _ = oracle.fine(qt, kt, vt, idx, vbs, wl.sm_scale, units)
     N = wl.ncubes
