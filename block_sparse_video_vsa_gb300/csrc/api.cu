@@ -178,7 +178,8 @@ vsa_status vsa_pair_cubes(const int32_t* topk_idx, int32_t B, int32_t ncubes, in
                           void* workspace, uint32_t* pairs, vsa_stream_t stream) {
     if (!topk_idx || !workspace || !pairs) return VSA_ERR_INVALID_ARG;
     if (B <= 0 || ncubes <= 0 || heads <= 0 || topk <= 0 || topk > ncubes) return VSA_ERR_INVALID_ARG;
-    if (ncubes > pair_max_cubes() || topk > pair_max_topk() || (int64_t)B * heads * ncubes >= ((int64_t)1 << 31) ||
+    if (ncubes > pair_max_cubes() || topk > pair_max_topk() || (int64_t)B * heads > 65535 ||
+        (int64_t)B * heads * ncubes >= ((int64_t)1 << 31) ||
         (int64_t)B * heads * ncubes * topk >= ((int64_t)1 << 40))
         return VSA_ERR_UNSUPPORTED;
     if (!aligned16(workspace) || (reinterpret_cast<uintptr_t>(topk_idx) & 3u) ||
@@ -187,7 +188,7 @@ vsa_status vsa_pair_cubes(const int32_t* topk_idx, int32_t B, int32_t ncubes, in
     DevCtx ctx;
     if (get_dev_ctx(&ctx) != cudaSuccess) return VSA_ERR_CUDA;
     return from_cuda(launch_pair(topk_idx, B, ncubes, heads, topk, workspace, pairs, ctx.num_sms,
-                                 static_cast<cudaStream_t>(stream)));
+                                 ctx.max_smem_optin, static_cast<cudaStream_t>(stream)));
 }
 
 vsa_status vsa_validate_indices(const int32_t* topk_idx, const int32_t* vbs, int32_t B, int32_t heads,

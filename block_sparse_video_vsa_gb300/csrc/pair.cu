@@ -11,19 +11,21 @@
 //
 // Deterministic and integer only, in three launches:
 //  1. selection bitmaps of the N cubes of every (batch, head) (workspace);
-//  2. for every cube i, the cubes j != i of sel(i) sorted by overlap
-//     |sel(i) & sel(j)| (popcount of the AND of two bitmaps; largest first,
-//     ties: smaller j), kept as int16 lists in the workspace (whole grid);
+//  2. for every cube i, the kTopC cubes j != i of sel(i) of largest overlap
+//     |sel(i) & sel(j)| (popcount of the AND of two bitmaps; ties: smaller j),
+//     best first, kept as int16 lists in the workspace (whole grid);
 //  then one CTA per (batch, head):
 //  3. kRounds1 rounds of mutual-best matching: every unpaired cube proposes to
-//     the unpaired j != i in sel(i) of largest overlap (ties: smaller j), the
-//     first unpaired entry of its sorted list; mutual proposals pair up;
+//     its unpaired candidate of largest overlap (ties: smaller j), the first
+//     unpaired entry of its list, if any; mutual proposals pair up;
 //  4. the cubes still unpaired, in index order (the first kMaxLeft of them),
 //     run kRounds2 more rounds in which each proposes among the kWindow list
 //     entries before and after it (their overlaps computed once);
 //  5. the rest pair in index order; with N odd one cube stays single.
 // Units are written in order of their smaller cube index:
 //   pairs[b, head, u] = i | (j << 16), j = 0xFFFF for a single cube.
+#include <type_traits>
+
 #include "vsa_common.cuh"
 
 namespace vsa {
@@ -32,6 +34,7 @@ namespace {
 
 constexpr int kPairThreads = 512;
 constexpr int kPairWarps = kPairThreads / 32;
+constexpr int kTopC = 16;  // candidates kept per cube
 constexpr int kRounds1 = 4;
 constexpr int kRounds2 = 4;
 constexpr int kMaxLeft = 640;
@@ -45,7 +48,7 @@ struct PairArgs {
     int N, k, Wp;        // Wp: bitmap words per cube, a multiple of 4
     int npairs;          // ceil(N / 2)
     uint32_t* bm;        // [B * heads][N][Wp]
-    int16_t* cand;       // [B * heads][N][k]: sorted candidate lists
+    int16_t* cand;       // [B * heads][N][kTopC]: candidate lists, best first
     uint32_t* pairs;     // [B * heads][npairs]
 };
 
@@ -79,19 +82,33 @@ __device__ __forceinline__ int bitmap_overlap(const uint32_t* a, const uint32_t*
     return s;
 }
 
+// 16-byte load of bitmap words, from shared memory (kShared) or global memory.
+template <bool kShared>
+__device__ __forceinline__ uint4 ld_words(const uint32_t* p) {
+    if constexpr (kShared) {
+        uint4 v;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"((uint32_t)__cvta_generic_to_shared(p)));
+        return v;
+    } else {
+        return __ldg(reinterpret_cast<const uint4*>(p));
+    }
+}
+
 // Overlaps of row a with rows b[0..3] (null: skipped, 0); the loads of the
 // four rows are issued together.
+template <bool kShared>
 __device__ __forceinline__ void bitmap_overlap4(const uint32_t* a, const uint32_t* const (&b)[4], int Wp,
                                                 int (&o)[4]) {
-    const uint4* a4 = reinterpret_cast<const uint4*>(a);
     int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     for (int q = 0; q < Wp / 4; ++q) {
-        const uint4 x = a4[q];
-        const uint4 y0 = b[0] ? reinterpret_cast<const uint4*>(b[0])[q] : z;
-        const uint4 y1 = b[1] ? reinterpret_cast<const uint4*>(b[1])[q] : z;
-        const uint4 y2 = b[2] ? reinterpret_cast<const uint4*>(b[2])[q] : z;
-        const uint4 y3 = b[3] ? reinterpret_cast<const uint4*>(b[3])[q] : z;
+        const uint4 x = ld_words<kShared>(a + 4 * q);
+        const uint4 y0 = b[0] ? ld_words<kShared>(b[0] + 4 * q) : z;
+        const uint4 y1 = b[1] ? ld_words<kShared>(b[1] + 4 * q) : z;
+        const uint4 y2 = b[2] ? ld_words<kShared>(b[2] + 4 * q) : z;
+        const uint4 y3 = b[3] ? ld_words<kShared>(b[3] + 4 * q) : z;
         s0 += __popc(x.x & y0.x) + __popc(x.y & y0.y) + __popc(x.z & y0.z) + __popc(x.w & y0.w);
         s1 += __popc(x.x & y1.x) + __popc(x.y & y1.y) + __popc(x.z & y1.z) + __popc(x.w & y1.w);
         s2 += __popc(x.x & y2.x) + __popc(x.y & y2.y) + __popc(x.z & y2.z) + __popc(x.w & y2.w);
@@ -118,69 +135,68 @@ __global__ void __launch_bounds__(kPairThreads) pair_bitmap_kernel(PairArgs a, s
     }
 }
 
-// 2. Candidate lists: for every cube i, the cubes j != i of sel(i) sorted by
-// overlap |sel(i) & sel(j)| (largest first, ties: smaller j), -1 past the
-// valid entries.  One warp per (batch, head, cube): overlaps from the bitmaps,
-// then a bitonic sort of the keys (ov << 16) | (0xFFFF - j) in shared memory.
-__global__ void __launch_bounds__(kPairThreads) pair_candidates_kernel(PairArgs a, size_t rows, int kp) {
-    extern __shared__ uint32_t keys_all[];  // [kPairWarps][kp]
+// 2. Candidate lists: for every cube i, the kTopC cubes j != i of sel(i) of
+// largest overlap |sel(i) & sel(j)| (ties: smaller j), best first, -1 past
+// the valid entries.  Blocks (chunk, b * heads + head); one warp per cube:
+// overlaps from the bitmaps (staged in shared memory when the head's fit),
+// keys (ov << 16) | (0xFFFF - j) in registers, kTopC rounds of a warp max.
+template <bool kStaged, int kPerLane>
+__global__ void __launch_bounds__(kPairThreads) pair_candidates_kernel(PairArgs a) {
+    extern __shared__ __align__(16) uint32_t dsm_c[];  // [N][Wp] bitmaps when staged
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t* keys = keys_all + warp * kp;
     const int N = a.N, k = a.k, Wp = a.Wp;
-    for (size_t row = (size_t)blockIdx.x * kPairWarps + warp; row < rows; row += (size_t)gridDim.x * kPairWarps) {
-        const size_t bh = row / N;
-        const int i = (int)(row - bh * N);
-        const uint32_t* base = a.bm + bh * (size_t)N * Wp;
+    const size_t bh = blockIdx.y;
+    const uint32_t* base = a.bm + bh * (size_t)N * Wp;
+    if constexpr (kStaged) {
+        uint4* dst = reinterpret_cast<uint4*>(dsm_c);
+        const uint4* src = reinterpret_cast<const uint4*>(base);
+        for (int t = threadIdx.x; t < N * Wp / 4; t += kPairThreads) dst[t] = src[t];
+        __syncthreads();
+        base = dsm_c;
+    }
+    const int per = (N + gridDim.x - 1) / gridDim.x;
+    const int i_end = min(N, ((int)blockIdx.x + 1) * per);
+    for (int i = (int)blockIdx.x * per + warp; i < i_end; i += kPairWarps) {
+        const size_t row = bh * (size_t)N + i;
         const int32_t* sel = a.idx + row * k;
-        for (int e0 = lane; e0 < kp; e0 += 128) {
+        uint32_t key[kPerLane];
+#pragma unroll
+        for (int m0 = 0; m0 < kPerLane; m0 += 4) {
             int jj[4];
             const uint32_t* rb[4];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-                const int e = e0 + 32 * v;
+                const int e = lane + 32 * (m0 + v);
                 jj[v] = e < k ? sel[e] : -1;
                 const bool ok = jj[v] >= 0 && jj[v] < N && jj[v] != i;
                 if (!ok) jj[v] = -1;
                 rb[v] = ok ? base + (size_t)jj[v] * Wp : nullptr;
             }
             int o[4];
-            bitmap_overlap4(base + (size_t)i * Wp, rb, Wp, o);
+            bitmap_overlap4<kStaged>(base + (size_t)i * Wp, rb, Wp, o);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int e = e0 + 32 * v;
-                if (e < kp) keys[e] = jj[v] >= 0 ? ((uint32_t)o[v] << 16) | (uint32_t)(0xFFFF - jj[v]) : 0u;
+            for (int v = 0; v < 4; ++v)
+                key[m0 + v] = jj[v] >= 0 ? ((uint32_t)o[v] << 16) | (uint32_t)(0xFFFF - jj[v]) : 0u;
+        }
+        int16_t* out = a.cand + row * kTopC;
+        for (int r = 0; r < kTopC; ++r) {
+            uint32_t best = 0u;
+#pragma unroll
+            for (int m = 0; m < kPerLane; ++m) best = key[m] > best ? key[m] : best;
+            best = __reduce_max_sync(0xffffffffu, best);
+            if (best) {
+#pragma unroll
+                for (int m = 0; m < kPerLane; ++m) key[m] = key[m] == best ? 0u : key[m];
             }
+            if (lane == 0) out[r] = best ? (int16_t)(0xFFFF - (best & 0xFFFFu)) : (int16_t)-1;
         }
-        __syncwarp();
-        // Bitonic sort, descending.
-        for (int size = 2; size <= kp; size <<= 1) {
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                for (int t = lane; t < kp / 2; t += 32) {
-                    const int lo = 2 * t - (t & (stride - 1));
-                    const int hi = lo + stride;
-                    const bool desc = (lo & size) == 0;
-                    const uint32_t x = keys[lo], y = keys[hi];
-                    if ((x < y) == desc) {
-                        keys[lo] = y;
-                        keys[hi] = x;
-                    }
-                }
-                __syncwarp();
-            }
-        }
-        int16_t* out = a.cand + row * k;
-        for (int e = lane; e < k; e += 32) {
-            const uint32_t key = keys[e];
-            out[e] = key ? (int16_t)(0xFFFF - (key & 0xFFFFu)) : (int16_t)-1;
-        }
-        __syncwarp();
     }
 }
 
 // 3-5. Matching and the unit list, one CTA per (batch, head).  Dynamic shared
 // memory: the overlaps of each leftover cube with its window, then the
 // partner, proposal and list-position arrays of N entries, the leftover list.
-__global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a) {
+__global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a, int rows_cap) {
     extern __shared__ __align__(16) unsigned char dsm[];
     const int N = a.N, k = a.k, Wp = a.Wp;
     uint16_t* wov = reinterpret_cast<uint16_t*>(dsm);                   // [2 kWindow][kWovStride]
@@ -189,12 +205,15 @@ __global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a) {
     int16_t* ptr = prop + N;                                            // next candidate to look at
     int16_t* left = ptr + N;                                            // [kMaxLeft]
     int16_t* lprop = left + kMaxLeft;                                   // [kMaxLeft]
+    uint32_t* lrows = reinterpret_cast<uint32_t*>(dsm + (((reinterpret_cast<uintptr_t>(lprop + kMaxLeft) -
+                                                          reinterpret_cast<uintptr_t>(dsm)) + 15) & ~(uintptr_t)15));
+    // lrows: bitmap rows of the leftover list when nleft * Wp words fit rows_cap
     __shared__ int wsum[kPairWarps];
     __shared__ uint32_t lfree[kMaxLeft / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t bh = blockIdx.x;
     const uint32_t* bm = a.bm + bh * (size_t)N * Wp;
-    const int16_t* cand = a.cand + bh * (size_t)N * k;
+    const int16_t* cand = a.cand + bh * (size_t)N * kTopC;
 
     for (int i = tid; i < N; i += kPairThreads) {
         partner[i] = -1;
@@ -209,12 +228,12 @@ __global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a) {
         for (int i = tid; i < N; i += kPairThreads) {
             int best = -1;
             if (partner[i] < 0) {
-                const int16_t* row = cand + (size_t)i * k;
+                const int16_t* row = cand + (size_t)i * kTopC;
                 int e = ptr[i];
-                for (; e < k; ++e) {
+                for (; e < kTopC; ++e) {
                     const int j = row[e];
                     if (j < 0) {
-                        e = k;
+                        e = kTopC;
                         break;
                     }
                     if (partner[j] < 0) {
@@ -251,6 +270,14 @@ __global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a) {
     }
     nleft = min(nleft, kMaxLeft);
     __syncthreads();
+    const bool staged = nleft * Wp <= rows_cap;
+    if (staged) {
+        for (int t = tid; t < nleft * (Wp / 4); t += kPairThreads) {
+            const int f = t / (Wp / 4), q = t - f * (Wp / 4);
+            reinterpret_cast<uint4*>(lrows)[t] = reinterpret_cast<const uint4*>(bm + (size_t)left[f] * Wp)[q];
+        }
+        __syncthreads();
+    }
     static_assert(2 * kWindow == 128, "one candidate per lane and slot of four");
     for (int f = warp; f < nleft; f += kPairWarps) {
         const uint32_t* rb[4];
@@ -258,10 +285,13 @@ __global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a) {
         for (int v = 0; v < 4; ++v) {
             const int d = lane + 32 * v;
             const int g = d < kWindow ? f - kWindow + d : f + 1 + (d - kWindow);
-            rb[v] = (g >= 0 && g < nleft) ? bm + (size_t)left[g] * Wp : nullptr;
+            rb[v] = (g >= 0 && g < nleft) ? (staged ? lrows + (size_t)g * Wp : bm + (size_t)left[g] * Wp) : nullptr;
         }
         int o[4];
-        bitmap_overlap4(bm + (size_t)left[f] * Wp, rb, Wp, o);
+        if (staged)
+            bitmap_overlap4<true>(lrows + (size_t)f * Wp, rb, Wp, o);
+        else
+            bitmap_overlap4<false>(bm + (size_t)left[f] * Wp, rb, Wp, o);
 #pragma unroll
         for (int v = 0; v < 4; ++v) wov[(lane + 32 * v) * kWovStride + f] = (uint16_t)o[v];
     }
@@ -269,31 +299,29 @@ __global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a) {
     for (int rd = 0; rd < kRounds2; ++rd) {
         // Unpaired list entries as a bitmask (the list is in increasing cube
         // order, so list position breaks ties like the cube index).
-        for (int w = tid; w < kMaxLeft / 32; w += kPairThreads) {
-            uint32_t m = 0u;
-            for (int b = 0; b < 32; ++b) {
-                const int g = 32 * w + b;
-                if (g < nleft && partner[left[g]] < 0) m |= 1u << b;
-            }
-            lfree[w] = m;
+        for (int g0 = warp * 32; g0 < kMaxLeft; g0 += kPairThreads) {
+            const int g = g0 + lane;
+            const unsigned m = __ballot_sync(0xffffffffu, g < nleft && partner[left[min(g, nleft - 1)]] < 0);
+            if (lane == 0) lfree[g0 >> 5] = m;
         }
         __syncthreads();
-        for (int f = tid; f < nleft; f += kPairThreads) {
-            int best = -1, bv = -1;
+        // A warp per leftover, a lane per four window entries; the best is the
+        // largest overlap, ties to the smaller list position.
+        for (int f = warp; f < nleft; f += kPairWarps) {
+            uint32_t key = 0u;  // (overlap + 1) << 16 | (0xFFFF - g); 0: none
             if ((lfree[f >> 5] >> (f & 31)) & 1u) {
-                const uint16_t* ov = wov + f;
-#pragma unroll 8
-                for (int d = 0; d < 2 * kWindow; ++d) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int d = lane + 32 * v;
                     const int g = d < kWindow ? f - kWindow + d : f + 1 + (d - kWindow);
-                    const bool fr = g >= 0 && g < nleft && ((lfree[g >> 5] >> (g & 31)) & 1u);
-                    const int o = fr ? (int)ov[d * kWovStride] : -1;
-                    if (o > bv) {  // increasing g: the first of equal overlaps is kept
-                        best = g;
-                        bv = o;
+                    if (g >= 0 && g < nleft && ((lfree[g >> 5] >> (g & 31)) & 1u)) {
+                        const uint32_t kk = ((uint32_t)wov[d * kWovStride + f] + 1u) << 16 | (uint32_t)(0xFFFF - g);
+                        key = kk > key ? kk : key;
                     }
                 }
             }
-            lprop[f] = (int16_t)best;
+            key = __reduce_max_sync(0xffffffffu, key);
+            if (lane == 0) lprop[f] = key ? (int16_t)(0xFFFF - (key & 0xFFFFu)) : (int16_t)-1;
         }
         __syncthreads();
         for (int f = tid; f < nleft; f += kPairThreads) {
@@ -349,14 +377,15 @@ int pair_words(int ncubes) { return ((ncubes + 31) / 32 + 3) & ~3; }
 
 size_t pair_workspace_bytes(int B, int heads, int ncubes, int topk) {
     const size_t bh = (size_t)B * heads;
-    return align256(bh * ncubes * pair_words(ncubes) * sizeof(uint32_t)) + align256(bh * ncubes * topk * sizeof(uint16_t));
+    (void)topk;
+    return align256(bh * ncubes * pair_words(ncubes) * sizeof(uint32_t)) + align256(bh * ncubes * kTopC * sizeof(int16_t));
 }
 
 int pair_max_cubes() { return kPairMaxCubes; }
 int pair_max_topk() { return kPairMaxTopk; }
 
 cudaError_t launch_pair(const int32_t* topk_idx, int B, int ncubes, int heads, int topk, void* workspace,
-                        uint32_t* pairs, int num_sms, cudaStream_t stream) {
+                        uint32_t* pairs, int num_sms, int max_smem, cudaStream_t stream) {
     PairArgs a;
     a.idx = topk_idx;
     a.N = ncubes;
@@ -370,17 +399,35 @@ cudaError_t launch_pair(const int32_t* topk_idx, int B, int ncubes, int heads, i
     a.pairs = pairs;
     const size_t rows = bh * ncubes;
     pair_bitmap_kernel<<<(unsigned)((rows + kPairWarps - 1) / kPairWarps), kPairThreads, 0, stream>>>(a, rows);
-    int kp = 32;
-    while (kp < topk) kp <<= 1;
-    const size_t want = (rows + kPairWarps - 1) / kPairWarps;
-    const unsigned blocks = (unsigned)(want < (size_t)num_sms * 4 ? want : (size_t)num_sms * 4);
-    const size_t dyn_c = (size_t)kPairWarps * kp * sizeof(uint32_t);
-    pair_candidates_kernel<<<blocks, kPairThreads, dyn_c, stream>>>(a, rows, kp);
-    const size_t dyn = (size_t)2 * kWindow * kWovStride * sizeof(uint16_t) + 3 * (size_t)ncubes * 2 +
-                       2 * (size_t)kMaxLeft * 2;
-    cudaError_t e = cudaFuncSetAttribute(pair_match_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    const size_t bm_bytes = (size_t)ncubes * a.Wp * sizeof(uint32_t);
+    const bool stage_bm = bm_bytes <= (size_t)max_smem - 1024;
+    const size_t dyn_c = stage_bm ? bm_bytes : 0;
+    int chunks = (int)((2 * (size_t)num_sms + bh - 1) / bh);
+    chunks = chunks < 1 ? 1 : chunks;
+    const int max_chunks = (ncubes + kPairWarps - 1) / kPairWarps;
+    chunks = chunks > max_chunks ? max_chunks : chunks;
+    auto pick = [&](auto staged) -> void (*)(PairArgs) {
+        constexpr bool S = decltype(staged)::value;
+        if (topk <= 128) return pair_candidates_kernel<S, 4>;
+        if (topk <= 256) return pair_candidates_kernel<S, 8>;
+        return pair_candidates_kernel<S, 16>;
+    };
+    void (*cand_kernel)(PairArgs) = stage_bm ? pick(std::true_type()) : pick(std::false_type());
+    cudaError_t e = cudaFuncSetAttribute(cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_c);
     if (e != cudaSuccess) return e;
-    pair_match_kernel<<<(unsigned)bh, kPairThreads, dyn, stream>>>(a);
+    cand_kernel<<<dim3((unsigned)chunks, (unsigned)bh), kPairThreads, dyn_c, stream>>>(a);
+    // Matching: window overlaps, N-entry arrays, leftover list, then as many
+    // leftover bitmap rows as the rest of the shared memory holds.
+    const size_t fixed = (size_t)2 * kWindow * kWovStride * sizeof(uint16_t) + 3 * (size_t)ncubes * 2 +
+                         2 * (size_t)kMaxLeft * 2 + 16;
+    const size_t avail = (size_t)max_smem - 1024;  // static shared memory of the kernel is below 1 KB
+    if (fixed > avail) return cudaErrorInvalidValue;
+    const size_t rows_bytes = avail - fixed < (size_t)kMaxLeft * a.Wp * 4 ? avail - fixed : (size_t)kMaxLeft * a.Wp * 4;
+    const int rows_cap = (int)(rows_bytes / 4);
+    const size_t dyn = fixed + rows_bytes;
+    e = cudaFuncSetAttribute(pair_match_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e != cudaSuccess) return e;
+    pair_match_kernel<<<(unsigned)bh, kPairThreads, dyn, stream>>>(a, rows_cap);
     return cudaGetLastError();
 }
 

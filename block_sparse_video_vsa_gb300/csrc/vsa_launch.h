@@ -42,6 +42,6 @@ size_t pair_workspace_bytes(int B, int heads, int ncubes, int topk);
 int pair_max_cubes();
 int pair_max_topk();
 cudaError_t launch_pair(const int32_t* topk_idx, int B, int ncubes, int heads, int topk, void* workspace,
-                        uint32_t* pairs, int num_sms, cudaStream_t stream);
+                        uint32_t* pairs, int num_sms, int max_smem, cudaStream_t stream);
 
 }  // namespace vsa

@@ -205,8 +205,8 @@ vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt,
  *   pairs     : uint32 [B, heads, (ncubes + 1) / 2] (written): unit u holds
  *               cubes i | (j << 16), i < j, j = 0xFFFF for a single cube;
  *               units in increasing i; every cube appears exactly once
- * Limits: ncubes <= 8192, topk <= 512.  Entries of topk_idx outside
- * [0, ncubes) are ignored.
+ * Limits: ncubes <= 8192, topk <= 512, B * heads <= 65535.  Entries of
+ * topk_idx outside [0, ncubes) are ignored.
  */
 size_t vsa_pair_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t topk);
 vsa_status vsa_pair_cubes(const int32_t* topk_idx, int32_t B, int32_t ncubes, int32_t heads,

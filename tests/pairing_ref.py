@@ -7,9 +7,10 @@ scheduling choice: the attention results do not depend on it.  This module
 states the same deterministic integer procedure with numpy and plain loops so
 that the GPU pass can be checked for exact agreement on small cases.
 
-  1. overlap(i, j) = |sel(i) & sel(j)| for j in sel(i);
-  2. ROUNDS1 rounds: every unpaired cube proposes to the unpaired j != i in
-     sel(i) of largest overlap (ties: smaller j); mutual proposals pair up;
+  1. overlap(i, j) = |sel(i) & sel(j)| for j in sel(i); the candidates of i
+     are the TOPC cubes j != i of sel(i) of largest overlap (ties: smaller j);
+  2. ROUNDS1 rounds: every unpaired cube proposes to its unpaired candidate of
+     largest overlap (ties: smaller j), if any; mutual proposals pair up;
   3. the still-unpaired cubes, in index order (the first max_left(n) of them),
      run ROUNDS2 rounds of the same matching where each proposes to the
      unpaired cube of largest overlap among the next WINDOW entries of that
@@ -19,6 +20,7 @@ Units are listed by their smaller cube index: (i, j) or (i, -1).
 """
 import numpy as np
 
+TOPC = 16
 ROUNDS1 = 4
 ROUNDS2 = 4
 MAX_LEFT = 640
@@ -67,8 +69,13 @@ def pair_cubes(sel_rows, n):
     """sel_rows: list of n index arrays (one head). Returns the unit list."""
     ov = overlap_matrix(sel_rows, n)
     partner = [-1] * n
+    cand = []
+    for i in range(n):
+        js = sorted({int(j) for j in sel_rows[i] if 0 <= int(j) < n and int(j) != i},
+                    key=lambda j: (-int(ov[i, j]), j))
+        cand.append(js[:TOPC])
     for _ in range(ROUNDS1):
-        _round(lambda i: [int(j) for j in sel_rows[i]], lambda i, j: int(ov[i, j]), partner)
+        _round(lambda i: cand[i], lambda i, j: int(ov[i, j]), partner)
     left = [i for i in range(n) if partner[i] < 0][:max_left(n)]
     pos = {c: a for a, c in enumerate(left)}
     for _ in range(ROUNDS2):

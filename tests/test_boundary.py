@@ -111,10 +111,10 @@ def test_pairing_validation(lib):
     assert f(A, 1, 9000, 2, 3, A, A, None) == UNSUPPORTED  # ncubes > 8192
     assert f(A, 1, 12, 2, 3, MIS, A, None) == ALIGNMENT   # workspace
     assert f(A, 1, 12, 2, 3, A, A + 2, None) == ALIGNMENT  # pairs
-    # bitmaps: 4-word rows (12 cubes -> 1 word, rounded up to 4), then uint16 overlaps
-    assert lib.vsa_pair_workspace_bytes(1, 2, 12, 3) == 512 + 256  # 2*12*4*4 B -> 512, 2*12*3*2 B -> 256
-    wan = 40 * 624 * 20 * 4
-    assert lib.vsa_pair_workspace_bytes(1, 40, 624, 78) == (wan + 255) // 256 * 256 + (40 * 624 * 78 * 2 + 255) // 256 * 256
+    # bitmaps: 4-word rows (12 cubes -> 1 word, rounded up to 4), then the lists
+    assert lib.vsa_pair_workspace_bytes(1, 2, 12, 3) == 512 + 768  # bitmaps 2*12*4*4 B -> 512; lists 2*12*16*2 B
+    # bitmaps 40*624 rows of 20 words; candidate lists of 16 int16 per cube
+    assert lib.vsa_pair_workspace_bytes(1, 40, 624, 78) == 40 * 624 * 20 * 4 + 40 * 624 * 16 * 2
     g = lib.vsa_sparse_attn_fwd_paired
     assert g(A, A, A, A, A, A + 2, 1, 12, 2, 64, 3, 0.0, A, None, None) == ALIGNMENT  # pairs
     assert g(A, A, A, A, A, None, 1, 12, 2, 64, 0, 0.0, A, None, None) == INVALID
