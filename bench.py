@@ -49,9 +49,9 @@ KERNELS_PER_STEP = 10  # tile x3, pool sums, score/top-k, pairing x3, sparse att
 # was taken from: if fine.cu no longer hashes to `source_sha256`, the traffic is reported
 # as null.
 FINE_TRAFFIC = {
-    "bytes_per_launch": (247.233792e6 + 67.947264e6) * 40 / 8,
+    "bytes_per_launch": (247.347712e6 + 66.999296e6) * 40 / 8,
     "capture": "profiles/fine_fwd_kernel_wan.md",
-    "source_sha256": "cb88cefd773f05c9fd830549513351fef64369c2c8c8d620ab48214210351242",
+    "source_sha256": "2d161dcaefb420642c5d2b5fc58f21b2ddc61df07bf9facf23367fefe18207a5",
 }
 
 
