@@ -9,23 +9,29 @@
 // Reference", Operator contract); only the order of floating-point
 // accumulation does.
 //
-// Deterministic and integer only, in three launches:
-//  1. selection bitmaps of the N cubes of every (batch, head) (workspace);
-//  2. for every cube i, the kTopC cubes j != i of sel(i) of largest overlap
-//     |sel(i) & sel(j)| (popcount of the AND of two bitmaps; ties: smaller j),
-//     best first, kept as int16 lists in the workspace (whole grid);
-//  then one CTA per (batch, head):
-//  3. kRounds1 rounds of mutual-best matching: every unpaired cube proposes to
-//     its unpaired candidate of largest overlap (ties: smaller j), the first
-//     unpaired entry of its list, if any; mutual proposals pair up;
-//  4. the cubes still unpaired, in index order (the first kMaxLeft of them),
-//     run kRounds2 more rounds in which each proposes among the kWindow list
-//     entries before and after it (their overlaps computed once);
-//  5. the rest pair in index order; with N odd one cube stays single.
+// The procedure, per (batch, head), deterministic and integer only:
+//  a. overlap(i, j) = |sel(i) & sel(j)| for j in sel(i); the candidates of i
+//     are its kTopC cubes j != i of largest overlap (ties: smaller j);
+//  b. kRounds1 rounds of mutual-best matching: every unpaired cube proposes to
+//     its unpaired candidate of largest overlap (the first unpaired entry of
+//     its list), if any; mutual proposals pair up;
+//  c. the cubes still unpaired, in index order (the first kMaxLeft of them),
+//     run kRounds2 more rounds in which each proposes to the unpaired cube of
+//     largest overlap among the kWindow list entries before and after it
+//     (ties: smaller list position, i.e. smaller cube index);
+//  d. the rest pair in index order; with N odd one cube stays single.
 // Units are written in order of their smaller cube index:
 //   pairs[b, head, u] = i | (j << 16), j = 0xFFFF for a single cube.
-#include <type_traits>
-
+//
+// Five launches, each sized so that its working set sits in shared memory:
+//  1. selection bitmaps (a warp per cube);
+//  2. candidate lists (a): the bitmap columns are staged in chunks that fit
+//     shared memory, overlaps accumulate per (cube, entry), then a warp picks
+//     the kTopC best by rounds of a warp max;
+//  3. rounds (b), one CTA per (batch, head), lists in shared memory; writes the
+//     partner array and the leftover list;
+//  4. window overlaps of (c), blocks over (leftover chunk, batch, head);
+//  5. rounds (c) and (d) and the unit list, one CTA per (batch, head).
 #include "vsa_common.cuh"
 
 namespace vsa {
@@ -34,22 +40,28 @@ namespace {
 
 constexpr int kPairThreads = 512;
 constexpr int kPairWarps = kPairThreads / 32;
-constexpr int kTopC = 16;  // candidates kept per cube
+constexpr int kTopC = 16;        // candidates kept per cube
 constexpr int kRounds1 = 4;
 constexpr int kRounds2 = 4;
-constexpr int kMaxLeft = 640;
-constexpr int kWovStride = kMaxLeft + 2;  // window overlaps [2 kWindow][kWovStride]: conflict-free both ways
-constexpr int kWindow = 64;
+constexpr int kMaxLeft = 640;    // leftover list length cap
+constexpr int kWindow = 64;      // list entries on each side
+constexpr int kWin = 2 * kWindow;
+constexpr int kWinChunk = 64;    // leftovers per window block
 constexpr int kPairMaxCubes = 8192;
 constexpr int kPairMaxTopk = 512;
+constexpr size_t kSmemBudget = 200 * 1024;  // dynamic shared memory a pairing block plans for
 
 struct PairArgs {
-    const int32_t* idx;  // [B * heads][N][k]
+    const int32_t* idx;  // [BH][N][k]
     int N, k, Wp;        // Wp: bitmap words per cube, a multiple of 4
     int npairs;          // ceil(N / 2)
-    uint32_t* bm;        // [B * heads][N][Wp]
-    int16_t* cand;       // [B * heads][N][kTopC]: candidate lists, best first
-    uint32_t* pairs;     // [B * heads][npairs]
+    uint32_t* bm;        // [BH][N][Wp]
+    int16_t* cand;       // [BH][N][kTopC]: candidate lists, best first, -1 past the end
+    int16_t* partner;    // [BH][N]: after (b); -1 unpaired
+    int16_t* left;       // [BH][kMaxLeft]: leftover list
+    int* nleft;          // [BH]
+    uint16_t* wov;       // [BH][kMaxLeft][kWin]: window overlaps
+    uint32_t* pairs;     // [BH][npairs]
 };
 
 // Ordered compaction over one chunk of kPairThreads flags: this thread's rank
@@ -71,53 +83,22 @@ __device__ __forceinline__ int chunk_rank(bool flag, int* wsum, int& total) {
     return before + __popc(b & ((1u << lane) - 1u));
 }
 
-__device__ __forceinline__ int bitmap_overlap(const uint32_t* a, const uint32_t* b, int Wp) {
-    const uint4* a4 = reinterpret_cast<const uint4*>(a);
-    const uint4* b4 = reinterpret_cast<const uint4*>(b);
+__device__ __forceinline__ uint4 lds128(const uint32_t* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"((uint32_t)__cvta_generic_to_shared(p)));
+    return v;
+}
+
+// |a & b| over `words` words (a multiple of 4) of two shared-memory rows.
+__device__ __forceinline__ int smem_overlap(const uint32_t* a, const uint32_t* b, int words) {
     int s = 0;
-    for (int q = 0; q < Wp / 4; ++q) {
-        const uint4 x = a4[q], y = b4[q];
+    for (int q = 0; q < words; q += 4) {
+        const uint4 x = lds128(a + q), y = lds128(b + q);
         s += __popc(x.x & y.x) + __popc(x.y & y.y) + __popc(x.z & y.z) + __popc(x.w & y.w);
     }
     return s;
-}
-
-// 16-byte load of bitmap words, from shared memory (kShared) or global memory.
-template <bool kShared>
-__device__ __forceinline__ uint4 ld_words(const uint32_t* p) {
-    if constexpr (kShared) {
-        uint4 v;
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                     : "r"((uint32_t)__cvta_generic_to_shared(p)));
-        return v;
-    } else {
-        return __ldg(reinterpret_cast<const uint4*>(p));
-    }
-}
-
-// Overlaps of row a with rows b[0..3] (null: skipped, 0); the loads of the
-// four rows are issued together.
-template <bool kShared>
-__device__ __forceinline__ void bitmap_overlap4(const uint32_t* a, const uint32_t* const (&b)[4], int Wp,
-                                                int (&o)[4]) {
-    int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    for (int q = 0; q < Wp / 4; ++q) {
-        const uint4 x = ld_words<kShared>(a + 4 * q);
-        const uint4 y0 = b[0] ? ld_words<kShared>(b[0] + 4 * q) : z;
-        const uint4 y1 = b[1] ? ld_words<kShared>(b[1] + 4 * q) : z;
-        const uint4 y2 = b[2] ? ld_words<kShared>(b[2] + 4 * q) : z;
-        const uint4 y3 = b[3] ? ld_words<kShared>(b[3] + 4 * q) : z;
-        s0 += __popc(x.x & y0.x) + __popc(x.y & y0.y) + __popc(x.z & y0.z) + __popc(x.w & y0.w);
-        s1 += __popc(x.x & y1.x) + __popc(x.y & y1.y) + __popc(x.z & y1.z) + __popc(x.w & y1.w);
-        s2 += __popc(x.x & y2.x) + __popc(x.y & y2.y) + __popc(x.z & y2.z) + __popc(x.w & y2.w);
-        s3 += __popc(x.x & y3.x) + __popc(x.y & y3.y) + __popc(x.z & y3.z) + __popc(x.w & y3.w);
-    }
-    o[0] = s0;
-    o[1] = s1;
-    o[2] = s2;
-    o[3] = s3;
 }
 
 // 1. Selection bitmaps: one warp per (batch, head, cube) row.
@@ -135,51 +116,59 @@ __global__ void __launch_bounds__(kPairThreads) pair_bitmap_kernel(PairArgs a, s
     }
 }
 
-// 2. Candidate lists: for every cube i, the kTopC cubes j != i of sel(i) of
-// largest overlap |sel(i) & sel(j)| (ties: smaller j), best first, -1 past
-// the valid entries.  Blocks (chunk, b * heads + head); one warp per cube:
-// overlaps from the bitmaps (staged in shared memory when the head's fit),
-// keys (ov << 16) | (0xFFFF - j) in registers, kTopC rounds of a warp max.
-template <bool kStaged, int kPerLane>
-__global__ void __launch_bounds__(kPairThreads) pair_candidates_kernel(PairArgs a) {
-    extern __shared__ __align__(16) uint32_t dsm_c[];  // [N][Wp] bitmaps when staged
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// 2. Candidate lists.  Block (row chunk, b * heads + head) owns rows
+// [i0, i0 + rb).  Shared memory: bitmap columns [N][cs] (cw words of the
+// current column chunk; the row stride cs is an odd number of 16-byte quads so
+// that rows at random indices spread over the banks), overlap accumulators
+// [rb][k] (uint16) and the entries [rb][k] (int16, -1 for j == i or out of range).
+template <int kPerLane>
+__global__ void __launch_bounds__(kPairThreads) pair_candidates_kernel(PairArgs a, int rb, int cw, int cs) {
+    extern __shared__ __align__(16) uint32_t dsm_c[];
     const int N = a.N, k = a.k, Wp = a.Wp;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t bh = blockIdx.y;
-    const uint32_t* base = a.bm + bh * (size_t)N * Wp;
-    if constexpr (kStaged) {
-        uint4* dst = reinterpret_cast<uint4*>(dsm_c);
-        const uint4* src = reinterpret_cast<const uint4*>(base);
-        for (int t = threadIdx.x; t < N * Wp / 4; t += kPairThreads) dst[t] = src[t];
-        __syncthreads();
-        base = dsm_c;
+    const int i0 = (int)blockIdx.x * rb;
+    const int rows = min(rb, N - i0);
+    if (rows <= 0) return;
+    uint32_t* cols = dsm_c;
+    uint16_t* acc = reinterpret_cast<uint16_t*>(cols + (size_t)N * cs);
+    int16_t* ids = reinterpret_cast<int16_t*>(acc + (size_t)rb * k);
+    const uint32_t* bm = a.bm + bh * (size_t)N * Wp;
+    const int32_t* sel = a.idx + (bh * (size_t)N + i0) * k;
+    for (int t = tid; t < rows * k; t += kPairThreads) {
+        const int i = i0 + t / k;
+        const int j = sel[t];
+        ids[t] = (j >= 0 && j < N && j != i) ? (int16_t)j : (int16_t)-1;
+        acc[t] = 0;
     }
-    const int per = (N + gridDim.x - 1) / gridDim.x;
-    const int i_end = min(N, ((int)blockIdx.x + 1) * per);
-    for (int i = (int)blockIdx.x * per + warp; i < i_end; i += kPairWarps) {
-        const size_t row = bh * (size_t)N + i;
-        const int32_t* sel = a.idx + row * k;
+    for (int c0 = 0; c0 < Wp; c0 += cw) {
+        const int w = min(cw, Wp - c0);  // a multiple of 4
+        __syncthreads();                 // the previous chunk is no longer read
+        for (int t = tid; t < N * (w / 4); t += kPairThreads) {
+            const int n = t / (w / 4), q = t - n * (w / 4);
+            reinterpret_cast<uint4*>(cols + (size_t)n * cs)[q] =
+                reinterpret_cast<const uint4*>(bm + (size_t)n * Wp + c0)[q];
+        }
+        __syncthreads();
+        for (int t = tid; t < rows * k; t += kPairThreads) {
+            const int j = ids[t];
+            if (j < 0) continue;
+            const int i = i0 + t / k;
+            acc[t] = (uint16_t)(acc[t] + smem_overlap(cols + (size_t)i * cs, cols + (size_t)j * cs, w));
+        }
+    }
+    __syncthreads();
+    // The kTopC best of each row: keys (overlap << 16) | (0xFFFF - j).
+    for (int r = warp; r < rows; r += kPairWarps) {
         uint32_t key[kPerLane];
 #pragma unroll
-        for (int m0 = 0; m0 < kPerLane; m0 += 4) {
-            int jj[4];
-            const uint32_t* rb[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int e = lane + 32 * (m0 + v);
-                jj[v] = e < k ? sel[e] : -1;
-                const bool ok = jj[v] >= 0 && jj[v] < N && jj[v] != i;
-                if (!ok) jj[v] = -1;
-                rb[v] = ok ? base + (size_t)jj[v] * Wp : nullptr;
-            }
-            int o[4];
-            bitmap_overlap4<kStaged>(base + (size_t)i * Wp, rb, Wp, o);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-                key[m0 + v] = jj[v] >= 0 ? ((uint32_t)o[v] << 16) | (uint32_t)(0xFFFF - jj[v]) : 0u;
+        for (int m = 0; m < kPerLane; ++m) {
+            const int e = lane + 32 * m;
+            const int j = e < k ? ids[r * k + e] : -1;
+            key[m] = j >= 0 ? ((uint32_t)acc[r * k + e] << 16) | (uint32_t)(0xFFFF - j) : 0u;
         }
-        int16_t* out = a.cand + row * kTopC;
-        for (int r = 0; r < kTopC; ++r) {
+        int16_t* out = a.cand + (bh * (size_t)N + i0 + r) * kTopC;
+        for (int c = 0; c < kTopC; ++c) {
             uint32_t best = 0u;
 #pragma unroll
             for (int m = 0; m < kPerLane; ++m) best = key[m] > best ? key[m] : best;
@@ -188,42 +177,34 @@ __global__ void __launch_bounds__(kPairThreads) pair_candidates_kernel(PairArgs 
 #pragma unroll
                 for (int m = 0; m < kPerLane; ++m) key[m] = key[m] == best ? 0u : key[m];
             }
-            if (lane == 0) out[r] = best ? (int16_t)(0xFFFF - (best & 0xFFFFu)) : (int16_t)-1;
+            if (lane == 0) out[c] = best ? (int16_t)(0xFFFF - (best & 0xFFFFu)) : (int16_t)-1;
         }
     }
 }
 
-// 3-5. Matching and the unit list, one CTA per (batch, head).  Dynamic shared
-// memory: the overlaps of each leftover cube with its window, then the
-// partner, proposal and list-position arrays of N entries, the leftover list.
-__global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a, int rows_cap) {
+// 3. Rounds (b), one CTA per (batch, head).  Shared memory: partner, proposal
+// and list-position arrays [N] and, when they fit (stage_lists), the
+// candidate lists [N][kTopC].
+__global__ void __launch_bounds__(kPairThreads) pair_match1_kernel(PairArgs a, int stage_lists) {
     extern __shared__ __align__(16) unsigned char dsm[];
-    const int N = a.N, k = a.k, Wp = a.Wp;
-    uint16_t* wov = reinterpret_cast<uint16_t*>(dsm);                   // [2 kWindow][kWovStride]
-    int16_t* partner = reinterpret_cast<int16_t*>(wov + 2 * kWindow * kWovStride);  // -1 unpaired, j, or i single
-    int16_t* prop = partner + N;                                        // proposals, later the rest
-    int16_t* ptr = prop + N;                                            // next candidate to look at
-    int16_t* left = ptr + N;                                            // [kMaxLeft]
-    int16_t* lprop = left + kMaxLeft;                                   // [kMaxLeft]
-    uint32_t* lrows = reinterpret_cast<uint32_t*>(dsm + (((reinterpret_cast<uintptr_t>(lprop + kMaxLeft) -
-                                                          reinterpret_cast<uintptr_t>(dsm)) + 15) & ~(uintptr_t)15));
-    // lrows: bitmap rows of the leftover list when nleft * Wp words fit rows_cap
     __shared__ int wsum[kPairWarps];
-    __shared__ uint32_t lfree[kMaxLeft / 32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int N = a.N;
+    const int tid = threadIdx.x;
     const size_t bh = blockIdx.x;
-    const uint32_t* bm = a.bm + bh * (size_t)N * Wp;
+    int16_t* partner = reinterpret_cast<int16_t*>(dsm);
+    int16_t* prop = partner + N;
+    int16_t* ptr = prop + N;
     const int16_t* cand = a.cand + bh * (size_t)N * kTopC;
-
+    if (stage_lists) {
+        int16_t* lists = ptr + N;
+        for (int t = tid; t < N * kTopC; t += kPairThreads) lists[t] = cand[t];
+        cand = lists;
+    }
     for (int i = tid; i < N; i += kPairThreads) {
         partner[i] = -1;
         ptr[i] = 0;
     }
     __syncthreads();
-
-    // 3. mutual-best rounds over the own selection: the first unpaired entry of
-    // the sorted candidate list (paired cubes stay paired, so the scan resumes
-    // where the previous round stopped).
     for (int rd = 0; rd < kRounds1; ++rd) {
         for (int i = tid; i < N; i += kPairThreads) {
             int best = -1;
@@ -255,10 +236,8 @@ __global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a, in
         }
         __syncthreads();
     }
-
-    // 4. the unpaired cubes (first kMaxLeft, index order) within a window:
-    // overlaps with the kWindow list entries on each side, once (a warp per
-    // leftover cube, a lane per candidate), then kRounds2 rounds.
+    // The leftover list (first kMaxLeft unpaired cubes, index order).
+    int16_t* left = a.left + bh * kMaxLeft;
     int nleft = 0;
     for (int base = 0; base < N; base += kPairThreads) {
         const int i = base + tid;
@@ -268,37 +247,68 @@ __global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a, in
         if (f && nleft + r < kMaxLeft) left[nleft + r] = (int16_t)i;
         nleft += tot;
     }
-    nleft = min(nleft, kMaxLeft);
-    __syncthreads();
-    const bool staged = nleft * Wp <= rows_cap;
-    if (staged) {
-        for (int t = tid; t < nleft * (Wp / 4); t += kPairThreads) {
-            const int f = t / (Wp / 4), q = t - f * (Wp / 4);
-            reinterpret_cast<uint4*>(lrows)[t] = reinterpret_cast<const uint4*>(bm + (size_t)left[f] * Wp)[q];
-        }
-        __syncthreads();
+    if (tid == 0) a.nleft[bh] = min(nleft, kMaxLeft);
+    int16_t* pout = a.partner + bh * (size_t)N;
+    for (int i = tid; i < N; i += kPairThreads) pout[i] = partner[i];
+}
+
+// 4. Window overlaps: block (chunk of kWinChunk leftovers, b * heads + head).
+// Shared memory: the bitmap rows of the list entries the chunk's windows
+// reach (at most kWinChunk + kWin rows).
+__global__ void __launch_bounds__(kPairThreads) pair_window_kernel(PairArgs a) {
+    extern __shared__ __align__(16) uint32_t rows_s[];
+    const int Wp = a.Wp;
+    const size_t bh = blockIdx.y;
+    const int nleft = a.nleft[bh];
+    const int f0 = (int)blockIdx.x * kWinChunk;
+    if (f0 >= nleft) return;
+    const int f1 = min(nleft, f0 + kWinChunk);
+    const int g0 = max(0, f0 - kWindow), g1 = min(nleft, f1 + kWindow);
+    const int16_t* left = a.left + bh * kMaxLeft;
+    const uint32_t* bm = a.bm + bh * (size_t)a.N * Wp;
+    for (int t = threadIdx.x; t < (g1 - g0) * (Wp / 4); t += kPairThreads) {
+        const int g = t / (Wp / 4), q = t - g * (Wp / 4);
+        reinterpret_cast<uint4*>(rows_s + (size_t)g * Wp)[q] =
+            reinterpret_cast<const uint4*>(bm + (size_t)left[g0 + g] * Wp)[q];
     }
-    static_assert(2 * kWindow == 128, "one candidate per lane and slot of four");
-    for (int f = warp; f < nleft; f += kPairWarps) {
-        const uint32_t* rb[4];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const int d = lane + 32 * v;
-            const int g = d < kWindow ? f - kWindow + d : f + 1 + (d - kWindow);
-            rb[v] = (g >= 0 && g < nleft) ? (staged ? lrows + (size_t)g * Wp : bm + (size_t)left[g] * Wp) : nullptr;
-        }
-        int o[4];
-        if (staged)
-            bitmap_overlap4<true>(lrows + (size_t)f * Wp, rb, Wp, o);
-        else
-            bitmap_overlap4<false>(bm + (size_t)left[f] * Wp, rb, Wp, o);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) wov[(lane + 32 * v) * kWovStride + f] = (uint16_t)o[v];
+    __syncthreads();
+    uint16_t* wov = a.wov + bh * (size_t)kMaxLeft * kWin;
+    for (int t = threadIdx.x; t < (f1 - f0) * kWin; t += kPairThreads) {
+        const int f = f0 + t / kWin, d = t % kWin;
+        const int g = d < kWindow ? f - kWindow + d : f + 1 + (d - kWindow);
+        int o = 0;
+        if (g >= 0 && g < nleft)
+            o = smem_overlap(rows_s + (size_t)(f - g0) * Wp, rows_s + (size_t)(g - g0) * Wp, Wp);
+        wov[(size_t)f * kWin + d] = (uint16_t)o;
+    }
+}
+
+// 5. Rounds (c), (d) and the unit list, one CTA per (batch, head).  Shared
+// memory: window overlaps [kMaxLeft][kWin], partner and rest arrays [N].
+__global__ void __launch_bounds__(kPairThreads) pair_match2_kernel(PairArgs a) {
+    extern __shared__ __align__(16) unsigned char dsm[];
+    __shared__ int wsum[kPairWarps];
+    __shared__ uint32_t lfree[kMaxLeft / 32];
+    __shared__ int16_t left[kMaxLeft];
+    __shared__ int16_t lprop[kMaxLeft];
+    const int N = a.N;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t bh = blockIdx.x;
+    uint16_t* wov = reinterpret_cast<uint16_t*>(dsm);
+    int16_t* partner = reinterpret_cast<int16_t*>(wov + (size_t)kMaxLeft * kWin);
+    int16_t* rest = partner + N;
+    const int nleft = a.nleft[bh];
+    {
+        const int16_t* pin = a.partner + bh * (size_t)N;
+        for (int i = tid; i < N; i += kPairThreads) partner[i] = pin[i];
+        const int16_t* lin = a.left + bh * kMaxLeft;
+        for (int f = tid; f < nleft; f += kPairThreads) left[f] = lin[f];
+        const uint4* win = reinterpret_cast<const uint4*>(a.wov + bh * (size_t)kMaxLeft * kWin);
+        for (int t = tid; t < nleft * kWin / 8; t += kPairThreads) reinterpret_cast<uint4*>(wov)[t] = win[t];
     }
     __syncthreads();
     for (int rd = 0; rd < kRounds2; ++rd) {
-        // Unpaired list entries as a bitmask (the list is in increasing cube
-        // order, so list position breaks ties like the cube index).
+        // Unpaired list entries as a bitmask.
         for (int g0 = warp * 32; g0 < kMaxLeft; g0 += kPairThreads) {
             const int g = g0 + lane;
             const unsigned m = __ballot_sync(0xffffffffu, g < nleft && partner[left[min(g, nleft - 1)]] < 0);
@@ -311,11 +321,11 @@ __global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a, in
             uint32_t key = 0u;  // (overlap + 1) << 16 | (0xFFFF - g); 0: none
             if ((lfree[f >> 5] >> (f & 31)) & 1u) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
+                for (int v = 0; v < kWin / 32; ++v) {
                     const int d = lane + 32 * v;
                     const int g = d < kWindow ? f - kWindow + d : f + 1 + (d - kWindow);
                     if (g >= 0 && g < nleft && ((lfree[g >> 5] >> (g & 31)) & 1u)) {
-                        const uint32_t kk = ((uint32_t)wov[d * kWovStride + f] + 1u) << 16 | (uint32_t)(0xFFFF - g);
+                        const uint32_t kk = ((uint32_t)wov[f * kWin + d] + 1u) << 16 | (uint32_t)(0xFFFF - g);
                         key = kk > key ? kk : key;
                     }
                 }
@@ -333,26 +343,24 @@ __global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a, in
         }
         __syncthreads();
     }
-
-    // 5. the rest in index order.
+    // (d) the rest in index order.
     int nrest = 0;
     for (int base = 0; base < N; base += kPairThreads) {
         const int i = base + tid;
         const bool f = i < N && partner[i] < 0;
         int tot;
         const int r = chunk_rank(f, wsum, tot);
-        if (f) prop[nrest + r] = (int16_t)i;
+        if (f) rest[nrest + r] = (int16_t)i;
         nrest += tot;
     }
     __syncthreads();
     for (int q = tid; 2 * q + 1 < nrest; q += kPairThreads) {
-        const int x = prop[2 * q], y = prop[2 * q + 1];
+        const int x = rest[2 * q], y = rest[2 * q + 1];
         partner[x] = (int16_t)y;
         partner[y] = (int16_t)x;
     }
-    if (tid == 0 && (nrest & 1)) partner[prop[nrest - 1]] = prop[nrest - 1];
+    if (tid == 0 && (nrest & 1)) partner[rest[nrest - 1]] = rest[nrest - 1];
     __syncthreads();
-
     // Units in order of their smaller cube index.
     uint32_t* out = a.pairs + bh * (size_t)a.npairs;
     int u0 = 0;
@@ -371,14 +379,35 @@ __global__ void __launch_bounds__(kPairThreads) pair_match_kernel(PairArgs a, in
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+struct PairLayout {
+    size_t bm, cand, partner, left, nleft, wov, total;
+};
+
+PairLayout pair_layout(size_t bh, int ncubes, int words) {
+    PairLayout L;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t r = o;
+        o += align256(bytes);
+        return r;
+    };
+    L.bm = take(bh * ncubes * words * sizeof(uint32_t));
+    L.cand = take(bh * ncubes * kTopC * sizeof(int16_t));
+    L.partner = take(bh * ncubes * sizeof(int16_t));
+    L.left = take(bh * kMaxLeft * sizeof(int16_t));
+    L.nleft = take(bh * sizeof(int));
+    L.wov = take(bh * kMaxLeft * kWin * sizeof(uint16_t));
+    L.total = o;
+    return L;
+}
+
 }  // namespace
 
 int pair_words(int ncubes) { return ((ncubes + 31) / 32 + 3) & ~3; }
 
 size_t pair_workspace_bytes(int B, int heads, int ncubes, int topk) {
-    const size_t bh = (size_t)B * heads;
     (void)topk;
-    return align256(bh * ncubes * pair_words(ncubes) * sizeof(uint32_t)) + align256(bh * ncubes * kTopC * sizeof(int16_t));
+    return pair_layout((size_t)B * heads, ncubes, pair_words(ncubes)).total;
 }
 
 int pair_max_cubes() { return kPairMaxCubes; }
@@ -386,48 +415,76 @@ int pair_max_topk() { return kPairMaxTopk; }
 
 cudaError_t launch_pair(const int32_t* topk_idx, int B, int ncubes, int heads, int topk, void* workspace,
                         uint32_t* pairs, int num_sms, int max_smem, cudaStream_t stream) {
+    const size_t bh = (size_t)B * heads;
+    const int N = ncubes, k = topk;
     PairArgs a;
     a.idx = topk_idx;
-    a.N = ncubes;
-    a.k = topk;
-    a.Wp = pair_words(ncubes);
-    a.npairs = (ncubes + 1) / 2;
-    const size_t bh = (size_t)B * heads;
-    a.bm = static_cast<uint32_t*>(workspace);
-    a.cand = reinterpret_cast<int16_t*>(static_cast<unsigned char*>(workspace) +
-                                        align256(bh * ncubes * a.Wp * sizeof(uint32_t)));
+    a.N = N;
+    a.k = k;
+    a.Wp = pair_words(N);
+    a.npairs = (N + 1) / 2;
+    const PairLayout L = pair_layout(bh, N, a.Wp);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    a.bm = reinterpret_cast<uint32_t*>(ws + L.bm);
+    a.cand = reinterpret_cast<int16_t*>(ws + L.cand);
+    a.partner = reinterpret_cast<int16_t*>(ws + L.partner);
+    a.left = reinterpret_cast<int16_t*>(ws + L.left);
+    a.nleft = reinterpret_cast<int*>(ws + L.nleft);
+    a.wov = reinterpret_cast<uint16_t*>(ws + L.wov);
     a.pairs = pairs;
-    const size_t rows = bh * ncubes;
+    const size_t budget = kSmemBudget < (size_t)max_smem - 1024 ? kSmemBudget : (size_t)max_smem - 1024;
+    cudaError_t e;
+
+    // 1. bitmaps
+    const size_t rows = bh * N;
     pair_bitmap_kernel<<<(unsigned)((rows + kPairWarps - 1) / kPairWarps), kPairThreads, 0, stream>>>(a, rows);
-    const size_t bm_bytes = (size_t)ncubes * a.Wp * sizeof(uint32_t);
-    const bool stage_bm = bm_bytes <= (size_t)max_smem - 1024;
-    const size_t dyn_c = stage_bm ? bm_bytes : 0;
+
+    // 2. candidate lists: first the staged row stride cs (an odd number of
+    // quads, at most ~60% of the budget, at most the padded row), then rows
+    // per block (about two blocks per SM in all) within the rest.
+    int cs = (int)(((budget * 3 / 5) / ((size_t)N * 4)) & ~(size_t)3);
+    if (cs > 0 && ((cs / 4) & 1) == 0) cs -= 4;
+    const int wp_odd = ((a.Wp / 4) & 1) ? a.Wp : a.Wp + 4;
+    if (cs > wp_odd) cs = wp_odd;
+    if (cs < 4) cs = 4;
+    const int cw = cs > a.Wp ? a.Wp : cs;
+    const size_t cols_bytes = (size_t)N * cs * 4;
+    if (cols_bytes + (size_t)k * 4 > budget) return cudaErrorInvalidValue;
     int chunks = (int)((2 * (size_t)num_sms + bh - 1) / bh);
     chunks = chunks < 1 ? 1 : chunks;
-    const int max_chunks = (ncubes + kPairWarps - 1) / kPairWarps;
-    chunks = chunks > max_chunks ? max_chunks : chunks;
-    auto pick = [&](auto staged) -> void (*)(PairArgs) {
-        constexpr bool S = decltype(staged)::value;
-        if (topk <= 128) return pair_candidates_kernel<S, 4>;
-        if (topk <= 256) return pair_candidates_kernel<S, 8>;
-        return pair_candidates_kernel<S, 16>;
-    };
-    void (*cand_kernel)(PairArgs) = stage_bm ? pick(std::true_type()) : pick(std::false_type());
-    cudaError_t e = cudaFuncSetAttribute(cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_c);
+    int rb = (N + chunks - 1) / chunks;
+    const size_t rb_cap = (budget - cols_bytes) / ((size_t)k * 4);
+    if ((size_t)rb > rb_cap) rb = (int)rb_cap;
+    chunks = (N + rb - 1) / rb;
+    const size_t dyn_c = cols_bytes + (size_t)rb * k * 4;
+    auto cand_kernel = k <= 128 ? pair_candidates_kernel<4> : k <= 256 ? pair_candidates_kernel<8>
+                                                                        : pair_candidates_kernel<16>;
+    e = cudaFuncSetAttribute(cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_c);
     if (e != cudaSuccess) return e;
-    cand_kernel<<<dim3((unsigned)chunks, (unsigned)bh), kPairThreads, dyn_c, stream>>>(a);
-    // Matching: window overlaps, N-entry arrays, leftover list, then as many
-    // leftover bitmap rows as the rest of the shared memory holds.
-    const size_t fixed = (size_t)2 * kWindow * kWovStride * sizeof(uint16_t) + 3 * (size_t)ncubes * 2 +
-                         2 * (size_t)kMaxLeft * 2 + 16;
-    const size_t avail = (size_t)max_smem - 1024;  // static shared memory of the kernel is below 1 KB
-    if (fixed > avail) return cudaErrorInvalidValue;
-    const size_t rows_bytes = avail - fixed < (size_t)kMaxLeft * a.Wp * 4 ? avail - fixed : (size_t)kMaxLeft * a.Wp * 4;
-    const int rows_cap = (int)(rows_bytes / 4);
-    const size_t dyn = fixed + rows_bytes;
-    e = cudaFuncSetAttribute(pair_match_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    cand_kernel<<<dim3((unsigned)chunks, (unsigned)bh), kPairThreads, dyn_c, stream>>>(a, rb, cw, cs);
+
+    // 3. rounds (b)
+    const size_t arrays = 3 * (size_t)N * sizeof(int16_t);
+    const size_t lists = (size_t)N * kTopC * sizeof(int16_t);
+    const int stage_lists = arrays + lists <= budget ? 1 : 0;
+    const size_t dyn_1 = arrays + (stage_lists ? lists : 0);
+    e = cudaFuncSetAttribute(pair_match1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_1);
     if (e != cudaSuccess) return e;
-    pair_match_kernel<<<(unsigned)bh, kPairThreads, dyn, stream>>>(a, rows_cap);
+    pair_match1_kernel<<<(unsigned)bh, kPairThreads, dyn_1, stream>>>(a, stage_lists);
+
+    // 4. window overlaps
+    const size_t dyn_w = (size_t)(kWinChunk + kWin) * a.Wp * sizeof(uint32_t);
+    if (dyn_w > budget) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(pair_window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_w);
+    if (e != cudaSuccess) return e;
+    pair_window_kernel<<<dim3(kMaxLeft / kWinChunk, (unsigned)bh), kPairThreads, dyn_w, stream>>>(a);
+
+    // 5. rounds (c), (d), units
+    const size_t dyn_2 = (size_t)kMaxLeft * kWin * sizeof(uint16_t) + 2 * (size_t)N * sizeof(int16_t);
+    if (dyn_2 > budget) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(pair_match2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_2);
+    if (e != cudaSuccess) return e;
+    pair_match2_kernel<<<(unsigned)bh, kPairThreads, dyn_2, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -111,10 +111,16 @@ def test_pairing_validation(lib):
     assert f(A, 1, 9000, 2, 3, A, A, None) == UNSUPPORTED  # ncubes > 8192
     assert f(A, 1, 12, 2, 3, MIS, A, None) == ALIGNMENT   # workspace
     assert f(A, 1, 12, 2, 3, A, A + 2, None) == ALIGNMENT  # pairs
-    # bitmaps: 4-word rows (12 cubes -> 1 word, rounded up to 4), then the lists
-    assert lib.vsa_pair_workspace_bytes(1, 2, 12, 3) == 512 + 768  # bitmaps 2*12*4*4 B -> 512; lists 2*12*16*2 B
-    # bitmaps 40*624 rows of 20 words; candidate lists of 16 int16 per cube
-    assert lib.vsa_pair_workspace_bytes(1, 40, 624, 78) == 40 * 624 * 20 * 4 + 40 * 624 * 16 * 2
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    # per (b, head): bitmaps N x Wp words (Wp: N/32 rounded up to 4), candidate
+    # lists N x 16 int16, partner N int16, leftover list 640 int16, its length,
+    # window overlaps 640 x 128 uint16; each region 256-byte aligned
+    def ws(bh, n):
+        wp = ((n + 31) // 32 + 3) // 4 * 4
+        return (a256(bh * n * wp * 4) + a256(bh * n * 16 * 2) + a256(bh * n * 2) + a256(bh * 640 * 2)
+                + a256(bh * 4) + a256(bh * 640 * 128 * 2))
+    assert lib.vsa_pair_workspace_bytes(1, 2, 12, 3) == ws(2, 12) == 512 + 768 + 256 + 2560 + 256 + 327680
+    assert lib.vsa_pair_workspace_bytes(1, 40, 624, 78) == ws(40, 624)
     g = lib.vsa_sparse_attn_fwd_paired
     assert g(A, A, A, A, A, A + 2, 1, 12, 2, 64, 3, 0.0, A, None, None) == ALIGNMENT  # pairs
     assert g(A, A, A, A, A, None, 1, 12, 2, 64, 0, 0.0, A, None, None) == INVALID
