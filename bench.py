@@ -41,7 +41,7 @@ if HERE not in sys.path:
 METRIC = "VSA sparse-attn fwd ms/call and effective TFLOPS; % of GB300 bf16 TC peak"
 UNIT = "TFLOPS (effective)"
 WORKLOAD = "wan"
-KERNELS_PER_STEP = 10  # tile x3, pool sums, score/top-k, pairing x3, sparse attention, untile
+KERNELS_PER_STEP = 12  # tile x3, pool sums, score/top-k, pairing x5, sparse attention, untile
 
 # DRAM traffic of one fine_fwd_kernel launch, from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum) of the Wan grid with 8 heads, scaled by 40/8 (traffic grows with
