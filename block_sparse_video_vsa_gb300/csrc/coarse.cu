@@ -231,6 +231,145 @@ __device__ double precise_score(const double* __restrict__ qsum, const ScoreArgs
     return (double)a.sm_scale * acc * inv_vq / (double)vk;
 }
 
+// Top-k of one score row (one warp): the k-th largest fp32 score by bitwise
+// search, then the scores within the fp32 error band of that boundary are
+// re-ranked in fp64 from the exact cube sums; the selected cube ids are
+// written in ascending order.  `row` (shared or global memory) is scratch:
+// band members are overwritten with +inf (chosen) or -inf.  kMaxCase bounds
+// the register-held search (N <= 128 * kMaxCase); longer rows are searched in
+// place.
+template <int D, int kMaxCase>
+__device__ void select_row(float* row, const ScoreArgs& a, size_t bh, size_t hrow, int i, float qnorm_i,
+                           float kmax_all, double* qsum, double* cs, int* cj, int lane) {
+    const int N = a.N;
+    const int k = a.topk;
+    uint32_t T;
+    switch ((N + 127) / 128) {  // register slots per lane: N / 32 rounded up to a multiple of 4
+        case 1: T = kth_key<4>(row, N, k, lane); break;
+        case 2: T = kth_key<8>(row, N, k, lane); break;
+        case 3: T = kth_key<12>(row, N, k, lane); break;
+        case 4: T = kth_key<16>(row, N, k, lane); break;
+        case 5: T = kth_key<20>(row, N, k, lane); break;
+        case 6: T = kth_key<24>(row, N, k, lane); break;
+        case 7: T = kth_key<28>(row, N, k, lane); break;
+        case 8: T = kth_key<32>(row, N, k, lane); break;
+        default:
+            if constexpr (kMaxCase >= 16) {
+                const int c = (N + 127) / 128;
+                if (c <= 10) T = kth_key<40>(row, N, k, lane);
+                else if (c <= 12) T = kth_key<48>(row, N, k, lane);
+                else if (c <= 14) T = kth_key<56>(row, N, k, lane);
+                else if (c <= 16) T = kth_key<64>(row, N, k, lane);
+                else T = kth_key_smem(row, N, k, lane);
+            } else {
+                T = kth_key_smem(row, N, k, lane);
+            }
+            break;
+    }
+    const float tau = key2f(T);
+    // Error bound of an fp32 score against the exact one (dot of rounded
+    // means with fp32 accumulation, then the scale): (D + 8) u |q||k|,
+    // doubled for margin; the band is twice that around tau.
+    const float eps = 2.f * (float)(D + 8) * 5.9604645e-8f * a.sm_scale * qnorm_i * kmax_all;
+    const float band = 2.f * eps + 1e-30f;
+    const float lo = tau - band, hi = tau + band;
+    int cA = 0, cC = 0;
+    for (int j = lane; j < N; j += 32) {
+        const float s = row[j];
+        cA += s > hi;
+        cC += (s >= lo) && (s <= hi);
+    }
+    cA = __reduce_add_sync(0xffffffffu, cA);
+    cC = __reduce_add_sync(0xffffffffu, cC);
+    const int need = k - cA;  // 1 <= need <= cC
+    const bool take_band = (cC == need);  // the whole band is selected: no re-ranking
+    if (!take_band) {
+        // Re-rank the boundary band with exact cube sums in fp64.
+        const size_t qrow = hrow + (size_t)i * D;
+        const int vq = clamp_vbs(a.vbs[i]);
+        for (int d = lane; d < D; d += 32)
+            qsum[d] = fma((double)a.qm[qrow + d], (double)vq, (double)a.qr[qrow + d]);
+        __syncwarp();
+        const double inv_vq = vq > 0 ? 1.0 / (double)vq : 0.0;
+        if (cC <= kCandCap) {
+            int pos = 0;
+            for (int j0b = 0; j0b < N; j0b += 32) {
+                const int j = j0b + lane;
+                const bool inC = j < N && row[j] >= lo && row[j] <= hi;
+                const unsigned m = __ballot_sync(0xffffffffu, inC);
+                if (inC) cj[pos + __popc(m & ((1u << lane) - 1u))] = j;
+                pos += __popc(m);
+            }
+            __syncwarp();
+            for (int c = lane; c < cC; c += 32) cs[c] = precise_score<D>(qsum, a, hrow, cj[c], inv_vq);
+            __syncwarp();
+            // rank among candidates: (score desc, index asc); chosen if rank < need.
+            for (int c = lane; c < cC; c += 32) {
+                const double s = cs[c];
+                const int jc = cj[c];
+                int rank = 0;
+                for (int o = 0; o < cC; ++o) {
+                    const double so = cs[o];
+                    rank += (so > s) || (so == s && cj[o] < jc);
+                }
+                row[jc] = rank < need ? INFINITY : -INFINITY;
+            }
+            __syncwarp();
+        } else {
+            // Degenerate band (many near-equal scores): 64-bit bitwise search
+            // over the exact scores of the band, recomputed per pass.
+            unsigned long long T2 = 0;
+            for (int bit = 63; bit >= 0; --bit) {
+                const unsigned long long cand = T2 | (1ull << bit);
+                int cnt = 0;
+                for (int j = lane; j < N; j += 32)
+                    if (row[j] >= lo && row[j] <= hi)
+                        cnt += d2key(precise_score<D>(qsum, a, hrow, j, inv_vq)) >= cand;
+                cnt = __reduce_add_sync(0xffffffffu, cnt);
+                if (cnt >= need) T2 = cand;
+            }
+            int greater = 0;
+            for (int j = lane; j < N; j += 32)
+                if (row[j] >= lo && row[j] <= hi)
+                    greater += d2key(precise_score<D>(qsum, a, hrow, j, inv_vq)) > T2;
+            greater = __reduce_add_sync(0xffffffffu, greater);
+            int eq_left = need - greater;  // equal-to-T2 members to take, lowest index first
+            for (int j0b = 0; j0b < N; j0b += 32) {
+                const int j = j0b + lane;
+                bool inC = j < N && row[j] >= lo && row[j] <= hi;
+                unsigned long long kk = 0;
+                if (inC) kk = d2key(precise_score<D>(qsum, a, hrow, j, inv_vq));
+                const bool eq = inC && kk == T2;
+                const unsigned m = __ballot_sync(0xffffffffu, eq);
+                const int before = __popc(m & ((1u << lane) - 1u));
+                if (inC) row[j] = (kk > T2 || (eq && before < eq_left)) ? INFINITY : -INFINITY;
+                eq_left -= __popc(m);
+            }
+            __syncwarp();
+        }
+    }
+    // Emit the selected set in ascending cube index.  After re-ranking the
+    // band members hold +inf (chosen) or -inf (not chosen).
+    int32_t* out = a.topk_idx + (bh * N + i) * (size_t)k;
+    int pos = 0;
+    const unsigned below = (1u << lane) - 1u;
+    for (int j0b = 0; j0b < N; j0b += 128) {  // four 32-wide slices per pass: loads batched
+        bool sel[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = j0b + 32 * q + lane;
+            const float x = j < N ? row[j] : -INFINITY;
+            sel[q] = j < N && (x > hi || (take_band && x >= lo));
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const unsigned m = __ballot_sync(0xffffffffu, sel[q]);
+            if (sel[q]) out[pos + __popc(m & below)] = j0b + 32 * q + lane;
+            pos += __popc(m);
+        }
+    }
+}
+
 // WARPS warps; each thread scores RT query rows (R = WARPS * RT rows per block).
 template <int D, int RT, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) score_topk_kernel(ScoreArgs a) {
@@ -342,130 +481,101 @@ __global__ void __launch_bounds__(WARPS * 32) score_topk_kernel(ScoreArgs a) {
     }
 
     // Selection: one warp per row.
-    const int k = a.topk;
     for (int r = warp; r < R; r += kWarps) {
         const int i = i0 + r;
         if (i >= N) break;
-        float* row = sc + (size_t)r * N;
-        // k-th largest key by bitwise search: largest T with count(key >= T) >= k.
-        uint32_t T;
-        switch ((N + 127) / 128) {  // register slots per lane: N / 32 rounded up to a multiple of 4
-            case 1: T = kth_key<4>(row, N, k, lane); break;
-            case 2: T = kth_key<8>(row, N, k, lane); break;
-            case 3: T = kth_key<12>(row, N, k, lane); break;
-            case 4: T = kth_key<16>(row, N, k, lane); break;
-            case 5: T = kth_key<20>(row, N, k, lane); break;
-            case 6: T = kth_key<24>(row, N, k, lane); break;
-            case 7: T = kth_key<28>(row, N, k, lane); break;
-            case 8: T = kth_key<32>(row, N, k, lane); break;
-            default: T = kth_key_smem(row, N, k, lane); break;
-        }
-        const float tau = key2f(T);
-        // Error bound of an fp32 score against the exact one (dot of rounded
-        // means with fp32 accumulation, then the scale): (D + 8) u |q||k|,
-        // doubled for margin; the band is twice that around tau.
-        const float eps = 2.f * (float)(D + 8) * 5.9604645e-8f * a.sm_scale * qnorm[r] * kmax_all;
-        const float band = 2.f * eps + 1e-30f;
-        const float lo = tau - band, hi = tau + band;
-        int cA = 0, cC = 0;
-        for (int j = lane; j < N; j += 32) {
-            const float s = row[j];
-            cA += s > hi;
-            cC += (s >= lo) && (s <= hi);
-        }
-        cA = __reduce_add_sync(0xffffffffu, cA);
-        cC = __reduce_add_sync(0xffffffffu, cC);
-        const int need = k - cA;  // 1 <= need <= cC
-        const bool take_band = (cC == need);  // the whole band is selected: no re-ranking
-        if (!take_band) {
-            // Re-rank the boundary band with exact cube sums in fp64.
-            double* qsum = qsum_w + warp * D;
-            const size_t qrow = hrow + (size_t)i * D;
-            const int vq = clamp_vbs(a.vbs[i]);
-            for (int d = lane; d < D; d += 32)
-                qsum[d] = fma((double)a.qm[qrow + d], (double)vq, (double)a.qr[qrow + d]);
-            __syncwarp();
-            const double inv_vq = vq > 0 ? 1.0 / (double)vq : 0.0;
-            if (cC <= kCandCap) {
-                double* cs = cand_s + warp * kCandCap;
-                int* cj = cand_j + warp * kCandCap;
-                int pos = 0;
-                for (int j0b = 0; j0b < N; j0b += 32) {
-                    const int j = j0b + lane;
-                    const bool inC = j < N && row[j] >= lo && row[j] <= hi;
-                    const unsigned m = __ballot_sync(0xffffffffu, inC);
-                    if (inC) cj[pos + __popc(m & ((1u << lane) - 1u))] = j;
-                    pos += __popc(m);
-                }
-                __syncwarp();
-                for (int c = lane; c < cC; c += 32) cs[c] = precise_score<D>(qsum, a, hrow, cj[c], inv_vq);
-                __syncwarp();
-                // rank among candidates: (score desc, index asc); chosen if rank < need.
-                for (int c = lane; c < cC; c += 32) {
-                    const double s = cs[c];
-                    const int jc = cj[c];
-                    int rank = 0;
-                    for (int o = 0; o < cC; ++o) {
-                        const double so = cs[o];
-                        rank += (so > s) || (so == s && cj[o] < jc);
-                    }
-                    row[jc] = rank < need ? INFINITY : -INFINITY;
-                }
-                __syncwarp();
-            } else {
-                // Degenerate band (many near-equal scores): 64-bit bitwise search
-                // over the exact scores of the band, recomputed per pass.
-                unsigned long long T2 = 0;
-                for (int bit = 63; bit >= 0; --bit) {
-                    const unsigned long long cand = T2 | (1ull << bit);
-                    int cnt = 0;
-                    for (int j = lane; j < N; j += 32)
-                        if (row[j] >= lo && row[j] <= hi)
-                            cnt += d2key(precise_score<D>(qsum, a, hrow, j, inv_vq)) >= cand;
-                    cnt = __reduce_add_sync(0xffffffffu, cnt);
-                    if (cnt >= need) T2 = cand;
-                }
-                int greater = 0;
-                for (int j = lane; j < N; j += 32)
-                    if (row[j] >= lo && row[j] <= hi)
-                        greater += d2key(precise_score<D>(qsum, a, hrow, j, inv_vq)) > T2;
-                greater = __reduce_add_sync(0xffffffffu, greater);
-                int eq_left = need - greater;  // equal-to-T2 members to take, lowest index first
-                for (int j0b = 0; j0b < N; j0b += 32) {
-                    const int j = j0b + lane;
-                    bool inC = j < N && row[j] >= lo && row[j] <= hi;
-                    unsigned long long kk = 0;
-                    if (inC) kk = d2key(precise_score<D>(qsum, a, hrow, j, inv_vq));
-                    const bool eq = inC && kk == T2;
-                    const unsigned m = __ballot_sync(0xffffffffu, eq);
-                    const int before = __popc(m & ((1u << lane) - 1u));
-                    if (inC) row[j] = (kk > T2 || (eq && before < eq_left)) ? INFINITY : -INFINITY;
-                    eq_left -= __popc(m);
-                }
-                __syncwarp();
-            }
-        }
-        // Emit the selected set in ascending cube index.  After re-ranking the
-        // band members hold +inf (chosen) or -inf (not chosen).
-        int32_t* out = a.topk_idx + (bh * N + i) * (size_t)k;
-        int pos = 0;
-        const unsigned below = (1u << lane) - 1u;
-        for (int j0b = 0; j0b < N; j0b += 128) {  // four 32-wide slices per pass: loads batched
-            bool sel[4];
+        select_row<D, 8>(sc + (size_t)r * N, a, bh, hrow, i, qnorm[r], kmax_all, qsum_w + warp * D,
+                         cand_s + warp * kCandCap, cand_j + warp * kCandCap, lane);
+    }
+}
+
+// ------------------------------------------- large N: scores through memory
+// When few query rows fit the fused kernel's shared memory (N above ~1100 at
+// D = 128), the scores go to the workspace instead: a register-tiled fp32
+// GEMM (128 x 128 score tiles, the full depth D in shared memory, each thread
+// 8 x 8 scores on rows ty + 16 r and columns tx + 16 c; products accumulated
+// in increasing d as in the fused kernel, so the scores are the same), then
+// one warp per row runs the same selection on the row read back.
+constexpr int kGemmTile = 128;
+
+template <int D>
+__global__ void __launch_bounds__(256) score_gemm_kernel(ScoreArgs a, float* __restrict__ scores) {
+    constexpr int LD = D + 4;  // padded row (floats)
+    extern __shared__ __align__(16) float gsm[];
+    float* As = gsm;                   // [kGemmTile][LD] query means
+    float* Bs = gsm + kGemmTile * LD;  // [kGemmTile][LD] key means
+    const int N = a.N;
+    const int i0 = blockIdx.x * kGemmTile, j0 = blockIdx.y * kGemmTile;
+    const size_t bh = blockIdx.z;
+    const size_t hrow = bh * (size_t)N * D;
+    const int tid = threadIdx.x;
+    for (int e = tid; e < kGemmTile * (D / 4); e += 256) {
+        const int r = e / (D / 4), d4 = e - r * (D / 4);
+        float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
+        if (i0 + r < N) va = *reinterpret_cast<const float4*>(a.qm + hrow + (size_t)(i0 + r) * D + 4 * d4);
+        if (j0 + r < N) vb = *reinterpret_cast<const float4*>(a.km + hrow + (size_t)(j0 + r) * D + 4 * d4);
+        *reinterpret_cast<float4*>(As + r * LD + 4 * d4) = va;
+        *reinterpret_cast<float4*>(Bs + r * LD + 4 * d4) = vb;
+    }
+    __syncthreads();
+    const int ty = tid >> 4, tx = tid & 15;
+    float acc[8][8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = j0b + 32 * q + lane;
-                const float x = j < N ? row[j] : -INFINITY;
-                sel[q] = j < N && (x > hi || (take_band && x >= lo));
-            }
+    for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const unsigned m = __ballot_sync(0xffffffffu, sel[q]);
-                if (sel[q]) out[pos + __popc(m & below)] = j0b + 32 * q + lane;
-                pos += __popc(m);
+        for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+#pragma unroll 2
+    for (int d = 0; d < D; d += 4) {
+        float4 av[8], bv[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) av[r] = *reinterpret_cast<const float4*>(As + (ty + 16 * r) * LD + d);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) bv[c] = *reinterpret_cast<const float4*>(Bs + (tx + 16 * c) * LD + d);
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                acc[r][c] = fmaf(av[r].x, bv[c].x, acc[r][c]);
+                acc[r][c] = fmaf(av[r].y, bv[c].y, acc[r][c]);
+                acc[r][c] = fmaf(av[r].z, bv[c].z, acc[r][c]);
+                acc[r][c] = fmaf(av[r].w, bv[c].w, acc[r][c]);
             }
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int i = i0 + ty + 16 * r;
+        if (i >= N) continue;
+        float* dst = scores + (bh * N + i) * (size_t)N;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int j = j0 + tx + 16 * c;
+            if (j < N) dst[j] = a.sm_scale * acc[r][c];
         }
     }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) select_kernel(ScoreArgs a, float* __restrict__ scores) {
+    __shared__ double qsum_w[8][D];
+    __shared__ double cand_s[8][kCandCap];
+    __shared__ int cand_j[8][kCandCap];
+    __shared__ float red[8];
+    const int N = a.N;
+    const size_t bh = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float kmax = 0.f;  // largest key-mean norm of this head
+    for (int j = tid; j < N; j += 256) kmax = fmaxf(kmax, a.kn[bh * N + j]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    if (lane == 0) red[warp] = kmax;
+    __syncthreads();
+    float kmax_all = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) kmax_all = fmaxf(kmax_all, red[w]);
+    const int i = blockIdx.x * 8 + warp;
+    if (i >= N) return;
+    select_row<D, 16>(scores + (bh * N + i) * (size_t)N, a, bh, bh * (size_t)N * D, i, a.qn[bh * N + i],
+                      kmax_all, qsum_w[warp], cand_s[warp], cand_j[warp], lane);
 }
 
 // --------------------------------------------------------------- validator
@@ -519,8 +629,14 @@ __global__ void debug_wait_kernel(long long limit_ns, int32_t* result, unsigned 
 
 }  // namespace
 
+// Scores go through the workspace when the fused kernel would hold fewer than
+// 32 query rows per block.
+static bool scores_in_memory(int ncubes, int D);
+
 size_t coarse_workspace_bytes(int B, int heads, int ncubes, int D) {
-    return (size_t)16 * B * heads * ncubes * D + (size_t)8 * B * heads * ncubes;
+    size_t bytes = (size_t)16 * B * heads * ncubes * D + (size_t)8 * B * heads * ncubes;
+    if (scores_in_memory(ncubes, D)) bytes += (size_t)4 * B * heads * ncubes * ncubes;  // fp32 scores
+    return bytes;
 }
 
 // Score-block shapes: R rows per block on 16 warps (R = 32: two rows per
@@ -534,7 +650,12 @@ int coarse_rows_per_block(int ncubes, int D) {
     return 8;
 }
 
-size_t coarse_smem_bytes(int R, int N, int D) { return score_layout(R, N, D, score_warps(R)).total; }
+static bool scores_in_memory(int ncubes, int D) { return coarse_rows_per_block(ncubes, D) < 32; }
+
+size_t coarse_smem_bytes(int R, int N, int D) {
+    if (scores_in_memory(N, D)) return (size_t)2 * kGemmTile * (D + 4) * sizeof(float);
+    return score_layout(R, N, D, score_warps(R)).total;
+}
 
 cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes,
                           int heads, int D, int topk, float sm_scale, void* workspace,
@@ -567,6 +688,19 @@ cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, in
     a.topk = topk;
     a.R = coarse_rows_per_block(ncubes, D);
     a.sm_scale = sm_scale;
+    if (scores_in_memory(ncubes, D)) {
+        float* scores = po.norm + 2 * (size_t)B * heads * ncubes;
+        const size_t gsmem = (size_t)2 * kGemmTile * (D + 4) * sizeof(float);
+        const int tiles = (ncubes + kGemmTile - 1) / kGemmTile;
+        const dim3 gg(tiles, tiles, B * heads);
+        auto gemm = D == 128 ? score_gemm_kernel<128> : score_gemm_kernel<64>;
+        e = cudaFuncSetAttribute(gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsmem);
+        if (e != cudaSuccess) return e;
+        gemm<<<gg, 256, gsmem, stream>>>(a, scores);
+        auto sel = D == 128 ? select_kernel<128> : select_kernel<64>;
+        sel<<<dim3((ncubes + 7) / 8, B * heads), 256, 0, stream>>>(a, scores);
+        return cudaGetLastError();
+    }
     const size_t smem = coarse_smem_bytes(a.R, ncubes, D);
     dim3 grid((ncubes + a.R - 1) / a.R, heads, B);
     auto pick = [&](auto d) {

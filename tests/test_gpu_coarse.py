@@ -91,3 +91,29 @@ def test_all_scores_equal():
     vbs = np.full(N, 64, np.int32)
     got = vsa.coarse_select(to_dev(qt), to_dev(kt), i32_dev(vbs), k, 0.0).cpu().numpy()
     assert (got == np.arange(k)).all()
+
+
+# ---- large N: scores through the workspace (score GEMM, then per-row selection)
+def test_random_data_scores_in_memory():
+    wl = synth.Workload("big", 1, 29, 48, 52, heads=2, D=128, topk=100, seed=91)  # 8*12*13 = 1248 cubes
+    rows, differ = run_case(wl)
+    assert differ <= rows * 1e-3
+
+
+@pytest.mark.parametrize("N,D,k", [(1200, 128, 400), (1500, 64, 31)])
+def test_exact_ties_scores_in_memory(N, D, k):
+    const_q = np.zeros(D, np.float32)
+    const_q[:4] = [1.0, 1.0, 0.5, 0.5]
+    qt, kt, vbs = exact_tie_case(N, D, k, const_q)
+    ref = oracle.coarse(qt, kt, vbs, k, 0.125)
+    got = vsa.coarse_select(to_dev(qt), to_dev(kt), i32_dev(vbs), k, 0.125).cpu().numpy()
+    assert np.array_equal(np.sort(ref, -1), got)
+
+
+def test_all_scores_equal_scores_in_memory():
+    N, D, k = 1300, 128, 200  # the whole row is the band: the fp64 search over 1300 equal scores
+    qt = np.zeros((1, 64 * N, 1, D), np.uint16)
+    kt = synth.bf16_bits(np.random.default_rng(4).standard_normal((1, 64 * N, 1, D), dtype=np.float32))
+    vbs = np.full(N, 64, np.int32)
+    got = vsa.coarse_select(to_dev(qt), to_dev(kt), i32_dev(vbs), k, 0.0).cpu().numpy()
+    assert (got == np.arange(k)).all()
