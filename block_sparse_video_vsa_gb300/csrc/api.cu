@@ -112,7 +112,7 @@ vsa_status vsa_untile(const vsa_grid* g, const void* yt, void* y, vsa_stream_t s
 
 size_t vsa_coarse_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t D) {
     if (B <= 0 || heads <= 0 || ncubes <= 0 || D <= 0) return 0;
-    return coarse_workspace_bytes(B, heads, ncubes, D);
+    return coarse_workspace_bytes(B, heads, ncubes, D, coarse_split_default(ncubes, D));
 }
 
 vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs, int32_t B, int32_t ncubes,
@@ -129,10 +129,11 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
     DevCtx ctx;
     cudaError_t e = get_dev_ctx(&ctx);
     if (e != cudaSuccess) return VSA_ERR_CUDA;
-    const size_t smem = coarse_smem_bytes(coarse_rows_per_block(ncubes, D), ncubes, D);
+    const bool split = coarse_split_default(ncubes, D);
+    const size_t smem = coarse_smem_bytes(ncubes, D, split);
     if (smem > (size_t)ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
-    return from_cuda(launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, workspace, topk_idx,
+    return from_cuda(launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, workspace, topk_idx, split,
                                    static_cast<cudaStream_t>(stream)));
 }
 

@@ -629,13 +629,9 @@ __global__ void debug_wait_kernel(long long limit_ns, int32_t* result, unsigned 
 
 }  // namespace
 
-// Scores go through the workspace when the fused kernel would hold fewer than
-// 32 query rows per block.
-static bool scores_in_memory(int ncubes, int D);
-
-size_t coarse_workspace_bytes(int B, int heads, int ncubes, int D) {
+size_t coarse_workspace_bytes(int B, int heads, int ncubes, int D, bool split) {
     size_t bytes = (size_t)16 * B * heads * ncubes * D + (size_t)8 * B * heads * ncubes;
-    if (scores_in_memory(ncubes, D)) bytes += (size_t)4 * B * heads * ncubes * ncubes;  // fp32 scores
+    if (split) bytes += (size_t)4 * B * heads * ncubes * ncubes;  // fp32 scores
     return bytes;
 }
 
@@ -650,16 +646,19 @@ int coarse_rows_per_block(int ncubes, int D) {
     return 8;
 }
 
-static bool scores_in_memory(int ncubes, int D) { return coarse_rows_per_block(ncubes, D) < 32; }
+// Scores through memory (score GEMM + per-row selection) from 256 cubes, and
+// whenever the fused kernel would hold fewer than 32 query rows per block.
+bool coarse_split_default(int ncubes, int D) { return ncubes >= 256 || coarse_rows_per_block(ncubes, D) < 32; }
 
-size_t coarse_smem_bytes(int R, int N, int D) {
-    if (scores_in_memory(N, D)) return (size_t)2 * kGemmTile * (D + 4) * sizeof(float);
+size_t coarse_smem_bytes(int N, int D, bool split) {
+    if (split) return (size_t)2 * kGemmTile * (D + 4) * sizeof(float);
+    const int R = coarse_rows_per_block(N, D);
     return score_layout(R, N, D, score_warps(R)).total;
 }
 
 cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes,
                           int heads, int D, int topk, float sm_scale, void* workspace,
-                          int32_t* topk_idx, cudaStream_t stream) {
+                          int32_t* topk_idx, bool split, cudaStream_t stream) {
     float* ws = static_cast<float*>(workspace);
     const size_t half = (size_t)B * heads * ncubes * D;  // one [B][heads][N][D] plane
     PoolOut po;
@@ -688,7 +687,7 @@ cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, in
     a.topk = topk;
     a.R = coarse_rows_per_block(ncubes, D);
     a.sm_scale = sm_scale;
-    if (scores_in_memory(ncubes, D)) {
+    if (split) {
         float* scores = po.norm + 2 * (size_t)B * heads * ncubes;
         const size_t gsmem = (size_t)2 * kGemmTile * (D + 4) * sizeof(float);
         const int tiles = (ncubes + kGemmTile - 1) / kGemmTile;
@@ -701,7 +700,7 @@ cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, in
         sel<<<dim3((ncubes + 7) / 8, B * heads), 256, 0, stream>>>(a, scores);
         return cudaGetLastError();
     }
-    const size_t smem = coarse_smem_bytes(a.R, ncubes, D);
+    const size_t smem = coarse_smem_bytes(ncubes, D, false);
     dim3 grid((ncubes + a.R - 1) / a.R, heads, B);
     auto pick = [&](auto d) {
         constexpr int DD = decltype(d)::value;

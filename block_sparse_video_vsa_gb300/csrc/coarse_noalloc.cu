@@ -69,18 +69,21 @@ extern "C" vsa_status vsa_coarse_select_noalloc(const void* qt, const void* kt, 
     if (!(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return VSA_ERR_UNSUPPORTED;
     if (ncubes > 4096) return VSA_ERR_UNSUPPORTED;
-    // The problem must fit the fixed scratch array.
-    if (coarse_workspace_bytes(B, heads, ncubes, D) > kScratchBytes) return VSA_ERR_UNSUPPORTED;
+    // The problem must fit the fixed scratch array: scores through memory when
+    // that path is the default and its score matrix fits, else the fused path.
+    bool split = coarse_split_default(ncubes, D);
+    if (split && coarse_workspace_bytes(B, heads, ncubes, D, true) > kScratchBytes) split = false;
+    if (coarse_workspace_bytes(B, heads, ncubes, D, split) > kScratchBytes) return VSA_ERR_UNSUPPORTED;
     if (!aligned16(qt) || !aligned16(kt) || !aligned16(vbs) || (reinterpret_cast<uintptr_t>(topk_idx) & 3u))
         return VSA_ERR_ALIGNMENT;
     DevCtx ctx;
     if (get_dev_ctx(&ctx) != cudaSuccess) return VSA_ERR_CUDA;
-    if (coarse_smem_bytes(coarse_rows_per_block(ncubes, D), ncubes, D) > (size_t)ctx.max_smem_optin)
+    if (coarse_smem_bytes(ncubes, D, split) > (size_t)ctx.max_smem_optin)
         return VSA_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return VSA_ERR_CUDA;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
-    return launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, scratch, topk_idx,
+    return launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, scratch, topk_idx, split,
                          static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? VSA_OK
                : VSA_ERR_CUDA;

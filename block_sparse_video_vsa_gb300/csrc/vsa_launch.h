@@ -16,12 +16,13 @@ cudaError_t launch_tile(const vsa_grid& g, int ncubes, const void* x, void* xt, 
 cudaError_t launch_untile(const vsa_grid& g, int ncubes, const void* yt, void* y, cudaStream_t stream);
 
 // coarse.cu
-size_t coarse_workspace_bytes(int B, int heads, int ncubes, int D);
-size_t coarse_smem_bytes(int R, int N, int D);
+bool coarse_split_default(int ncubes, int D);
+size_t coarse_workspace_bytes(int B, int heads, int ncubes, int D, bool split);
+size_t coarse_smem_bytes(int N, int D, bool split);
 int coarse_rows_per_block(int ncubes, int D);
 cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes, int heads,
                           int D, int topk, float sm_scale, void* workspace, int32_t* topk_idx,
-                          cudaStream_t stream);
+                          bool split, cudaStream_t stream);
 cudaError_t launch_validate(const int32_t* idx, const int32_t* vbs, int rows, int ncubes, int topk,
                             int32_t* flag, cudaStream_t stream);
 int validate_max_cubes();

@@ -111,9 +111,9 @@ vsa_status vsa_untile(const vsa_grid* g, const void* yt, void* y, vsa_stream_t s
  * Bytes of device workspace vsa_coarse_select needs: 16 * B * heads * ncubes
  * * D + 8 * B * heads * ncubes (per cube and head: the fp32 mean of Q and K,
  * an fp32 residual that makes the channel sums exact to ~2^-48, and the norm
- * of each mean), plus 4 * B * heads * ncubes^2 for the fp32 score matrix when
- * ncubes is large (from 835 at D = 128, from 1219 at D = 64: the scores
- * then go through memory instead of shared memory).  0 for bad sizes.
+ * of each mean), plus 4 * B * heads * ncubes^2 for the fp32 score matrix
+ * when ncubes >= 256 (the scores then go through memory: a score GEMM, then
+ * a per-row selection).  0 for bad sizes.
  */
 size_t vsa_coarse_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t D);
 

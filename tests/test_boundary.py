@@ -62,14 +62,12 @@ def test_num_cubes(lib):
 
 
 def test_workspace_bytes(lib):
-    assert lib.vsa_coarse_workspace_bytes(1, 40, 624, 128) == 16 * 40 * 624 * 128 + 8 * 40 * 624
+    # from 256 cubes the fp32 score matrix goes through the workspace
+    assert lib.vsa_coarse_workspace_bytes(1, 40, 624, 128) == 16 * 40 * 624 * 128 + 8 * 40 * 624 + 4 * 40 * 624 * 624
+    assert lib.vsa_coarse_workspace_bytes(1, 2, 255, 128) == 16 * 2 * 255 * 128 + 8 * 2 * 255
     assert lib.vsa_coarse_workspace_bytes(0, 40, 624, 128) == 0
-    # large N: the fp32 score matrix goes through the workspace
     assert lib.vsa_coarse_workspace_bytes(1, 24, 1920, 128) == (16 * 24 * 1920 * 128 + 8 * 24 * 1920
                                                                + 4 * 24 * 1920 * 1920)
-    assert lib.vsa_coarse_workspace_bytes(1, 2, 834, 128) == 16 * 2 * 834 * 128 + 8 * 2 * 834
-    assert lib.vsa_coarse_workspace_bytes(1, 2, 835, 128) == 16 * 2 * 835 * 128 + 8 * 2 * 835 + 4 * 2 * 835 * 835
-    assert lib.vsa_coarse_workspace_bytes(1, 2, 1218, 64) == 16 * 2 * 1218 * 64 + 8 * 2 * 1218
 
 
 A = 0x10000   # fake, never dereferenced: every call below fails validation first

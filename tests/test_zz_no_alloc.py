@@ -60,3 +60,25 @@ def test_noalloc_refuses_problems_beyond_the_scratch():
     A = 0x10000  # never dereferenced: the size check fails first
     # 16 * 1 * 40 * 4096 * 128 bytes = 320 MiB > 64 MiB
     assert f(A, A, A, 1, 4096, 40, 128, 8, 0.0, A, None) == 2  # VSA_ERR_UNSUPPORTED
+
+
+def test_noalloc_falls_back_to_the_fused_kernel_when_the_scores_do_not_fit():
+    # 300 cubes, 80 heads, D = 128: with the score matrix the scratch would need
+    # 78 MB (> 64 MiB), without it 49 MB.  The allocation-free call then takes
+    # the fused kernel; both paths select the exact top-k, so the indices match
+    # those of the workspace version (which keeps the scores in memory).
+    f = noalloc_fn()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    B, N, H, D, k = 1, 300, 80, 128, 37
+    g = torch.Generator(device="cuda").manual_seed(5)
+    qt = torch.randn((B, 64 * N, H, D), generator=g, device="cuda").to(torch.bfloat16)
+    kt = torch.randn((B, 64 * N, H, D), generator=g, device="cuda").to(torch.bfloat16)
+    vbs = torch.full((N,), 64, dtype=torch.int32, device="cuda")
+    vbs[::7] = 16
+    assert vsa.coarse_workspace_bytes(B, H, N, D) > (64 << 20)
+    ref = vsa.coarse_select(qt, kt, vbs, k)
+    got = torch.full((B, H, N, k), -7, dtype=torch.int32, device="cuda")
+    st = f(qt.data_ptr(), kt.data_ptr(), vbs.data_ptr(), B, N, H, D, k, 0.0, got.data_ptr(), stream)
+    assert st == 0, vsa.library().vsa_status_string(st)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
