@@ -41,7 +41,6 @@ if HERE not in sys.path:
 METRIC = "VSA sparse-attn fwd ms/call and effective TFLOPS; % of GB300 bf16 TC peak"
 UNIT = "TFLOPS (effective)"
 WORKLOAD = "wan"
-KERNELS_PER_STEP = 12  # tile x3, pool sums, score/top-k, pairing x5, sparse attention, untile
 
 # DRAM traffic of one fine_fwd_kernel launch, from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum) of the Wan grid with 8 heads, scaled by 40/8 (traffic grows with
@@ -49,9 +48,9 @@ KERNELS_PER_STEP = 12  # tile x3, pool sums, score/top-k, pairing x5, sparse att
 # was taken from: if fine.cu no longer hashes to `source_sha256`, the traffic is reported
 # as null.
 FINE_TRAFFIC = {
-    "bytes_per_launch": (247.347712e6 + 66.999296e6) * 40 / 8,
+    "bytes_per_launch": (247.396352e6 + 68.179968e6) * 40 / 8,
     "capture": "profiles/fine_fwd_kernel_wan.md",
-    "source_sha256": "2d161dcaefb420642c5d2b5fc58f21b2ddc61df07bf9facf23367fefe18207a5",
+    "source_sha256": "6bf06424f116fc03ea9d0942cad0ae4ad2f6b4a87797b30e1333852fe843707e",
 }
 
 
@@ -320,10 +319,12 @@ def run_ours(args, wl, inputs, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize()
         t0 = time.monotonic()
+        n0 = vsa.kernel_launches()
         start.record(stream)
         for s in range(args.steps):
             step(marks[s])
         end.record(stream)
+        launches = vsa.kernel_launches() - n0  # every kernel the library enqueued in the timed region
         torch.cuda.synchronize()
         clk.window = (t0, time.monotonic())
     if dist:
@@ -341,7 +342,7 @@ def run_ours(args, wl, inputs, rank, world, dist):
         raise RuntimeError("device error word set during the timed run")
 
     if args.no_e2e:
-        return ms_step, stage, clk.summary(), None, 0, 0
+        return ms_step, stage, clk.summary(), None, 0, 0, launches
     # ---- end to end through host buffers (pinned), copies inside the timed region.
     # Every step copies its q, k, v from pinned host memory and reads its output
     # back; the copies run on their own streams, double-buffered, so the upload of
@@ -402,7 +403,7 @@ def run_ours(args, wl, inputs, rank, world, dist):
         e2e_ms = float(t.item())
     h2d = 3 * qh.numel() * 2
     d2h = ohs[0].numel() * 2
-    return ms_step, stage, clk.summary(), e2e_ms, h2d, d2h
+    return ms_step, stage, clk.summary(), e2e_ms, h2d, d2h, launches
 
 
 def main():
@@ -454,7 +455,7 @@ def main():
         dist.barrier()
 
     inputs = synth.make_inputs(wl)
-    ms_step, stage, clocks, e2e_ms, h2d, d2h = run_ours(args, wl, inputs, rank, world, dist)
+    ms_step, stage, clocks, e2e_ms, h2d, d2h, launches = run_ours(args, wl, inputs, rank, world, dist)
 
     burst, sustained, hbm, peak_kind = load_peaks()
     flops = wl.fine_flops()
@@ -481,7 +482,7 @@ def main():
         "e2e": None if e2e_ms is None else {
             "value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -63,6 +63,9 @@ def _declare(lib):
     lib.vsa_sparse_attn_fwd.restype = ctypes.c_int
     lib.vsa_sparse_attn_fwd.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_float,
                                         _p, _p, _p]
+    lib.vsa_sparse_attn_fwd_ex.restype = ctypes.c_int
+    lib.vsa_sparse_attn_fwd_ex.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32,
+                                           ctypes.c_float, _p, _p, _p]
     lib.vsa_sparse_attn_fwd_paired.restype = ctypes.c_int
     lib.vsa_sparse_attn_fwd_paired.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32,
                                                ctypes.c_float, _p, _p, _p]
@@ -76,6 +79,8 @@ def _declare(lib):
     lib.vsa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), _i32]
     lib.vsa_debug_wait_timeout.restype = ctypes.c_int
     lib.vsa_debug_wait_timeout.argtypes = [ctypes.c_int64, _p, _p]
+    lib.vsa_kernel_launches.restype = ctypes.c_uint64
+    lib.vsa_kernel_launches.argtypes = []
     return lib
 
 
@@ -226,11 +231,12 @@ def pair_cubes(topk_idx, workspace=None, out=None, stream=None):
 
 
 def sparse_attn_fwd(qt, kt, vt, topk_idx, vbs, sm_scale: float = 0.0, out=None, lse=None,
-                    want_lse: bool = True, pairs=None, stream=None):
+                    want_lse: bool = True, pairs=None, counts=None, stream=None):
     """Block-sparse attention -> (out bf16 [B, 64*N, heads, D], lse fp32 [B, heads, 64*N] or None).
 
     `pairs` (from pair_cubes) sets which query cubes share a tile; None pairs
-    cubes (2u, 2u + 1).  The results do not depend on it beyond rounding."""
+    cubes (2u, 2u + 1).  The results do not depend on it beyond rounding.
+    `counts` (int32 [B, heads, N]) limits row i to its first counts[i] entries."""
     torch = _torch()
     for t, n in ((qt, "qt"), (kt, "kt"), (vt, "vt")):
         _need(t, torch.bfloat16, n)
@@ -254,10 +260,15 @@ def sparse_attn_fwd(qt, kt, vt, topk_idx, vbs, sm_scale: float = 0.0, out=None, 
         _need(pairs, torch.int32, "pairs")
         if tuple(pairs.shape) != (B, heads, (N + 1) // 2):
             raise ValueError("pairs must be [B, heads, (N + 1) // 2]")
-    _check(library().vsa_sparse_attn_fwd_paired(qt.data_ptr(), kt.data_ptr(), vt.data_ptr(), topk_idx.data_ptr(),
-                                                vbs.data_ptr(), pairs.data_ptr() if pairs is not None else None,
-                                                B, N, heads, D, topk, float(sm_scale), out.data_ptr(),
-                                                lse.data_ptr() if lse is not None else None, _stream(stream)),
+    if counts is not None:
+        _need(counts, torch.int32, "counts")
+        if tuple(counts.shape) != (B, heads, N):
+            raise ValueError("counts must be [B, heads, N]")
+    _check(library().vsa_sparse_attn_fwd_ex(qt.data_ptr(), kt.data_ptr(), vt.data_ptr(), topk_idx.data_ptr(),
+                                            counts.data_ptr() if counts is not None else None, vbs.data_ptr(),
+                                            pairs.data_ptr() if pairs is not None else None,
+                                            B, N, heads, D, topk, float(sm_scale), out.data_ptr(),
+                                            lse.data_ptr() if lse is not None else None, _stream(stream)),
            "vsa_sparse_attn_fwd")
     return out, lse
 
@@ -272,6 +283,11 @@ def validate_indices(topk_idx, vbs, stream=None) -> int:
     _check(library().vsa_validate_indices(topk_idx.data_ptr(), vbs.data_ptr(), B, heads, N, topk,
                                           flag.data_ptr(), _stream(stream)), "vsa_validate_indices")
     return int(flag.item())
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process so far (host counter)."""
+    return int(library().vsa_kernel_launches())
 
 
 def device_error(reset: bool = False) -> int:

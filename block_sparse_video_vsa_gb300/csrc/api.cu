@@ -4,6 +4,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "vsa_common.cuh"
@@ -15,10 +16,13 @@ __device__ unsigned int g_device_error;
 
 namespace {
 constexpr int kMaxDevices = 64;
+std::atomic<uint64_t> g_launches{0};
 std::mutex g_ctx_mu;
 DevCtx g_ctx[kMaxDevices];
 bool g_ctx_ok[kMaxDevices];
 }  // namespace
+
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 cudaError_t get_dev_ctx(DevCtx* out) {
     int dev = 0;
@@ -137,10 +141,10 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
                                    static_cast<cudaStream_t>(stream)));
 }
 
-vsa_status vsa_sparse_attn_fwd_paired(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
-                                      const int32_t* vbs, const uint32_t* pairs, int32_t B, int32_t ncubes,
-                                      int32_t heads, int32_t D, int32_t topk, float sm_scale, void* out, float* lse,
-                                      vsa_stream_t stream) {
+vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                                  const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int32_t B,
+                                  int32_t ncubes, int32_t heads, int32_t D, int32_t topk, float sm_scale,
+                                  void* out, float* lse, vsa_stream_t stream) {
     if (!qt || !kt || !vt || !topk_idx || !vbs || !out) return VSA_ERR_INVALID_ARG;
     if (B <= 0 || ncubes <= 0 || heads <= 0 || topk <= 0 || topk > ncubes) return VSA_ERR_INVALID_ARG;
     if (!(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
@@ -152,22 +156,31 @@ vsa_status vsa_sparse_attn_fwd_paired(const void* qt, const void* kt, const void
     if (topk > fine_max_topk() || ncubes > fine_max_cubes()) return VSA_ERR_UNSUPPORTED;
     if (!aligned16(qt) || !aligned16(kt) || !aligned16(vt) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(vbs) & 3u) ||
-        (reinterpret_cast<uintptr_t>(pairs) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        (reinterpret_cast<uintptr_t>(pairs) & 3u) || (reinterpret_cast<uintptr_t>(counts) & 3u) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return VSA_ERR_ALIGNMENT;
     DevCtx ctx;
     cudaError_t e = get_dev_ctx(&ctx);
     if (e != cudaSuccess) return VSA_ERR_CUDA;
     if (fine_smem_bytes() > ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
-    return from_cuda(launch_fine(qt, kt, vt, topk_idx, vbs, pairs, B, ncubes, heads, D, topk, sm_scale, out,
-                                 lse, ctx.err, ctx.num_sms, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_fine(qt, kt, vt, topk_idx, counts, vbs, pairs, B, ncubes, heads, D, topk, sm_scale,
+                                 out, lse, ctx.err, ctx.num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status vsa_sparse_attn_fwd_paired(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                                      const int32_t* vbs, const uint32_t* pairs, int32_t B, int32_t ncubes,
+                                      int32_t heads, int32_t D, int32_t topk, float sm_scale, void* out, float* lse,
+                                      vsa_stream_t stream) {
+    return vsa_sparse_attn_fwd_ex(qt, kt, vt, topk_idx, nullptr, vbs, pairs, B, ncubes, heads, D, topk, sm_scale,
+                                  out, lse, stream);
 }
 
 vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                                const int32_t* vbs, int32_t B, int32_t ncubes, int32_t heads, int32_t D,
                                int32_t topk, float sm_scale, void* out, float* lse, vsa_stream_t stream) {
-    return vsa_sparse_attn_fwd_paired(qt, kt, vt, topk_idx, vbs, nullptr, B, ncubes, heads, D, topk, sm_scale,
-                                      out, lse, stream);
+    return vsa_sparse_attn_fwd_ex(qt, kt, vt, topk_idx, nullptr, vbs, nullptr, B, ncubes, heads, D, topk,
+                                  sm_scale, out, lse, stream);
 }
 
 size_t vsa_pair_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t topk) {
@@ -224,5 +237,7 @@ vsa_status vsa_debug_wait_timeout(int64_t limit_ns, int32_t* dev_result, vsa_str
     if (get_dev_ctx(&ctx) != cudaSuccess) return VSA_ERR_CUDA;
     return from_cuda(launch_debug_wait((long long)limit_ns, dev_result, ctx.err, static_cast<cudaStream_t>(stream)));
 }
+
+uint64_t vsa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -669,6 +669,7 @@ cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, in
     dim3 pg(B * ncubes, 2);
     pool_kernel<<<pg, row_vecs < 256 ? ((row_vecs + 31) / 32) * 32 : 256, 0, stream>>>(
         static_cast<const uint4*>(qt), static_cast<const uint4*>(kt), vbs, po, B, ncubes, heads, D);
+    note_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -698,6 +699,7 @@ cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, in
         gemm<<<gg, 256, gsmem, stream>>>(a, scores);
         auto sel = D == 128 ? select_kernel<128> : select_kernel<64>;
         sel<<<dim3((ncubes + 7) / 8, B * heads), 256, 0, stream>>>(a, scores);
+        note_launches(2);
         return cudaGetLastError();
     }
     const size_t smem = coarse_smem_bytes(ncubes, D, false);
@@ -711,6 +713,7 @@ cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, in
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kernel<<<grid, score_warps(a.R) * 32, smem, stream>>>(a);
+    note_launches(1);
     return cudaGetLastError();
 }
 
@@ -725,6 +728,7 @@ cudaError_t launch_validate(const int32_t* idx, const int32_t* vbs, int rows, in
                                          (int)smem);
     if (e != cudaSuccess) return e;
     validate_kernel<<<blocks, kValWarps * 32, smem, stream>>>(idx, vbs, rows, ncubes, topk, flag);
+    note_launches(1);
     return cudaGetLastError();
 }
 
@@ -733,6 +737,7 @@ int validate_max_cubes() { return kValMaxCubes; }
 cudaError_t launch_debug_wait(long long limit_ns, int32_t* result, unsigned int* err,
                               cudaStream_t stream) {
     debug_wait_kernel<<<1, 32, 0, stream>>>(limit_ns, result, err);
+    note_launches(1);
     return cudaGetLastError();
 }
 

@@ -113,6 +113,7 @@ struct FineParams {
     const int32_t* topk_idx;
     const int32_t* vbs;
     const uint32_t* pairs;  // [B * heads][npairs]: i | (j << 16), j = 0xFFFF single; or null: (2u, 2u + 1)
+    const int32_t* counts;  // [B * heads * N] entries of each topk_idx row in use (<= topk), or null: all
     const uint4* q;      // tiled q rows (for staging Q into TMEM)
     __nv_bfloat16* out;
     float* lse;
@@ -158,16 +159,19 @@ __device__ int build_union(const FineParams& p, int u, uint32_t* list, uint32_t*
     }
     __syncwarp();
     const int32_t* rows = p.topk_idx + ((size_t)b * p.heads + h) * N * (size_t)k;
+    const int32_t* cnt = p.counts ? p.counts + ((size_t)b * p.heads + h) * N : nullptr;
     if (i0 >= 0) {
         const int32_t* r0 = rows + (size_t)i0 * k;
-        for (int e = lane; e < k; e += 32) {
+        const int k0 = cnt ? min(max(__ldg(cnt + i0), 0), k) : k;
+        for (int e = lane; e < k0; e += 32) {
             const int j = __ldg(r0 + e);
             atomicOr(&bm0[j >> 5], 1u << (j & 31));
         }
     }
     if (i1 >= 0) {
         const int32_t* r1 = rows + (size_t)i1 * k;
-        for (int e = lane; e < k; e += 32) {
+        const int k1 = cnt ? min(max(__ldg(cnt + i1), 0), k) : k;
+        for (int e = lane; e < k1; e += 32) {
             const int j = __ldg(r1 + e);
             atomicOr(&bm1[j >> 5], 1u << (j & 31));
         }
@@ -520,6 +524,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t* list = lists + lb * kMaxUnion;
             const int count = ok ? ms.list_count[lb] : 0;
             const int nst = (count + 1) >> 1;
+            // Stages the next unit's Q once this unit's Q is no longer read (its
+            // last QK has completed: after S of its last step, or at once for a
+            // unit with an empty union, which issues no QK).
+            auto stage_next_q = [&]() {
+                if (ul + 1 < my_units && ok) {
+                    ok = mbar_wait_bounded(smem_u32(&ms.q_empty), ul & 1, abort_flag, p.err, kWaitLimitNs);
+                    if (ok) {
+                        tc_fence_after();
+                        stage_q(p, u + gridDim.x, r, t_lane, hf);
+                        tc_fence_before();
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ms.q_full));
+                }
+            };
+            if (nst == 0) stage_next_q();
             float m = ninf, l = 0.f;
             for (int t = 0; t < nst; ++t, ++g) {
                 const int e = 2 * t + hf;
@@ -530,18 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) ok = mbar_wait_bounded(smem_u32(&ms.s_full[g & 1]), (g >> 1) & 1, abort_flag, p.err,
                                                kWaitLimitNs);
                 tc_fence_after();
-                if (t + 1 == nst && ul + 1 < my_units && ok) {
-                    // Last step of the unit: its Q is no longer read (the unit's last
-                    // QK has completed with S(g)), so stage the next unit's Q now.
-                    ok = mbar_wait_bounded(smem_u32(&ms.q_empty), ul & 1, abort_flag, p.err, kWaitLimitNs);
-                    if (ok) {
-                        tc_fence_after();
-                        stage_q(p, u + gridDim.x, r, t_lane, hf);
-                        tc_fence_before();
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ms.q_full));
-                }
+                if (t + 1 == nst) stage_next_q();
                 float x[64];
                 if (ok && mem) {
                     tmem_ld32(t_lane + sc + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
@@ -583,16 +592,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t pk[32];
                 if (ok && mem) {
                     const float mb = (m == ninf) ? 0.f : m;
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                    // Packed two-wide fp32 FMA and add (the same roundings as the
+                    // scalar forms, half the instructions).
+                    const float2 c2v = make_float2(c2, c2), nmb = make_float2(-mb, -mb);
+                    float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int c = 0; c < 64; c += 4) {
-                        const float p0 = ex2_approx(fmaf(x[c], c2, -mb)), p1 = ex2_approx(fmaf(x[c + 1], c2, -mb));
-                        const float p2 = ex2_approx(fmaf(x[c + 2], c2, -mb)), p3 = ex2_approx(fmaf(x[c + 3], c2, -mb));
-                        s0 += p0; s1 += p1; s2 += p2; s3 += p3;
+                        const float2 a01 = __ffma2_rn(make_float2(x[c], x[c + 1]), c2v, nmb);
+                        const float2 a23 = __ffma2_rn(make_float2(x[c + 2], x[c + 3]), c2v, nmb);
+                        const float p0 = ex2_approx(a01.x), p1 = ex2_approx(a01.y);
+                        const float p2 = ex2_approx(a23.x), p3 = ex2_approx(a23.y);
+                        s01 = __fadd2_rn(s01, make_float2(p0, p1));
+                        s23 = __fadd2_rn(s23, make_float2(p2, p3));
                         pk[c >> 1] = pack_bf16x2(p0, p1);
                         pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
                     }
-                    l += (s0 + s1) + (s2 + s3);
+                    l += (s01.x + s01.y) + (s23.x + s23.y);
                 } else {
 #pragma unroll
                     for (int c = 0; c < 32; ++c) pk[c] = 0u;
@@ -630,7 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(1 + quarter, 64);
             const float lt = l + ms.xsum[hf ^ 1][r];
             const uint32_t gl = g - 1;  // last step of the unit
-            if (ok) ok = mbar_wait_bounded(smem_u32(&ms.pv_done), gl & 1, abort_flag, p.err, kWaitLimitNs);
+            // An empty union issued no PV: O holds nothing of this unit, write zeros.
+            if (ok && nst > 0) ok = mbar_wait_bounded(smem_u32(&ms.pv_done), gl & 1, abort_flag, p.err, kWaitLimitNs);
             if (ok) {
                 tc_fence_after();
                 const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
@@ -638,8 +654,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint4* dst = reinterpret_cast<uint4*>(p.out) + (row * p.heads + h) * (size_t)(D / 8);
                 for (int c0 = hf * dh; c0 < hf * dh + dh; c0 += 32) {
                     uint32_t o[32];
-                    tmem_ld32(t_lane + kTmemO + c0, o);
-                    tmem_wait_ld();
+                    if (nst > 0) {
+                        tmem_ld32(t_lane + kTmemO + c0, o);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) o[q] = 0u;
+                    }
                     if (i >= 0) {
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
@@ -708,9 +729,9 @@ int fine_max_topk() { return kMaxTopk; }
 int fine_max_cubes() { return kMaxCubes; }
 
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
-                        const int32_t* vbs, const uint32_t* pairs, int B, int ncubes, int heads, int D, int topk,
-                        float sm_scale, void* out, float* lse, unsigned int* err, int num_sms,
-                        cudaStream_t stream) {
+                        const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int B, int ncubes,
+                        int heads, int D, int topk, float sm_scale, void* out, float* lse, unsigned int* err,
+                        int num_sms, cudaStream_t stream) {
     CUtensorMap mk, mv;
     const int rows = B * ncubes * kCubeTokens;
     if (!make_map(&mk, kt, rows, heads, D, true) || !make_map(&mv, vt, rows, heads, D, true))
@@ -719,6 +740,7 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     p.topk_idx = topk_idx;
     p.vbs = vbs;
     p.pairs = pairs;
+    p.counts = counts;
     p.q = static_cast<const uint4*>(qt);
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;
@@ -736,6 +758,7 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     if (e != cudaSuccess) return e;
     const int grid = p.num_units < num_sms ? p.num_units : num_sms;
     kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, p);
+    note_launches(1);
     return cudaGetLastError();
 }
 

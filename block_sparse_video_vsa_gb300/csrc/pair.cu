@@ -438,6 +438,7 @@ cudaError_t launch_pair(const int32_t* topk_idx, int B, int ncubes, int heads, i
     // 1. bitmaps
     const size_t rows = bh * N;
     pair_bitmap_kernel<<<(unsigned)((rows + kPairWarps - 1) / kPairWarps), kPairThreads, 0, stream>>>(a, rows);
+    note_launches(1);
 
     // 2. candidate lists: first the staged row stride cs (an odd number of
     // quads, at most ~60% of the budget, at most the padded row), then rows
@@ -462,6 +463,7 @@ cudaError_t launch_pair(const int32_t* topk_idx, int B, int ncubes, int heads, i
     e = cudaFuncSetAttribute(cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_c);
     if (e != cudaSuccess) return e;
     cand_kernel<<<dim3((unsigned)chunks, (unsigned)bh), kPairThreads, dyn_c, stream>>>(a, rb, cw, cs);
+    note_launches(1);
 
     // 3. rounds (b)
     const size_t arrays = 3 * (size_t)N * sizeof(int16_t);
@@ -471,6 +473,7 @@ cudaError_t launch_pair(const int32_t* topk_idx, int B, int ncubes, int heads, i
     e = cudaFuncSetAttribute(pair_match1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_1);
     if (e != cudaSuccess) return e;
     pair_match1_kernel<<<(unsigned)bh, kPairThreads, dyn_1, stream>>>(a, stage_lists);
+    note_launches(1);
 
     // 4. window overlaps
     const size_t dyn_w = (size_t)(kWinChunk + kWin) * a.Wp * sizeof(uint32_t);
@@ -478,6 +481,7 @@ cudaError_t launch_pair(const int32_t* topk_idx, int B, int ncubes, int heads, i
     e = cudaFuncSetAttribute(pair_window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_w);
     if (e != cudaSuccess) return e;
     pair_window_kernel<<<dim3(kMaxLeft / kWinChunk, (unsigned)bh), kPairThreads, dyn_w, stream>>>(a);
+    note_launches(1);
 
     // 5. rounds (c), (d), units
     const size_t dyn_2 = (size_t)kMaxLeft * kWin * sizeof(uint16_t) + 2 * (size_t)N * sizeof(int16_t);
@@ -485,6 +489,7 @@ cudaError_t launch_pair(const int32_t* topk_idx, int B, int ncubes, int heads, i
     e = cudaFuncSetAttribute(pair_match2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_2);
     if (e != cudaSuccess) return e;
     pair_match2_kernel<<<(unsigned)bh, kPairThreads, dyn_2, stream>>>(a);
+    note_launches(1);
     return cudaGetLastError();
 }
 

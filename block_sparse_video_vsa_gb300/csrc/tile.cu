@@ -137,6 +137,7 @@ cudaError_t launch_tile(const vsa_grid& g, int ncubes, const void* x, void* xt, 
     tile_kernel<<<g.B * ncubes, kThreads, 0, stream>>>(static_cast<const int4*>(x),
                                                       static_cast<int4*>(xt), vbs, make_geom(g),
                                                       ncubes, row_vecs, tokens);
+    note_launches(1);
     return cudaGetLastError();
 }
 
@@ -147,6 +148,7 @@ cudaError_t launch_untile(const vsa_grid& g, int ncubes, const void* yt, void* y
     untile_kernel<<<g.B * ncubes, kThreads, 0, stream>>>(static_cast<const int4*>(yt),
                                                         static_cast<int4*>(y), make_geom(g),
                                                         ncubes, row_vecs, tokens);
+    note_launches(1);
     return cudaGetLastError();
 }
 

@@ -10,6 +10,9 @@
 
 namespace vsa {
 
+// api.cu: counts kernel launches (n kernels enqueued by the caller).
+void note_launches(int n);
+
 // tile.cu
 cudaError_t launch_tile(const vsa_grid& g, int ncubes, const void* x, void* xt, int32_t* vbs,
                         cudaStream_t stream);
@@ -33,9 +36,9 @@ int fine_smem_bytes();
 int fine_max_topk();
 int fine_max_cubes();
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
-                        const int32_t* vbs, const uint32_t* pairs, int B, int ncubes, int heads, int D, int topk,
-                        float sm_scale, void* out, float* lse, unsigned int* err, int num_sms,
-                        cudaStream_t stream);
+                        const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int B, int ncubes,
+                        int heads, int D, int topk, float sm_scale, void* out, float* lse, unsigned int* err,
+                        int num_sms, cudaStream_t stream);
 
 // pair.cu
 int pair_words(int ncubes);

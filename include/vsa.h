@@ -229,6 +229,24 @@ vsa_status vsa_sparse_attn_fwd_paired(const void* qt, const void* kt, const void
                                       void* out, float* lse, vsa_stream_t stream);
 
 /*
+ * The fine stage with a variable number of selected cubes per query cube
+ * ([VSA-AMD] Block-Sparse Encoding: a per-row count of valid blocks beside the
+ * block-index table).  Row (b, head, i) attends the cubes
+ * topk_idx[b, head, i, 0 .. counts[b, head, i] - 1] only; entries past the
+ * count are not read (fill them with -1 so that vsa_pair_cubes, which reads
+ * whole rows, ignores them).  A count of 0 gives out = 0 and lse = -inf.
+ *   counts : int32 [B, heads, ncubes], values clamped to [0, topk], or NULL
+ *            for topk everywhere
+ *   pairs  : as for vsa_sparse_attn_fwd_paired, or NULL
+ * Same arguments, limits and errors as vsa_sparse_attn_fwd otherwise.
+ */
+vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt,
+                                  const int32_t* topk_idx, const int32_t* counts,
+                                  const int32_t* vbs, const uint32_t* pairs, int32_t B,
+                                  int32_t ncubes, int32_t heads, int32_t D, int32_t topk,
+                                  float sm_scale, void* out, float* lse, vsa_stream_t stream);
+
+/*
  * Debug aid for the block-sparse encoding ([VSA-AMD] Block-Sparse Encoding):
  * checks every topk_idx entry is in [0, ncubes), that no row repeats an
  * index, and that every vbs entry is in [0, 64].  ORs into *dev_flag (device
@@ -257,6 +275,14 @@ vsa_status vsa_device_error(uint32_t* out, int32_t reset);
  * *dev_result (device int32), else 0.  The kernel then returns normally.
  */
 vsa_status vsa_debug_wait_timeout(int64_t limit_ns, int32_t* dev_result, vsa_stream_t stream);
+
+/*
+ * Number of kernels this library has launched in this process so far, over
+ * every entry point, device and stream (a host-side counter, incremented when
+ * a launch is enqueued; thread safe; never reset).  The difference of two
+ * reads is the number of kernels launched between them.
+ */
+uint64_t vsa_kernel_launches(void);
 
 #ifdef __cplusplus
 }

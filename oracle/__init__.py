@@ -202,5 +202,44 @@ def fine_full(qt, kt, vt, topk_idx, vbs, sm_scale: float, nthreads: int = 0):
     return out, lse
 
 
+def fine_counts(qt, kt, vt, topk_idx, counts, vbs, sm_scale: float, units=None, nthreads: int = 0):
+    """Fine stage with a per-row count of valid entries ([VSA-AMD] Block-Sparse
+    Encoding: a per-row number of valid blocks beside the block-index table):
+    query cube i attends the cubes topk_idx[b, h, i, :counts[b, h, i]] only.
+
+    Computed by the fixed-length routine on an equivalent problem: one extra
+    cube with no real token (vbs = 0) is appended and every unused entry
+    points to it, so it adds no key.  Same returns as fine(); units index the
+    original N cubes.
+    """
+    qt, kt, vt = _u16(qt), _u16(kt), _u16(vt)
+    topk_idx, vbs = _i32(topk_idx), _i32(vbs)
+    B, S, heads, D = qt.shape
+    N = S // 64
+    k = topk_idx.shape[-1]
+    c = np.clip(np.asarray(counts, np.int64), 0, k)
+    assert c.shape == (B, heads, N)
+    pad = np.zeros((B, 64, heads, D), np.uint16)
+    qt2, kt2, vt2 = (np.ascontiguousarray(np.concatenate([x, pad], axis=1)) for x in (qt, kt, vt))
+    vbs2 = np.concatenate([vbs, np.zeros(1, np.int32)])
+    idx2 = np.full((B, heads, N + 1, k), N, np.int32)
+    idx2[:, :, :N] = np.where(np.arange(k)[None, None, None, :] < c[..., None], topk_idx, N)
+    if units is None:
+        units = np.arange(B * heads * N, dtype=np.int64)
+    units = np.asarray(units, dtype=np.int64)
+    units2 = (units // N) * (N + 1) + units % N
+    return fine(qt2, kt2, vt2, idx2, vbs2, sm_scale, units2, nthreads)
+
+
+def fine_full_counts(qt, kt, vt, topk_idx, counts, vbs, sm_scale: float, nthreads: int = 0):
+    """fine_counts over every query cube, in the tiled token layout (as fine_full)."""
+    B, S, heads, D = _u16(qt).shape
+    N = S // 64
+    out_u, lse_u, _ = fine_counts(qt, kt, vt, topk_idx, counts, vbs, sm_scale, None, nthreads)
+    out = out_u.reshape(B, heads, N * 64, D).transpose(0, 2, 1, 3).copy()
+    lse = lse_u.reshape(B, heads, N * 64).copy()
+    return out, lse
+
+
 def default_threads() -> int:
     return int(lib().oracle_default_threads())

@@ -67,7 +67,8 @@ def assert_lse_close(got, ref):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     both_inf = np.isneginf(got) & np.isneginf(ref)
-    d = np.where(both_inf, 0.0, np.abs(got - ref))
+    with np.errstate(invalid="ignore"):  # -inf - -inf where both rows are empty
+        d = np.where(both_inf, 0.0, np.abs(got - ref))
     bound = LSE_REL * np.maximum(1.0, np.abs(np.where(both_inf, 0.0, ref)))
     bad = ~(d <= bound)
     assert not bad.any(), f"lse mismatch at {np.argwhere(bad)[:5].tolist()}: max {np.nanmax(d):.3e}"

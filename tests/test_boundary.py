@@ -37,7 +37,8 @@ def test_header_declares_the_entry_points():
     for n in ("vsa_tile", "vsa_untile", "vsa_coarse_select", "vsa_sparse_attn_fwd",
               "vsa_coarse_workspace_bytes", "vsa_num_cubes", "vsa_status_string",
               "vsa_validate_indices", "vsa_device_error", "vsa_debug_wait_timeout",
-              "vsa_pair_cubes", "vsa_pair_workspace_bytes", "vsa_sparse_attn_fwd_paired"):
+              "vsa_pair_cubes", "vsa_pair_workspace_bytes", "vsa_sparse_attn_fwd_paired",
+              "vsa_sparse_attn_fwd_ex"):
         assert n in names
 
 
@@ -128,6 +129,23 @@ def test_pairing_validation(lib):
     g = lib.vsa_sparse_attn_fwd_paired
     assert g(A, A, A, A, A, A + 2, 1, 12, 2, 64, 3, 0.0, A, None, None) == ALIGNMENT  # pairs
     assert g(A, A, A, A, A, None, 1, 12, 2, 64, 0, 0.0, A, None, None) == INVALID
+
+
+def test_counts_validation(lib):
+    h = lib.vsa_sparse_attn_fwd_ex
+    #   qt kt vt idx counts vbs pairs  B  N  H  D  k  scale out lse stream
+    assert h(A, A, A, A, A + 2, A, None, 1, 12, 2, 64, 3, 0.0, A, None, None) == ALIGNMENT  # counts
+    assert h(A, A, A, A, A, A, A + 2, 1, 12, 2, 64, 3, 0.0, A, None, None) == ALIGNMENT     # pairs
+    assert h(A, A, A, A, A, A, None, 1, 12, 2, 64, 13, 0.0, A, None, None) == INVALID      # topk > N
+    assert h(A, A, A, A, A, A, None, 1, 12, 2, 256, 3, 0.0, A, None, None) == UNSUPPORTED
+
+
+def test_refused_calls_launch_nothing(lib):
+    lib.vsa_kernel_launches.restype = ctypes.c_uint64
+    n0 = lib.vsa_kernel_launches()
+    assert lib.vsa_pair_cubes(None, 1, 12, 2, 3, A, A, None) == INVALID
+    assert lib.vsa_sparse_attn_fwd(A, A, A, A, A, 1, 12, 2, 64, 0, 0.0, A, None, None) == INVALID
+    assert lib.vsa_kernel_launches() == n0
 
 
 def test_validator_and_debug_validation(lib):

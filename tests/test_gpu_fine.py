@@ -21,10 +21,12 @@ from gpu_util import (assert_lse_close, assert_scoring_rule, i32_dev, score_outp
 pytestmark = pytest.mark.gpu
 
 
-def gpu_fine(qt, kt, vt, idx, vbs, sm, paired=False):
+def gpu_fine(qt, kt, vt, idx, vbs, sm, paired=False, counts=None):
     idx_d = i32_dev(idx)
     pairs = vsa.pair_cubes(idx_d) if paired else None
-    o, lse = vsa.sparse_attn_fwd(to_dev(qt), to_dev(kt), to_dev(vt), idx_d, i32_dev(vbs), sm, pairs=pairs)
+    cnt = None if counts is None else i32_dev(counts)
+    o, lse = vsa.sparse_attn_fwd(to_dev(qt), to_dev(kt), to_dev(vt), idx_d, i32_dev(vbs), sm, pairs=pairs,
+                                 counts=cnt)
     torch.cuda.synchronize()
     assert vsa.device_error(reset=True) == 0
     return to_bits(o), lse.cpu().numpy()
@@ -116,6 +118,58 @@ def test_deterministic():
     assert np.array_equal(a, b) and np.array_equal(la, lb)
 
 
+# ---------------------------------------------- per-row counts (variable length)
+def ragged_counts(idx, seed, fill=-1):
+    """Random counts in [0, topk] (0 and topk always present); entries past a
+    row's count are overwritten by `fill` (-1, or "garbage": random cubes)."""
+    rng = np.random.default_rng(seed)
+    k = idx.shape[-1]
+    counts = rng.integers(0, k + 1, size=idx.shape[:3]).astype(np.int32)
+    counts.reshape(-1)[:4] = [0, k, 1, k]
+    out = idx.copy()
+    N = idx.shape[2]
+    for r in np.ndindex(idx.shape[:3]):
+        tail = k - counts[r]
+        out[r][counts[r]:] = rng.integers(0, N, size=tail) if fill == "garbage" else fill
+    return out, counts
+
+
+@pytest.mark.parametrize("paired", [False, True])
+@pytest.mark.parametrize("topk", [5, 48])
+def test_counts_ragged_rows(paired, topk):
+    wl = synth.WORKLOADS["mid"]
+    _, _, qt, kt, vt, vbs = tiled_inputs(wl)
+    idx, counts = ragged_counts(oracle.coarse(qt, kt, vbs, topk, wl.sm_scale), 5 + topk)
+    got, got_lse = gpu_fine(qt, kt, vt, idx, vbs, wl.sm_scale, paired=paired, counts=counts)
+    ref, ref_lse = oracle.fine_full_counts(qt, kt, vt, idx, counts, vbs, wl.sm_scale)
+    assert_scoring_rule(score_outputs(got, ref))
+    assert_lse_close(got_lse, ref_lse)
+    empty = np.repeat(counts == 0, 64, axis=2)                 # [B, H, S]
+    assert np.isneginf(got_lse[empty]).all() and np.isfinite(got_lse[~empty]).all()
+    assert (synth.bf16_to_f32(got).transpose(0, 2, 1, 3)[empty] == 0).all()
+
+
+def test_counts_ignore_entries_past_the_count():
+    wl = synth.WORKLOADS["mid"]
+    _, _, qt, kt, vt, vbs = tiled_inputs(wl)
+    base = oracle.coarse(qt, kt, vbs, 11, wl.sm_scale)
+    a_idx, counts = ragged_counts(base, 9)
+    b_idx, _ = ragged_counts(base, 9, fill="garbage")
+    a, la = gpu_fine(qt, kt, vt, a_idx, vbs, wl.sm_scale, counts=counts)
+    b, lb = gpu_fine(qt, kt, vt, b_idx, vbs, wl.sm_scale, counts=counts)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+def test_counts_full_equal_the_fixed_length_call():
+    wl = synth.WORKLOADS["mid"]
+    _, _, qt, kt, vt, vbs = tiled_inputs(wl)
+    idx = oracle.coarse(qt, kt, vbs, 13, wl.sm_scale)
+    full = np.full(idx.shape[:3], 13, np.int32)
+    a, la = gpu_fine(qt, kt, vt, idx, vbs, wl.sm_scale)
+    b, lb = gpu_fine(qt, kt, vt, idx, vbs, wl.sm_scale, counts=full)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
 # ------------------------------------------------------------- full size
 _CACHE = {}
 
@@ -139,11 +193,14 @@ def sample_units(wl, n, seed, heads=None):
     return np.unique(hs.astype(np.int64) * N + cubes)
 
 
-def sampled_compare(wl, qt, kt, vt, vbs, idx, units):
+def sampled_compare(wl, qt, kt, vt, vbs, idx, units, counts=None):
     # the launch configuration the benchmark times: pairing, then the paired fine stage
-    got, got_lse = gpu_fine(qt, kt, vt, idx, vbs, wl.sm_scale, paired=True)
+    got, got_lse = gpu_fine(qt, kt, vt, idx, vbs, wl.sm_scale, paired=True, counts=counts)
     assert np.isfinite(synth.bf16_to_f32(got)).all()
-    ref_u, ref_lse_u, _ = oracle.fine(qt, kt, vt, idx, vbs, wl.sm_scale, units)
+    if counts is None:
+        ref_u, ref_lse_u, _ = oracle.fine(qt, kt, vt, idx, vbs, wl.sm_scale, units)
+    else:
+        ref_u, ref_lse_u, _ = oracle.fine_counts(qt, kt, vt, idx, counts, vbs, wl.sm_scale, units)
     N = wl.ncubes
     h = units // N
     i = units % N
@@ -158,7 +215,8 @@ def sampled_compare(wl, qt, kt, vt, vbs, idx, units):
     for hh, us in by_head.items():
         a = synth.bf16_to_f32(got_u[us]).astype(np.float64).ravel()
         b = ref_u[us].astype(np.float32).astype(np.float64).ravel()
-        cos_min = min(cos_min, float(a @ b / max(np.linalg.norm(a) * np.linalg.norm(b), 1e-300)))
+        na, nb = np.linalg.norm(a), np.linalg.norm(b)
+        cos_min = min(cos_min, 1.0 if na == nb == 0 else float(a @ b / max(na * nb, 1e-300)))
     stats = score_outputs(got_u[None].transpose(0, 2, 1, 3), ref_u[None].transpose(0, 2, 1, 3), 2)
     stats["min_head_cos"] = cos_min
     assert_scoring_rule(stats)
@@ -178,6 +236,14 @@ def test_wan_outlier_sweep_sampled(topk):
     idx = oracle.coarse(qt, kt, vbs, topk, wl.sm_scale)
     units = sample_units(wl, 48, 2 + topk, heads=[0, 0, 0, 1, 2, 5])
     sampled_compare(wl, qt, kt, vt, vbs, idx, units)
+
+
+def test_wan_full_size_counts_sampled():
+    wl, qt, kt, vt, vbs, idx = big_case("wan")
+    ridx, counts = ragged_counts(idx, 17)
+    units = sample_units(wl, 64, 4)
+    counts.reshape(-1)[units[:2]] = 0                          # sampled empty rows as well
+    sampled_compare(wl, qt, kt, vt, vbs, ridx, units, counts)
 
 
 def test_hunyuan_full_size_sampled():

@@ -30,3 +30,18 @@ def test_pipeline_matches_oracle(name):
     ref = ref_t[:, slot.astype(np.int64)]
     assert_scoring_rule(score_outputs(to_bits(out), ref))
     assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("grid, expect", [
+    ((1, 9, 16, 16), 12),    # 48 cubes: tile x3, pooled sums, fused score/top-k, pairing x5, fine, untile
+    ((1, 16, 32, 32), 13),   # 256 cubes: the score GEMM and the selection run as two kernels
+])
+def test_launch_counter_counts_every_kernel(grid, expect):
+    wl = synth.Workload("count", *grid, heads=2, D=64, topk=3, seed=5)
+    d = synth.make_inputs(wl)
+    q, k, v = (to_dev(d[n]) for n in "qkv")
+    n0 = vsa.kernel_launches()
+    vsa.pipeline(q, k, v, wl.grid, wl.topk, wl.sm_scale)
+    assert vsa.kernel_launches() - n0 == expect
+    torch.cuda.synchronize()
+    assert vsa.device_error(reset=True) == 0

@@ -70,8 +70,9 @@ def test_dense_equivalence_with_padding():
     assert np.abs(lse[0][:, raster_slot] - ref_lse[0]).max() < 1e-10
 
 
-def brute_force(qt, kt, vt, idx, vbs, scale):
-    """Explicit masked [S_pad x S_pad] softmax per (b, head)."""
+def brute_force(qt, kt, vt, idx, vbs, scale, counts=None):
+    """Explicit masked [S_pad x S_pad] softmax per (b, head); with counts, row
+    cube i attends idx[b, h, i, :counts[b, h, i]] (every count >= 1)."""
     B, S, H, D = qt.shape
     N = S // 64
     q, k, v = f64(qt), f64(kt), f64(vt)
@@ -84,7 +85,8 @@ def brute_force(qt, kt, vt, idx, vbs, scale):
             logits = scale * q[b, :, h] @ k[b, :, h].T
             allowed = np.zeros((S, S), bool)
             for i in range(N):
-                sel = np.isin(key_cube, idx[b, h, i]) & key_ok
+                row = idx[b, h, i] if counts is None else idx[b, h, i, :counts[b, h, i]]
+                sel = np.isin(key_cube, row) & key_ok
                 allowed[64 * i: 64 * (i + 1)] = sel[None]
             masked = np.where(allowed, logits, -np.inf)
             m = masked.max(axis=1, keepdims=True)
@@ -199,3 +201,39 @@ def test_outlier_logits_stay_finite():
     # The head-0 logits really are large enough to overflow exp without a max shift.
     q, k = f64(qt)[0, :, 0], f64(kt)[0, :, 0]
     assert (wl.sm_scale * q @ k.T).max() > 710.0
+
+
+# ---- per-row counts (variable-length selection lists)
+def test_counts_equal_to_topk_is_the_fixed_length_stage():
+    wl, qt, kt, vt, idx, vbs = tiny_case(topk=5)
+    full = np.full(idx.shape[:3], idx.shape[-1], np.int32)
+    a, la = oracle.fine_full(qt, kt, vt, idx, vbs, wl.sm_scale)
+    b, lb = oracle.fine_full_counts(qt, kt, vt, idx, full, vbs, wl.sm_scale)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_counts_brute_force(seed):
+    wl, qt, kt, vt, idx, vbs = tiny_case(topk=6)
+    rng = np.random.default_rng(40 + seed)
+    counts = rng.integers(1, idx.shape[-1] + 1, size=idx.shape[:3]).astype(np.int32)
+    garbage = idx.copy()
+    for r in np.ndindex(idx.shape[:3]):  # entries past the count are never read
+        garbage[r][counts[r]:] = rng.integers(0, wl.ncubes, size=idx.shape[-1] - counts[r])
+    o, lse = oracle.fine_full_counts(qt, kt, vt, garbage, counts, vbs, wl.sm_scale)
+    ref_o, ref_lse = brute_force(qt, kt, vt, idx, vbs, wl.sm_scale, counts)
+    assert np.abs(o - ref_o).max() < 1e-12
+    assert np.abs(lse - ref_lse).max() < 1e-10
+
+
+def test_count_zero_rows_are_empty():
+    wl, qt, kt, vt, idx, vbs = tiny_case(topk=4)
+    counts = np.full(idx.shape[:3], 4, np.int32)
+    counts[0, 1, 2] = 0
+    o, lse = oracle.fine_full_counts(qt, kt, vt, idx, counts, vbs, wl.sm_scale)
+    assert (o[0, 128:192, 1] == 0).all() and np.isneginf(lse[0, 1, 128:192]).all()
+    ref_o, ref_lse = oracle.fine_full(qt, kt, vt, idx, vbs, wl.sm_scale)
+    keep = np.ones(o.shape[1], bool)
+    keep[128:192] = False
+    assert np.array_equal(o[0, keep, 1], ref_o[0, keep, 1])
+    assert np.array_equal(o[:, :, 0], ref_o[:, :, 0]) and np.array_equal(lse[0, 0], ref_lse[0, 0])
