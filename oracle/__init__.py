@@ -16,6 +16,12 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*.py``):
                                   restatement, invariances, hand cases)
     fine                       -- pinned (dense SDPA special case, brute-force
                                   masked matrix, closed forms, invariances)
+    fine_counts                -- pinned (reduction to the fixed-length stage,
+                                  brute force on truncated rows, empty rows)
+    coarse_attn                -- pinned (dense SDPA on the pooled cubes,
+                                  closed forms, excluded empty cubes)
+    gated_combine              -- pinned (gate values that select one term,
+                                  hand-computed broadcast)
 """
 from __future__ import annotations
 
@@ -239,6 +245,50 @@ def fine_full_counts(qt, kt, vt, topk_idx, counts, vbs, sm_scale: float, nthread
     out = out_u.reshape(B, heads, N * 64, D).transpose(0, 2, 1, 3).copy()
     lse = lse_u.reshape(B, heads, N * 64).copy()
     return out, lse
+
+
+def coarse_attn(qt, kt, vt, vbs, sm_scale: float) -> np.ndarray:
+    """Coarse-stage attention output ([VSA-AMD] Two-Stage Architecture, Stage 1:
+    Coarse Selection -- each cube mean-pooled into cube-level Qc, Kc, Vc,
+    cube-to-cube attention; the final output gates it with the fine output).
+
+    Per (b, head): O_c = softmax(sm_scale * Qc Kc^T) Vc over the key cubes that
+    hold a real token (vbs > 0), in float64.  A query cube without a real token
+    gets zeros.  Returns [B, heads, N, D] float64.
+    """
+    vbs = _i32(vbs)
+    qm, km, vm = pool(qt, vbs), pool(kt, vbs), pool(vt, vbs)  # [B, heads, N, D]
+    live = vbs > 0
+    out = np.zeros_like(qm)
+    if not live.any():
+        return out
+    s = sm_scale * np.matmul(qm, km[:, :, live, :].transpose(0, 1, 3, 2))  # [B, heads, N, n_live]
+    s -= s.max(axis=-1, keepdims=True)
+    w = np.exp(s)
+    w /= w.sum(axis=-1, keepdims=True)
+    out[:] = np.matmul(w, vm[:, :, live, :])
+    out[:, :, ~live, :] = 0.0
+    return out
+
+
+def _bf16_to_f64(bits) -> np.ndarray:
+    return (_u16(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def gated_combine(fine_out, coarse_out, gate_c, gate_f) -> np.ndarray:
+    """Gated sum of the two stages ([VSA-AMD] Two-Stage Architecture: the
+    final output combines the coarse and fine outputs through gates), in the
+    tiled token layout: for token slot s of cube i,
+        out[b, 64 i + s, h, :] = gate_c[b, 64 i + s, h, :] * O_c[b, h, i, :]
+                               + gate_f[b, 64 i + s, h, :] * fine[b, 64 i + s, h, :].
+    fine_out: float [B, 64 N, heads, D]; coarse_out: [B, heads, N, D];
+    gate_c, gate_f: bf16 bits [B, 64 N, heads, D].  Returns float64."""
+    fine_out = np.asarray(fine_out, np.float64)
+    B, S, heads, D = fine_out.shape
+    N = S // 64
+    assert coarse_out.shape == (B, heads, N, D)
+    per_slot = np.repeat(np.asarray(coarse_out, np.float64).transpose(0, 2, 1, 3), 64, axis=1)
+    return _bf16_to_f64(gate_c) * per_slot + _bf16_to_f64(gate_f) * fine_out
 
 
 def default_threads() -> int:
