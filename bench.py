@@ -48,9 +48,9 @@ WORKLOAD = "wan"
 # was taken from: if fine.cu no longer hashes to `source_sha256`, the traffic is reported
 # as null.
 FINE_TRAFFIC = {
-    "bytes_per_launch": (247.396352e6 + 68.179968e6) * 40 / 8,
+    "bytes_per_launch": (247.384320e6 + 68.041216e6) * 40 / 8,
     "capture": "profiles/fine_fwd_kernel_wan.md",
-    "source_sha256": "6bf06424f116fc03ea9d0942cad0ae4ad2f6b4a87797b30e1333852fe843707e",
+    "source_sha256": "8d013deaba8423e25a16d6a81854c84a156f75636f33b45f6956c9b445e693cd",
 }
 
 
@@ -342,7 +342,8 @@ def run_ours(args, wl, inputs, rank, world, dist):
         raise RuntimeError("device error word set during the timed run")
 
     if args.no_e2e:
-        return ms_step, stage, clk.summary(), None, 0, 0, launches
+        nxt = time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream)
+        return ms_step, stage, clk.summary(), None, 0, 0, launches, nxt
     # ---- end to end through host buffers (pinned), copies inside the timed region.
     # Every step copies its q, k, v from pinned host memory and reads its output
     # back; the copies run on their own streams, double-buffered, so the upload of
@@ -403,7 +404,51 @@ def run_ours(args, wl, inputs, rank, world, dist):
         e2e_ms = float(t.item())
     h2d = 3 * qh.numel() * 2
     d2h = ohs[0].numel() * 2
-    return ms_step, stage, clk.summary(), e2e_ms, h2d, d2h, launches
+    # The next rows are timed last, after the end-to-end leg, on the step's tensors.
+    nxt = time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream)
+    return ms_step, stage, clk.summary(), e2e_ms, h2d, d2h, launches, nxt
+
+
+def time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream, calls=20):
+    """CUDA-event medians of the coarse-stage attention output and of the fine
+    stage with the gated combine, on the step's own tiled tensors (outside the
+    timed step; gates are seeded uniform [0, 1) bf16)."""
+    ws = torch.empty((vsa.coarse_attn_workspace_bytes(wl.B, wl.heads, wl.ncubes, wl.D),), dtype=torch.uint8,
+                     device=qt.device)
+    oc = torch.empty((wl.B, wl.heads, wl.ncubes, wl.D), dtype=torch.float32, device=qt.device)
+    gen = torch.Generator(device=qt.device)
+    gen.manual_seed(1234)
+    gc = torch.rand(qt.shape, generator=gen, device=qt.device).to(torch.bfloat16)
+    gf = torch.rand(qt.shape, generator=gen, device=qt.device).to(torch.bfloat16)
+
+    def median_ms(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(calls):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    ca_ms = median_ms(lambda: vsa.coarse_attn(qt, kt, vt, vbs, wl.sm_scale, workspace=ws, out=oc))
+    fg_ms = median_ms(lambda: vsa.sparse_attn_fwd(qt, kt, vt, idx, vbs, wl.sm_scale, out=ot, lse=lse, pairs=pairs,
+                                                  coarse_out=oc, gate_c=gc, gate_f=gf))
+    if vsa.device_error(reset=True):
+        raise RuntimeError("device error word set while timing the coarse output / gated fine stage")
+    n, real = wl.ncubes, wl.tokens
+    pool_bytes = 3 * wl.B * real * wl.heads * wl.D * 2   # the real tokens of q, k, v, read once
+    attn_flops = 4.0 * wl.B * wl.heads * n * n * wl.D   # scores and weighted sum, fp32 FMA
+    return {
+        "coarse_attn": {"ms_median": ca_ms, "algorithmic_bytes": pool_bytes, "fp32_flops": attn_flops,
+                        "note": "pooled means of q, k, v (HBM) + cube-level attention (fp32 FMA)"},
+        "sparse_attn_fwd_gated": {"ms_median": fg_ms, "effective_tflops": wl.fine_flops() / (fg_ms * 1e-3) / 1e12,
+                                  "extra_hbm_bytes": 2 * wl.B * wl.s_pad * wl.heads * wl.D * 2,
+                                  "note": "fine stage + gate_c * coarse + gate_f * fine in the epilogue"},
+    }
 
 
 def main():
@@ -455,7 +500,7 @@ def main():
         dist.barrier()
 
     inputs = synth.make_inputs(wl)
-    ms_step, stage, clocks, e2e_ms, h2d, d2h, launches = run_ours(args, wl, inputs, rank, world, dist)
+    ms_step, stage, clocks, e2e_ms, h2d, d2h, launches, nxt = run_ours(args, wl, inputs, rank, world, dist)
 
     burst, sustained, hbm, peak_kind = load_peaks()
     flops = wl.fine_flops()
@@ -483,6 +528,7 @@ def main():
             "value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
+        "next_rows": nxt,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:

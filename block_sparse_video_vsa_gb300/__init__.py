@@ -24,6 +24,7 @@ from .build import LIB_PATH
 __all__ = [
     "VsaError", "library", "num_cubes", "tile", "untile", "coarse_workspace_bytes", "coarse_select",
     "sparse_attn_fwd", "validate_indices", "device_error", "debug_wait_timeout", "pipeline",
+    "coarse_attn", "coarse_attn_workspace_bytes", "pair_cubes", "pair_workspace_bytes", "kernel_launches",
 ]
 
 _STATUS = {0: "VSA_OK", 1: "VSA_ERR_INVALID_ARG", 2: "VSA_ERR_UNSUPPORTED", 3: "VSA_ERR_ALIGNMENT",
@@ -79,6 +80,13 @@ def _declare(lib):
     lib.vsa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), _i32]
     lib.vsa_debug_wait_timeout.restype = ctypes.c_int
     lib.vsa_debug_wait_timeout.argtypes = [ctypes.c_int64, _p, _p]
+    lib.vsa_sparse_attn_fwd_gated.restype = ctypes.c_int
+    lib.vsa_sparse_attn_fwd_gated.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32,
+                                              ctypes.c_float, _p, _p, _p, _p, _p, _p]
+    lib.vsa_coarse_attn_workspace_bytes.restype = ctypes.c_size_t
+    lib.vsa_coarse_attn_workspace_bytes.argtypes = [_i32] * 4
+    lib.vsa_coarse_attn.restype = ctypes.c_int
+    lib.vsa_coarse_attn.argtypes = [_p, _p, _p, _p, _i32, _i32, _i32, _i32, ctypes.c_float, _p, _p, _p]
     lib.vsa_kernel_launches.restype = ctypes.c_uint64
     lib.vsa_kernel_launches.argtypes = []
     return lib
@@ -231,12 +239,16 @@ def pair_cubes(topk_idx, workspace=None, out=None, stream=None):
 
 
 def sparse_attn_fwd(qt, kt, vt, topk_idx, vbs, sm_scale: float = 0.0, out=None, lse=None,
-                    want_lse: bool = True, pairs=None, counts=None, stream=None):
+                    want_lse: bool = True, pairs=None, counts=None, coarse_out=None, gate_c=None, gate_f=None,
+                    stream=None):
     """Block-sparse attention -> (out bf16 [B, 64*N, heads, D], lse fp32 [B, heads, 64*N] or None).
 
     `pairs` (from pair_cubes) sets which query cubes share a tile; None pairs
     cubes (2u, 2u + 1).  The results do not depend on it beyond rounding.
-    `counts` (int32 [B, heads, N]) limits row i to its first counts[i] entries."""
+    `counts` (int32 [B, heads, N]) limits row i to its first counts[i] entries.
+    With `coarse_out` (fp32 [B, heads, N, D], from coarse_attn) and the bf16
+    gates `gate_c`, `gate_f` (shaped like out), out is the gated sum
+    gate_c * coarse + gate_f * fine."""
     torch = _torch()
     for t, n in ((qt, "qt"), (kt, "kt"), (vt, "vt")):
         _need(t, torch.bfloat16, n)
@@ -264,13 +276,48 @@ def sparse_attn_fwd(qt, kt, vt, topk_idx, vbs, sm_scale: float = 0.0, out=None, 
         _need(counts, torch.int32, "counts")
         if tuple(counts.shape) != (B, heads, N):
             raise ValueError("counts must be [B, heads, N]")
-    _check(library().vsa_sparse_attn_fwd_ex(qt.data_ptr(), kt.data_ptr(), vt.data_ptr(), topk_idx.data_ptr(),
-                                            counts.data_ptr() if counts is not None else None, vbs.data_ptr(),
-                                            pairs.data_ptr() if pairs is not None else None,
-                                            B, N, heads, D, topk, float(sm_scale), out.data_ptr(),
-                                            lse.data_ptr() if lse is not None else None, _stream(stream)),
+    gated = [coarse_out, gate_c, gate_f]
+    if any(t is not None for t in gated):
+        if any(t is None for t in gated):
+            raise ValueError("coarse_out, gate_c and gate_f go together")
+        _need(coarse_out, torch.float32, "coarse_out")
+        _need(gate_c, torch.bfloat16, "gate_c")
+        _need(gate_f, torch.bfloat16, "gate_f")
+        if tuple(coarse_out.shape) != (B, heads, N, D) or gate_c.shape != qt.shape or gate_f.shape != qt.shape:
+            raise ValueError("coarse_out must be [B, heads, N, D] and the gates shaped like qt")
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    _check(library().vsa_sparse_attn_fwd_gated(qt.data_ptr(), kt.data_ptr(), vt.data_ptr(), topk_idx.data_ptr(),
+                                               ptr(counts), vbs.data_ptr(), ptr(pairs), B, N, heads, D, topk,
+                                               float(sm_scale), ptr(coarse_out), ptr(gate_c), ptr(gate_f),
+                                               out.data_ptr(), ptr(lse), _stream(stream)),
            "vsa_sparse_attn_fwd")
     return out, lse
+
+
+def coarse_attn_workspace_bytes(B: int, heads: int, ncubes: int, D: int) -> int:
+    return int(library().vsa_coarse_attn_workspace_bytes(B, heads, ncubes, D))
+
+
+def coarse_attn(qt, kt, vt, vbs, sm_scale: float = 0.0, workspace=None, out=None, stream=None):
+    """Coarse-stage attention over the mean-pooled cubes -> fp32 [B, heads, N, D]."""
+    torch = _torch()
+    for t, n in ((qt, "qt"), (kt, "kt"), (vt, "vt")):
+        _need(t, torch.bfloat16, n)
+    _need(vbs, torch.int32, "vbs")
+    B, S, heads, D = qt.shape
+    if kt.shape != qt.shape or vt.shape != qt.shape or S % 64:
+        raise ValueError("qt/kt/vt must share a tiled [B, 64*N, heads, D] shape")
+    N = S // 64
+    if workspace is None:
+        workspace = torch.empty((coarse_attn_workspace_bytes(B, heads, N, D),), dtype=torch.uint8,
+                                device=qt.device)
+    if out is None:
+        out = torch.empty((B, heads, N, D), dtype=torch.float32, device=qt.device)
+    _need(out, torch.float32, "out")
+    _check(library().vsa_coarse_attn(qt.data_ptr(), kt.data_ptr(), vt.data_ptr(), vbs.data_ptr(), B, N, heads, D,
+                                     float(sm_scale), workspace.data_ptr(), out.data_ptr(), _stream(stream)),
+           "vsa_coarse_attn")
+    return out
 
 
 def validate_indices(topk_idx, vbs, stream=None) -> int:

@@ -141,11 +141,14 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
                                    static_cast<cudaStream_t>(stream)));
 }
 
-vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
-                                  const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int32_t B,
-                                  int32_t ncubes, int32_t heads, int32_t D, int32_t topk, float sm_scale,
-                                  void* out, float* lse, vsa_stream_t stream) {
+vsa_status vsa_sparse_attn_fwd_gated(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                                     const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int32_t B,
+                                     int32_t ncubes, int32_t heads, int32_t D, int32_t topk, float sm_scale,
+                                     const float* coarse_out, const void* gate_c, const void* gate_f, void* out,
+                                     float* lse, vsa_stream_t stream) {
     if (!qt || !kt || !vt || !topk_idx || !vbs || !out) return VSA_ERR_INVALID_ARG;
+    const bool gated = coarse_out || gate_c || gate_f;
+    if (gated && (!coarse_out || !gate_c || !gate_f)) return VSA_ERR_INVALID_ARG;
     if (B <= 0 || ncubes <= 0 || heads <= 0 || topk <= 0 || topk > ncubes) return VSA_ERR_INVALID_ARG;
     if (!(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return VSA_ERR_UNSUPPORTED;
@@ -157,7 +160,8 @@ vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt
     if (!aligned16(qt) || !aligned16(kt) || !aligned16(vt) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(vbs) & 3u) ||
         (reinterpret_cast<uintptr_t>(pairs) & 3u) || (reinterpret_cast<uintptr_t>(counts) & 3u) ||
-        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+        (gated && (!aligned16(coarse_out) || !aligned16(gate_c) || !aligned16(gate_f))))
         return VSA_ERR_ALIGNMENT;
     DevCtx ctx;
     cudaError_t e = get_dev_ctx(&ctx);
@@ -165,7 +169,39 @@ vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt
     if (fine_smem_bytes() > ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
     return from_cuda(launch_fine(qt, kt, vt, topk_idx, counts, vbs, pairs, B, ncubes, heads, D, topk, sm_scale,
-                                 out, lse, ctx.err, ctx.num_sms, static_cast<cudaStream_t>(stream)));
+                                 coarse_out, gate_c, gate_f, out, lse, ctx.err, ctx.num_sms,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                                  const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int32_t B,
+                                  int32_t ncubes, int32_t heads, int32_t D, int32_t topk, float sm_scale,
+                                  void* out, float* lse, vsa_stream_t stream) {
+    return vsa_sparse_attn_fwd_gated(qt, kt, vt, topk_idx, counts, vbs, pairs, B, ncubes, heads, D, topk, sm_scale,
+                                     nullptr, nullptr, nullptr, out, lse, stream);
+}
+
+size_t vsa_coarse_attn_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t D) {
+    if (B <= 0 || heads <= 0 || ncubes <= 0 || (D != 64 && D != 128)) return 0;
+    return coarse_attn_workspace_bytes(B, heads, ncubes, D);
+}
+
+vsa_status vsa_coarse_attn(const void* qt, const void* kt, const void* vt, const int32_t* vbs, int32_t B,
+                           int32_t ncubes, int32_t heads, int32_t D, float sm_scale, void* workspace,
+                           float* coarse_out, vsa_stream_t stream) {
+    if (!qt || !kt || !vt || !vbs || !workspace || !coarse_out) return VSA_ERR_INVALID_ARG;
+    if (B <= 0 || ncubes <= 0 || heads <= 0) return VSA_ERR_INVALID_ARG;
+    if (!(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return VSA_ERR_UNSUPPORTED;
+    if (!sizes_fit(B, (int64_t)ncubes * 64, heads, D) || B > 65535 || heads > 65535 ||
+        (int64_t)B * ncubes >= ((int64_t)1 << 31))
+        return VSA_ERR_UNSUPPORTED;
+    if (!aligned16(qt) || !aligned16(kt) || !aligned16(vt) || !aligned16(workspace) || !aligned16(coarse_out) ||
+        (reinterpret_cast<uintptr_t>(vbs) & 3u))
+        return VSA_ERR_ALIGNMENT;
+    if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
+    return from_cuda(launch_coarse_attn(qt, kt, vt, vbs, B, ncubes, heads, D, sm_scale, workspace, coarse_out,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 vsa_status vsa_sparse_attn_fwd_paired(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,

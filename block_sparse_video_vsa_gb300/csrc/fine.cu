@@ -115,6 +115,9 @@ struct FineParams {
     const uint32_t* pairs;  // [B * heads][npairs]: i | (j << 16), j = 0xFFFF single; or null: (2u, 2u + 1)
     const int32_t* counts;  // [B * heads * N] entries of each topk_idx row in use (<= topk), or null: all
     const uint4* q;      // tiled q rows (for staging Q into TMEM)
+    const float* oc;     // coarse-stage output [B * heads][N][D], or null: no gated combine
+    const uint4* gc;     // gates of the coarse and fine terms, bf16 in the layout of out
+    const uint4* gf;
     __nv_bfloat16* out;
     float* lse;
     unsigned int* err;
@@ -266,7 +269,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
-template <int kD>
+template <int kD, bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
     fine_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     FineParams p) {
@@ -519,6 +522,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ul = 0; ul < my_units; ++ul) {
             const int u = blockIdx.x + ul * gridDim.x;
             const int lb = ul & 1;
+            if constexpr (kGated) {
+                // The epilogue reads this thread's half row of both gates (one
+                // 128-byte line each for D = 128): start bringing them into L2.
+                int b, h, pair;
+                unit_coords(u, p, b, h, pair);
+                int i0, i1;
+                unit_cubes(p, b, h, pair, i0, i1);
+                const int i = (r >> 6) ? i1 : i0;
+                if (i >= 0) {
+                    const size_t gi = ((size_t)(b * s_pad + i * kCubeTokens + (r & 63)) * p.heads + h) *
+                                          (size_t)(D / 8) + hf * (dh / 8);
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.gc + gi));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.gf + gi));
+                }
+            }
             if (ok) ok = mbar_wait_bounded(smem_u32(&ms.list_full[lb]), (ul >> 1) & 1, abort_flag, p.err,
                                            kWaitLimitNs);
             const uint32_t* list = lists + lb * kMaxUnion;
@@ -661,7 +679,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int q = 0; q < 32; ++q) o[q] = 0u;
                     }
-                    if (i >= 0) {
+                    if (kGated && i >= 0) {
+                        // Gated sum with the coarse-stage output of the row's cube.  All
+                        // of the chunk's gate and coarse values are loaded before the
+                        // first store (the stores could alias them for the compiler).
+                        const float4* ocr = reinterpret_cast<const float4*>(
+                            p.oc + (((size_t)b * p.heads + h) * p.N + i) * D + c0);
+                        const size_t gi = (row * p.heads + h) * (size_t)(D / 8) + c0 / 8;
+                        uint4 gcv[4], gfv[4];
+                        float4 cv4[8];
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            gcv[v] = __ldcs(p.gc + gi + v);
+                            gfv[v] = __ldcs(p.gf + gi + v);
+                        }
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) cv4[v] = __ldg(ocr + v);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float cv[8] = {cv4[2 * v].x, cv4[2 * v].y, cv4[2 * v].z, cv4[2 * v].w,
+                                                 cv4[2 * v + 1].x, cv4[2 * v + 1].y, cv4[2 * v + 1].z,
+                                                 cv4[2 * v + 1].w};
+                            const uint32_t gcw[4] = {gcv[v].x, gcv[v].y, gcv[v].z, gcv[v].w};
+                            const uint32_t gfw[4] = {gfv[v].x, gfv[v].y, gfv[v].z, gfv[v].w};
+                            uint32_t pw[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float f0 = __uint_as_float(o[8 * v + 2 * e]) * inv_l;
+                                const float f1 = __uint_as_float(o[8 * v + 2 * e + 1]) * inv_l;
+                                const float r0 = fmaf(__uint_as_float(gcw[e] << 16), cv[2 * e],
+                                                      __uint_as_float(gfw[e] << 16) * f0);
+                                const float r1 = fmaf(__uint_as_float(gcw[e] & 0xFFFF0000u), cv[2 * e + 1],
+                                                      __uint_as_float(gfw[e] & 0xFFFF0000u) * f1);
+                                pw[e] = pack_bf16x2(r0, r1);
+                            }
+                            __stcs(dst + c0 / 8 + v, make_uint4(pw[0], pw[1], pw[2], pw[3]));
+                        }
+                    } else if (i >= 0) {
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint4 w;
@@ -730,8 +784,9 @@ int fine_max_cubes() { return kMaxCubes; }
 
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                         const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int B, int ncubes,
-                        int heads, int D, int topk, float sm_scale, void* out, float* lse, unsigned int* err,
-                        int num_sms, cudaStream_t stream) {
+                        int heads, int D, int topk, float sm_scale, const float* coarse_out, const void* gate_c,
+                        const void* gate_f, void* out, float* lse, unsigned int* err, int num_sms,
+                        cudaStream_t stream) {
     CUtensorMap mk, mv;
     const int rows = B * ncubes * kCubeTokens;
     if (!make_map(&mk, kt, rows, heads, D, true) || !make_map(&mv, vt, rows, heads, D, true))
@@ -741,6 +796,9 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     p.vbs = vbs;
     p.pairs = pairs;
     p.counts = counts;
+    p.oc = coarse_out;
+    p.gc = static_cast<const uint4*>(gate_c);
+    p.gf = static_cast<const uint4*>(gate_f);
     p.q = static_cast<const uint4*>(qt);
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;
@@ -753,7 +811,8 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     p.npairs = (ncubes + 1) / 2;
     p.num_units = B * heads * p.npairs;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
-    auto kernel = D == 64 ? fine_fwd_kernel<64> : fine_fwd_kernel<128>;
+    auto kernel = coarse_out ? (D == 64 ? fine_fwd_kernel<64, true> : fine_fwd_kernel<128, true>)
+                             : (D == 64 ? fine_fwd_kernel<64, false> : fine_fwd_kernel<128, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     const int grid = p.num_units < num_sms ? p.num_units : num_sms;

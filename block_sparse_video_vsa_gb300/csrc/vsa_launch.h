@@ -37,8 +37,15 @@ int fine_max_topk();
 int fine_max_cubes();
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                         const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int B, int ncubes,
-                        int heads, int D, int topk, float sm_scale, void* out, float* lse, unsigned int* err,
-                        int num_sms, cudaStream_t stream);
+                        int heads, int D, int topk, float sm_scale, const float* coarse_out, const void* gate_c,
+                        const void* gate_f, void* out, float* lse, unsigned int* err, int num_sms,
+                        cudaStream_t stream);
+
+// coarse_attn.cu
+size_t coarse_attn_workspace_bytes(int B, int heads, int ncubes, int D);
+cudaError_t launch_coarse_attn(const void* qt, const void* kt, const void* vt, const int32_t* vbs, int B,
+                               int ncubes, int heads, int D, float sm_scale, void* workspace, float* out,
+                               cudaStream_t stream);
 
 // pair.cu
 int pair_words(int ncubes);

@@ -12,6 +12,9 @@
  *      (vsa_pair_cubes     optional schedule for step 3: which query cubes
  *                          share a tensor-core tile; results are unchanged)
  *   4. vsa_untile          the inverse permutation of step 1.
+ * and, beside them, the coarse stage's own attention output
+ * (vsa_coarse_attn) and its gated sum with the fine output
+ * (vsa_sparse_attn_fwd_gated).
  *
  * Sources (page title, section):
  *   [VSA-AMD] "VSA: Accelerating Video Diffusion Inference with Sparse
@@ -245,6 +248,52 @@ vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt
                                   const int32_t* vbs, const uint32_t* pairs, int32_t B,
                                   int32_t ncubes, int32_t heads, int32_t D, int32_t topk,
                                   float sm_scale, void* out, float* lse, vsa_stream_t stream);
+
+/*
+ * Coarse-stage attention output ([VSA-AMD] Two-Stage Architecture, Stage 1:
+ * each cube is mean-pooled into cube-level Qc, Kc, Vc and attends cube to
+ * cube; the final output gates the coarse and fine outputs together):
+ *   coarse_out[b, head, i, :] = sum_j w_ij Vc[b, head, j, :],
+ *   w_ij = softmax_j(sm_scale * Qc[i] . Kc[j]) over the key cubes j with
+ *          vbs[j] > 0,
+ * with Qc, Kc, Vc the means over each cube's vbs real tokens, computed in
+ * fp32.  A query cube with vbs = 0 gets zeros.
+ *   qt, kt, vt : tiled bf16 [B, 64 * ncubes, heads, D]
+ *   vbs        : int32 [ncubes]
+ *   sm_scale   : <= 0 selects 1 / sqrt(D)
+ *   workspace  : device buffer of vsa_coarse_attn_workspace_bytes(...) bytes
+ *                (the fp32 cube means [3][B][heads][ncubes][D]), overwritten
+ *   coarse_out : fp32 [B, heads, ncubes, D] (written)
+ * Limits: D in {64, 128}; B, heads <= 65535.  Two kernel launches.
+ */
+size_t vsa_coarse_attn_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t D);
+vsa_status vsa_coarse_attn(const void* qt, const void* kt, const void* vt, const int32_t* vbs,
+                           int32_t B, int32_t ncubes, int32_t heads, int32_t D, float sm_scale,
+                           void* workspace, float* coarse_out, vsa_stream_t stream);
+
+/*
+ * vsa_sparse_attn_fwd_ex whose output is the gated sum of the two stages
+ * ([VSA-AMD] Two-Stage Architecture: the final output combines the coarse
+ * and fine outputs through gates): for token slot s of cube i,
+ *   out[b, 64 i + s, head, :] = gate_c[...] * coarse_out[b, head, i, :]
+ *                             + gate_f[...] * fine[b, 64 i + s, head, :],
+ * with [...] = [b, 64 i + s, head, :] and fine the normalised fine-stage
+ * output, formed in fp32 inside the fine kernel's epilogue and rounded to
+ * bf16 once.  lse stays the fine stage's.
+ *   coarse_out     : fp32 [B, heads, ncubes, D] (e.g. from vsa_coarse_attn)
+ *   gate_c, gate_f : bf16 in the layout of out, [B, 64 * ncubes, heads, D]
+ * All three are required together (any one NULL with another set is
+ * VSA_ERR_INVALID_ARG; all NULL is vsa_sparse_attn_fwd_ex) and must be
+ * 16-byte aligned.  Other arguments, limits and errors as for
+ * vsa_sparse_attn_fwd_ex.
+ */
+vsa_status vsa_sparse_attn_fwd_gated(const void* qt, const void* kt, const void* vt,
+                                     const int32_t* topk_idx, const int32_t* counts,
+                                     const int32_t* vbs, const uint32_t* pairs, int32_t B,
+                                     int32_t ncubes, int32_t heads, int32_t D, int32_t topk,
+                                     float sm_scale, const float* coarse_out, const void* gate_c,
+                                     const void* gate_f, void* out, float* lse,
+                                     vsa_stream_t stream);
 
 /*
  * Debug aid for the block-sparse encoding ([VSA-AMD] Block-Sparse Encoding):

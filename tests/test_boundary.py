@@ -38,7 +38,8 @@ def test_header_declares_the_entry_points():
               "vsa_coarse_workspace_bytes", "vsa_num_cubes", "vsa_status_string",
               "vsa_validate_indices", "vsa_device_error", "vsa_debug_wait_timeout",
               "vsa_pair_cubes", "vsa_pair_workspace_bytes", "vsa_sparse_attn_fwd_paired",
-              "vsa_sparse_attn_fwd_ex"):
+              "vsa_sparse_attn_fwd_ex", "vsa_sparse_attn_fwd_gated", "vsa_coarse_attn",
+              "vsa_coarse_attn_workspace_bytes", "vsa_kernel_launches"):
         assert n in names
 
 
@@ -138,6 +139,22 @@ def test_counts_validation(lib):
     assert h(A, A, A, A, A, A, A + 2, 1, 12, 2, 64, 3, 0.0, A, None, None) == ALIGNMENT     # pairs
     assert h(A, A, A, A, A, A, None, 1, 12, 2, 64, 13, 0.0, A, None, None) == INVALID      # topk > N
     assert h(A, A, A, A, A, A, None, 1, 12, 2, 256, 3, 0.0, A, None, None) == UNSUPPORTED
+
+
+def test_coarse_attn_and_gated_validation(lib):
+    f = lib.vsa_coarse_attn
+    #   qt kt vt vbs  B  N  H  D  scale ws out stream
+    assert f(A, A, A, A, 1, 12, 2, 64, 0.0, None, A, None) == INVALID
+    assert f(A, A, A, A, 1, 12, 2, 96, 0.0, A, A, None) == UNSUPPORTED
+    assert f(A, A, A, A, 1, 12, 2, 64, 0.0, MIS, A, None) == ALIGNMENT
+    assert f(A, A, A, A, 1, 12, 2, 64, float("nan"), A, A, None) == INVALID
+    lib.vsa_coarse_attn_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.vsa_coarse_attn_workspace_bytes(2, 3, 12, 64) == 3 * 2 * 3 * 12 * 64 * 4
+    assert lib.vsa_coarse_attn_workspace_bytes(1, 40, 624, 128) == 3 * 40 * 624 * 128 * 4
+    g = lib.vsa_sparse_attn_fwd_gated
+    #   qt kt vt idx counts vbs pairs  B  N  H  D  k  scale oc gc gf out lse stream
+    assert g(A, A, A, A, None, A, None, 1, 12, 2, 64, 3, 0.0, A, None, A, A, None, None) == INVALID
+    assert g(A, A, A, A, None, A, None, 1, 12, 2, 64, 3, 0.0, A, A, MIS, A, None, None) == ALIGNMENT
 
 
 def test_refused_calls_launch_nothing(lib):
