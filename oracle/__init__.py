@@ -22,6 +22,10 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*.py``):
                                   closed forms, excluded empty cubes)
     gated_combine              -- pinned (gate values that select one term,
                                   hand-computed broadcast)
+    block_pool / block_select_cdf / blocks_to_cube_lut
+                               -- pinned (closed forms, brute force over key
+                                  subsets, limits of the threshold, dense
+                                  attention over the kept blocks' tokens)
 """
 from __future__ import annotations
 
@@ -289,6 +293,66 @@ def gated_combine(fine_out, coarse_out, gate_c, gate_f) -> np.ndarray:
     assert coarse_out.shape == (B, heads, N, D)
     per_slot = np.repeat(np.asarray(coarse_out, np.float64).transpose(0, 2, 1, 3), 64, axis=1)
     return _bf16_to_f64(gate_c) * per_slot + _bf16_to_f64(gate_f) * fine_out
+
+
+def block_pool(x, block: int) -> np.ndarray:
+    """Means of contiguous token blocks ([INT8-WAN] Decoupling Block Selection
+    from Sparse CUDA Kernels, step 1): x bf16 bits [B, S, heads, D] in raster
+    token order, S a multiple of `block` -> [B, heads, S / block, D] float64."""
+    x = _bf16_to_f64(x)
+    B, S, heads, D = x.shape
+    assert S % block == 0
+    nb = S // block
+    return x.reshape(B, nb, block, heads, D).mean(axis=2).transpose(0, 2, 1, 3).copy()
+
+
+def block_select_cdf(q, k, block: int, tau: float, sm_scale: float):
+    """Mean-pool block selector with a cumulative threshold ([INT8-WAN]
+    Decoupling Block Selection from Sparse CUDA Kernels, steps 1-3): pool each
+    `block`-token query and key block, score S_ij = qbar_i . kbar_j, order each
+    query block's key blocks by score (descending; equal scores: lower index
+    first) and keep them in that order until the kept share of
+    softmax_j(sm_scale * S_ij) reaches tau (at least one block; all of them if
+    the sum never reaches tau).
+
+    Returns (idx int32 [B, heads, nb, nb]: the kept blocks first, in that
+    order, then -1; counts int32 [B, heads, nb]) and the fp64 scores."""
+    qm, km = block_pool(q, block), block_pool(k, block)
+    B, heads, nb, _ = qm.shape
+    scores = np.matmul(qm, km.transpose(0, 1, 3, 2))  # [B, heads, nb, nb]
+    idx = np.full((B, heads, nb, nb), -1, np.int32)
+    counts = np.zeros((B, heads, nb), np.int32)
+    for b in range(B):
+        for h in range(heads):
+            for i in range(nb):
+                s = scores[b, h, i]
+                order = sorted(range(nb), key=lambda j: (-s[j], j))
+                w = np.exp(sm_scale * (s - s.max()))
+                w /= w.sum()
+                kept, mass = 0, 0.0
+                while kept < nb and (kept == 0 or mass < tau):
+                    mass += w[order[kept]]
+                    kept += 1
+                idx[b, h, i, :kept] = order[:kept]
+                counts[b, h, i] = kept
+    return idx, counts, scores
+
+
+def blocks_to_cube_lut(idx, counts, cubes_per_block: int = 2):
+    """A block-level table over `cubes_per_block`-cube blocks (128 tokens = 2
+    cubes of 64) -> the cube-level table of the fine stage: query cube
+    c * cubes_per_block + r (any r) attends the cubes of its block's kept key
+    blocks, block j -> cubes j * cubes_per_block + 0 .. cubes_per_block - 1, in
+    the block order.  Returns (cube_idx [B, heads, nb * cpb, nb * cpb] with -1
+    past the count, cube_counts [B, heads, nb * cpb])."""
+    B, heads, nb, kmax = idx.shape
+    c = cubes_per_block
+    out = np.full((B, heads, nb * c, kmax * c), -1, np.int32)
+    cnt = np.repeat(counts * c, c, axis=2).astype(np.int32)
+    for r in range(c):
+        sub = np.where(idx >= 0, idx * c + r, -1)
+        out[:, :, :, r::c] = np.repeat(sub, c, axis=2)
+    return out, cnt
 
 
 def default_threads() -> int:
