@@ -75,10 +75,9 @@ def test_equal_scores_keep_a_fixed_share_in_index_order(m):
     assert (idx[0, 0, :, :m] == np.arange(m)).all()
 
 
-@pytest.mark.parametrize("seed, tau", [(4, 0.5), (5, 0.8), (6, 0.95)])
-def test_brute_force_smallest_subset(seed, tau):
+@pytest.mark.parametrize("seed, tau, scale", [(4, 0.5, 0.5), (5, 0.8, 0.5), (6, 0.95, 0.5), (7, 0.9, 8.0)])
+def test_brute_force_smallest_subset(seed, tau, scale):
     q, k = random_qk(seed, nb=6, heads=1)
-    scale = 0.5
     idx, counts, s = oracle.block_select_cdf(q, k, 128, tau, scale)
     for i in range(6):
         w = np.exp(scale * (s[0, 0, i] - s[0, 0, i].max()))

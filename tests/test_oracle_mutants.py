@@ -69,3 +69,64 @@ def test_planted_mistake_is_caught(name, tmp_path):
         for pin in pins:
             with pytest.raises(AssertionError):
                 pin()
+
+
+# ---- the Python-level oracle functions (numpy): a planted mistake in a copy
+# of the module source, the mutated function patched in, its pins must fail.
+import test_oracle_block_select as tb  # noqa: E402
+import test_oracle_coarse_attn as tca  # noqa: E402
+
+PY_SRC = os.path.join(os.path.dirname(oracle.__file__), "__init__.py")
+
+PY_MUTANTS = {
+    # name: (function, (old, new), pins expected to fail)
+    "coarse_attn_values_from_keys": (
+        "coarse_attn", ("qm, km, vm = pool(qt, vbs), pool(kt, vbs), pool(vt, vbs)",
+                        "qm, km, vm = pool(qt, vbs), pool(kt, vbs), pool(kt, vbs)"),
+        [lambda: tca.test_equals_dense_sdpa_on_pooled_cubes("tiny"), tca.test_equal_keys_give_the_plain_mean_of_values]),
+    "coarse_attn_unscaled": (
+        "coarse_attn", ("s = sm_scale * np.matmul(", "s = 1.0 * np.matmul("),
+        [lambda: tca.test_equals_dense_sdpa_on_pooled_cubes("mid")]),
+    "coarse_attn_keeps_empty_keys": (
+        "coarse_attn", ("live = vbs > 0", "live = vbs >= 0"),
+        [tca.test_empty_cubes_are_no_keys_and_give_zero_rows]),
+    "gated_swaps_gates": (
+        "gated_combine", ("return _bf16_to_f64(gate_c) * per_slot + _bf16_to_f64(gate_f) * fine_out",
+                          "return _bf16_to_f64(gate_f) * per_slot + _bf16_to_f64(gate_c) * fine_out"),
+        [tca.test_gates_select_one_stage, tca.test_gated_sum_by_hand]),
+    "gated_broadcast_by_token_not_cube": (
+        "gated_combine", ("np.repeat(np.asarray(coarse_out, np.float64).transpose(0, 2, 1, 3), 64, axis=1)",
+                          "np.tile(np.asarray(coarse_out, np.float64).transpose(0, 2, 1, 3), (1, 64, 1, 1))"),
+        [tca.test_gates_select_one_stage, tca.test_gated_sum_by_hand]),
+    "block_select_one_past_threshold": (
+        "block_select_cdf", ("while kept < nb and (kept == 0 or mass < tau):",
+                             "while kept < nb and (kept == 0 or mass - w[order[kept - 1]] < tau):"),
+        [lambda: tb.test_brute_force_smallest_subset(7, 0.9, 8.0), tb.test_threshold_limits]),
+    "block_select_ascending": (
+        "block_select_cdf", ("order = sorted(range(nb), key=lambda j: (-s[j], j))",
+                             "order = sorted(range(nb), key=lambda j: (s[j], j))"),
+        [tb.test_threshold_limits, lambda: tb.test_brute_force_smallest_subset(5, 0.8, 0.5)]),
+    "block_select_unscaled_weights": (
+        "block_select_cdf", ("w = np.exp(sm_scale * (s - s.max()))", "w = np.exp(s - s.max())"),
+        [lambda: tb.test_brute_force_smallest_subset(7, 0.9, 8.0)]),
+    "cube_lut_neighbouring_blocks": (
+        "blocks_to_cube_lut", ("sub = np.where(idx >= 0, idx * c + r, -1)", "sub = np.where(idx >= 0, idx + r, -1)"),
+        [tb.test_block_table_to_cube_table_by_hand, tb.test_block_sparse_attention_is_dense_attention_over_kept_blocks]),
+    "fine_counts_ignores_counts": (
+        "fine_counts", ("idx2[:, :, :N] = np.where(np.arange(k)[None, None, None, :] < c[..., None], topk_idx, N)",
+                        "idx2[:, :, :N] = topk_idx"),
+        [lambda: tf.test_counts_brute_force(0), tf.test_count_zero_rows_are_empty]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_planted_python_mistake_is_caught(name, monkeypatch):
+    func, (old, new), pins = PY_MUTANTS[name]
+    src = open(PY_SRC).read()
+    assert src.count(old) == 1, f"patch anchor missing for {name}"
+    ns = {"__name__": "oracle_mutant", "__file__": PY_SRC}
+    exec(compile(src.replace(old, new), PY_SRC, "exec"), ns)
+    monkeypatch.setattr(oracle, func, ns[func])
+    for pin in pins:
+        with pytest.raises(AssertionError):
+            pin()
