@@ -329,11 +329,7 @@ def run_ours(args, wl, inputs, rank, world, dist):
         clk.window = (t0, time.monotonic())
     if dist:
         dist.barrier()
-    ms_total = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(start.elapsed_time(end), dist, dev)
     ms_step = ms_total / args.steps
     stage = {name: [marks[s][i].elapsed_time(marks[s][i + 1]) for s in range(args.steps)]
              for i, name in enumerate(["tile_qk", "coarse_select", "pair_cubes", "sparse_attn_fwd", "untile"])}
@@ -398,15 +394,28 @@ def run_ours(args, wl, inputs, rank, world, dist):
     last = (e2e_steps - 1) & 1
     if not torch.equal(ohs[last], douts[last].cpu()):
         raise RuntimeError("end-to-end read-back differs from the device result")
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     h2d = 3 * qh.numel() * 2
     d2h = ohs[0].numel() * 2
     # The next rows are timed last, after the end-to-end leg, on the step's tensors.
     nxt = time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream)
     return ms_step, stage, clk.summary(), e2e_ms, h2d, d2h, launches, nxt
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The slowest rank's time (every rank gets it); x itself with one process."""
+    if not dist:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(world: int, flops_per_rank: float, ms: float) -> float:
+    """Effective TFLOP/s of all ranks together: every rank processed `flops_per_rank`
+    in at most `ms` milliseconds (weak scaling: per-rank work is fixed)."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
 def time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream, calls=20):
@@ -506,7 +515,7 @@ def main():
     flops = wl.fine_flops()
     fine_ms = statistics.mean(stage["sparse_attn_fwd"])
     fine_tflops = flops / (fine_ms * 1e-3) / 1e12
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_throughput(world, flops, ms_step)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -525,7 +534,7 @@ def main():
                      "peak_kind": f"{peak_kind} dense bf16 burst",
                      "kernel": "fine_fwd_kernel (vsa_sparse_attn_fwd)"},
         "e2e": None if e2e_ms is None else {
-            "value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+            "value": whole_job_throughput(world, flops, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "next_rows": nxt,
