@@ -26,6 +26,10 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*.py``):
                                -- pinned (closed forms, brute force over key
                                   subsets, limits of the threshold, dense
                                   attention over the kept blocks' tokens)
+    row_peak / captured_mass / rel_l1
+                               -- pinned (single key, equal logits, explicit
+                                  dense weights summed over the selection,
+                                  hand values)
 """
 from __future__ import annotations
 
@@ -353,6 +357,55 @@ def blocks_to_cube_lut(idx, counts, cubes_per_block: int = 2):
         sub = np.where(idx >= 0, idx * c + r, -1)
         out[:, :, :, r::c] = np.repeat(sub, c, axis=2)
     return out, cnt
+
+
+def row_peak(qt, kt, topk_idx, vbs, sm_scale: float, units):
+    """Row peakedness over the row's selected keys ([INT8-WAN] Dynamic
+    Sparsity Budgeting via Softmax Normalizer Registers: with m the row's
+    largest logit and l = sum_x exp(s_x - m), max_prob = 1 / l is the row's
+    largest softmax weight).
+
+    units: flat indices (b * heads + h) * N + i.  Returns (max_prob, lse),
+    each [len(units), 64] float64; a row with no key has max_prob 0 and
+    lse -inf."""
+    q, k = _bf16_to_f64(qt), _bf16_to_f64(kt)
+    vbs = _i32(vbs)
+    B, S, heads, D = q.shape
+    N = S // 64
+    units = np.asarray(units, np.int64)
+    max_prob = np.zeros((len(units), 64))
+    lse = np.full((len(units), 64), -np.inf)
+    for n, u in enumerate(units):
+        b, h, i = u // (heads * N), (u // N) % heads, u % N
+        keys = [64 * j + s for j in topk_idx[b, h, i] if 0 <= j < N for s in range(vbs[j])]
+        if not keys:
+            continue
+        logits = sm_scale * q[b, 64 * i: 64 * i + 64, h] @ k[b, keys, h].T  # [64, n_keys]
+        m = logits.max(axis=1)
+        l = np.exp(logits - m[:, None]).sum(axis=1)
+        max_prob[n] = 1.0 / l
+        lse[n] = m + np.log(l)
+    return max_prob, lse
+
+
+def captured_mass(lse_selected, lse_all) -> np.ndarray:
+    """The share of a row's full (dense) softmax mass that falls on its
+    selected keys, sum_{x selected} exp(s_x) / sum_{all x} exp(s_x) =
+    exp(lse_selected - lse_all): the recall of a selection against dense
+    attention ([INT8-WAN] Selection Heuristic Ablation and Recall Analysis).
+    A row with no selected key captures 0."""
+    a = np.asarray(lse_selected, np.float64)
+    b = np.asarray(lse_all, np.float64)
+    with np.errstate(invalid="ignore"):
+        return np.where(np.isneginf(a), 0.0, np.exp(a - b))
+
+
+def rel_l1(approx, ref) -> float:
+    """Mean absolute error over the mean absolute reference value ([INT8-WAN]
+    glossary: relative-L1, the quality gate of the sparse lever)."""
+    approx = np.asarray(approx, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.abs(approx - ref).mean() / np.abs(ref).mean())
 
 
 def default_threads() -> int:

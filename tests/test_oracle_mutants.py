@@ -75,6 +75,7 @@ def test_planted_mistake_is_caught(name, tmp_path):
 # of the module source, the mutated function patched in, its pins must fail.
 import test_oracle_block_select as tb  # noqa: E402
 import test_oracle_coarse_attn as tca  # noqa: E402
+import test_oracle_quality as tq  # noqa: E402
 
 PY_SRC = os.path.join(os.path.dirname(oracle.__file__), "__init__.py")
 
@@ -112,6 +113,15 @@ PY_MUTANTS = {
     "cube_lut_neighbouring_blocks": (
         "blocks_to_cube_lut", ("sub = np.where(idx >= 0, idx * c + r, -1)", "sub = np.where(idx >= 0, idx + r, -1)"),
         [tb.test_block_table_to_cube_table_by_hand, tb.test_block_sparse_attention_is_dense_attention_over_kept_blocks]),
+    "max_prob_is_the_normaliser": (
+        "row_peak", ("max_prob[n] = 1.0 / l", "max_prob[n] = l"),
+        [tq.test_equal_logits_spread_evenly]),
+    "max_prob_without_the_row_max": (
+        "row_peak", ("l = np.exp(logits - m[:, None]).sum(axis=1)", "l = np.exp(logits).sum(axis=1)"),
+        [tq.test_row_peak_lse_agrees_with_the_fine_stage]),
+    "captured_mass_inverted": (
+        "captured_mass", ("np.exp(a - b)", "np.exp(b - a)"),
+        [tq.test_captured_mass_is_the_dense_weight_of_the_selection]),
     "fine_counts_ignores_counts": (
         "fine_counts", ("idx2[:, :, :N] = np.where(np.arange(k)[None, None, None, :] < c[..., None], topk_idx, N)",
                         "idx2[:, :, :N] = topk_idx"),
