@@ -48,6 +48,30 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} not exported"
 
 
+def test_plain_c_program_links_against_the_abi(lib, tmp_path):
+    """The header is valid C99 and a C program links every entry point from
+    the shared library (it calls only the host-side status strings)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = ['#include <stdio.h>', '#include "vsa.h"', "int main(void) {",
+           "    typedef void (*fn_t)(void);",
+           "    const fn_t fns[] = {" + ", ".join(f"(fn_t)&{n}" for n in names) + "};",
+           "    for (unsigned i = 0; i < sizeof fns / sizeof fns[0]; ++i) if (!fns[i]) return 1;",
+           '    printf("%s %s\\n", vsa_status_string(VSA_OK), vsa_status_string(VSA_ERR_TIMEOUT));',
+           "    return 0;", "}"]
+    c_file = tmp_path / "abi.c"
+    c_file.write_text("\n".join(src) + "\n")
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(vbuild.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER), str(c_file),
+                    "-o", str(exe), "-L", libdir, "-lvsa", f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.split() == ["VSA_OK", "VSA_ERR_TIMEOUT"], (r.stdout, r.stderr)
+
+
 def test_status_strings(lib):
     for code, name in enumerate(["VSA_OK", "VSA_ERR_INVALID_ARG", "VSA_ERR_UNSUPPORTED", "VSA_ERR_ALIGNMENT",
                                  "VSA_ERR_INDEX_RANGE", "VSA_ERR_TIMEOUT", "VSA_ERR_CUDA"]):
