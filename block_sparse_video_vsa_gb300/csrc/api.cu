@@ -1,6 +1,7 @@
 // C ABI of the VSA library: argument validation on the host, then dispatch
-// to the kernels of tile.cu, coarse.cu and fine.cu.  See include/vsa.h for
-// the contract of each entry point.
+// to the kernels of tile.cu, coarse.cu, pair.cu, fine.cu and coarse_attn.cu
+// (coarse_noalloc.cu holds the allocation-free coarse entry point).  See
+// include/vsa.h for the contract of each entry point.
 #include <math.h>
 #include <string.h>
 

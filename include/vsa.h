@@ -40,6 +40,10 @@
  *     unless stated) and the stream.  The library allocates no memory.
  *     Every call is asynchronous on `stream`; results are ready when the
  *     stream reaches that point.
+ *   - Host threads: entry points may be called from several host threads at
+ *     once, on any streams; the only state they share is a per-device
+ *     context set up once under a lock and the launch counter (atomic).
+ *     vsa_coarse_select_noalloc's device scratch is the exception (see there).
  *   - Alignment: device pointers must be 16-byte aligned.
  *   - Errors: argument checks run on the host before any launch and return a
  *     status without touching memory.  Launch failures return VSA_ERR_CUDA.
