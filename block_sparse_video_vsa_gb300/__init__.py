@@ -25,6 +25,7 @@ __all__ = [
     "VsaError", "library", "num_cubes", "tile", "untile", "coarse_workspace_bytes", "coarse_select",
     "sparse_attn_fwd", "validate_indices", "device_error", "debug_wait_timeout", "pipeline",
     "coarse_attn", "coarse_attn_workspace_bytes", "pair_cubes", "pair_workspace_bytes", "kernel_launches",
+    "table_from_csr",
 ]
 
 _STATUS = {0: "VSA_OK", 1: "VSA_ERR_INVALID_ARG", 2: "VSA_ERR_UNSUPPORTED", 3: "VSA_ERR_ALIGNMENT",
@@ -87,6 +88,8 @@ def _declare(lib):
     lib.vsa_coarse_attn_workspace_bytes.argtypes = [_i32] * 4
     lib.vsa_coarse_attn.restype = ctypes.c_int
     lib.vsa_coarse_attn.argtypes = [_p, _p, _p, _p, _i32, _i32, _i32, _i32, ctypes.c_float, _p, _p, _p]
+    lib.vsa_table_from_csr.restype = ctypes.c_int
+    lib.vsa_table_from_csr.argtypes = [_p, _p, ctypes.c_int64, _i32, _p, _p]
     lib.vsa_kernel_launches.restype = ctypes.c_uint64
     lib.vsa_kernel_launches.argtypes = []
     return lib
@@ -330,6 +333,25 @@ def validate_indices(topk_idx, vbs, stream=None) -> int:
     _check(library().vsa_validate_indices(topk_idx.data_ptr(), vbs.data_ptr(), B, heads, N, topk,
                                           flag.data_ptr(), _stream(stream)), "vsa_validate_indices")
     return int(flag.item())
+
+
+def table_from_csr(lut_ptr, kv_idx, width: int, shape=None):
+    """Host-side: a compressed-row block table (int64 offsets `lut_ptr`
+    [rows + 1], int32 indices `kv_idx`) -> (table int32 [rows, width] with -1
+    after each row's entries, counts int32 [rows]), as numpy arrays; `shape`
+    (B, heads, ncubes) reshapes them for sparse_attn_fwd(..., counts=...)."""
+    import numpy as np
+    lut_ptr = np.ascontiguousarray(lut_ptr, dtype=np.int64)
+    kv_idx = np.ascontiguousarray(kv_idx, dtype=np.int32)
+    rows = lut_ptr.shape[0] - 1
+    table = np.empty((max(rows, 0), width), np.int32)
+    counts = np.empty((max(rows, 0),), np.int32)
+    _check(library().vsa_table_from_csr(lut_ptr.ctypes.data, kv_idx.ctypes.data if kv_idx.size else None, rows,
+                                        int(width), table.ctypes.data, counts.ctypes.data), "vsa_table_from_csr")
+    if shape is not None:
+        table = table.reshape(tuple(shape) + (width,))
+        counts = counts.reshape(tuple(shape))
+    return table, counts
 
 
 def kernel_launches() -> int:

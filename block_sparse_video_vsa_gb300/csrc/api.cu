@@ -277,4 +277,24 @@ vsa_status vsa_debug_wait_timeout(int64_t limit_ns, int32_t* dev_result, vsa_str
 
 uint64_t vsa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
+vsa_status vsa_table_from_csr(const int64_t* lut_ptr, const int32_t* kv_idx, int64_t rows, int32_t width,
+                              int32_t* table, int32_t* counts) {
+    if (!lut_ptr || !table || !counts || rows <= 0 || width <= 0) return VSA_ERR_INVALID_ARG;
+    if (lut_ptr[0] != 0) return VSA_ERR_INVALID_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        const int64_t n = lut_ptr[r + 1] - lut_ptr[r];
+        if (n < 0 || n > width) return VSA_ERR_INVALID_ARG;
+    }
+    if (lut_ptr[rows] > 0 && !kv_idx) return VSA_ERR_INVALID_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        const int64_t b = lut_ptr[r];
+        const int32_t n = (int32_t)(lut_ptr[r + 1] - b);
+        int32_t* row = table + r * (int64_t)width;
+        for (int32_t e = 0; e < n; ++e) row[e] = kv_idx[b + e];
+        for (int32_t e = n; e < width; ++e) row[e] = -1;
+        counts[r] = n;
+    }
+    return VSA_OK;
+}
+
 }  // extern "C"

@@ -337,6 +337,26 @@ vsa_status vsa_debug_wait_timeout(int64_t limit_ns, int32_t* dev_result, vsa_str
  */
 uint64_t vsa_kernel_launches(void);
 
+/*
+ * HOST-side conversion of a block table in compressed-row form ([VSA-AMD]
+ * Block-Sparse Encoding: the K/V block indices of all query blocks in one
+ * array, with per-row offsets and a per-row number of valid blocks) into the
+ * padded table and counts that vsa_sparse_attn_fwd_ex takes.  All pointers
+ * are host memory; synchronous; no CUDA call.
+ *   lut_ptr : int64 [rows + 1], lut_ptr[0] = 0, non-decreasing: row r owns
+ *             kv_idx[lut_ptr[r] .. lut_ptr[r + 1])
+ *   kv_idx  : int32 [lut_ptr[rows]] (may be NULL when that is 0)
+ *   rows    : B * heads * ncubes, in the row order of topk_idx
+ *   width   : the table width (topk); every row must hold <= width entries
+ *   table   : int32 [rows, width] (written): each row's entries, then -1
+ *   counts  : int32 [rows] (written): lut_ptr[r + 1] - lut_ptr[r]
+ * Returns VSA_ERR_INVALID_ARG (and writes nothing) on a null pointer,
+ * non-positive sizes, lut_ptr[0] != 0, a decreasing offset or a row longer
+ * than width.
+ */
+vsa_status vsa_table_from_csr(const int64_t* lut_ptr, const int32_t* kv_idx, int64_t rows, int32_t width,
+                              int32_t* table, int32_t* counts);
+
 #ifdef __cplusplus
 }
 #endif

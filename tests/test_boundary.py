@@ -39,7 +39,7 @@ def test_header_declares_the_entry_points():
               "vsa_validate_indices", "vsa_device_error", "vsa_debug_wait_timeout",
               "vsa_pair_cubes", "vsa_pair_workspace_bytes", "vsa_sparse_attn_fwd_paired",
               "vsa_sparse_attn_fwd_ex", "vsa_sparse_attn_fwd_gated", "vsa_coarse_attn",
-              "vsa_coarse_attn_workspace_bytes", "vsa_kernel_launches"):
+              "vsa_coarse_attn_workspace_bytes", "vsa_kernel_launches", "vsa_table_from_csr"):
         assert n in names
 
 
@@ -202,3 +202,31 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros((1, 300, 2, 64), dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         vsa.tile(x, (1, 5, 6, 10))
+
+
+def test_table_from_csr_matches_the_padded_layout():
+    import numpy as np
+    rng = np.random.default_rng(3)
+    B, heads, N, width = 1, 3, 7, 5
+    rows = B * heads * N
+    lengths = rng.integers(0, width + 1, size=rows)
+    lengths[:2] = [0, width]
+    lut_ptr = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    kv_idx = rng.integers(0, N, size=int(lut_ptr[-1])).astype(np.int32)
+    table, counts = vsa.table_from_csr(lut_ptr, kv_idx, width, shape=(B, heads, N))
+    assert table.shape == (B, heads, N, width) and counts.shape == (B, heads, N)
+    flat, cnt = table.reshape(rows, width), counts.reshape(rows)
+    for r in range(rows):
+        assert cnt[r] == lengths[r]
+        assert flat[r, :lengths[r]].tolist() == kv_idx[lut_ptr[r]:lut_ptr[r + 1]].tolist()
+        assert (flat[r, lengths[r]:] == -1).all()
+
+
+def test_table_from_csr_refuses_bad_offsets(lib):
+    import numpy as np
+    ok_idx = np.zeros(8, np.int32)
+    for bad in ([1, 2, 3], [0, 3, 2], [0, 9, 9]):  # nonzero start, decreasing, row longer than width
+        with pytest.raises(vsa.VsaError):
+            vsa.table_from_csr(np.array(bad, np.int64), ok_idx, 4)
+    table, counts = vsa.table_from_csr(np.array([0, 0, 0], np.int64), np.zeros(0, np.int32), 2)
+    assert (table == -1).all() and (counts == 0).all()
