@@ -92,6 +92,15 @@ WORKLOADS = {
 }
 OUTLIER_TOPKS = (187, 78, 31)
 
+# Token sequences attended in contiguous 128-token blocks (no cube tiling):
+# the Wan2.1-shape attention call of "VSA: Accelerating Video Diffusion
+# Inference with Sparse Attention on AMD GPUs" (q, k, v [1, 12, 32768, 128]).
+# Its fields are those of the 21 x 30 x 52 grid flattened in raster order
+# (32,760 tokens), zero-padded to 32,768.
+SEQUENCE_WORKLOADS = {
+    "blocks128": (Workload("blocks128", 1, 21, 30, 52, heads=12, D=128, topk=1, seed=1005), 32768),
+}
+
 V_SCALE = 0.05  # beta
 NOISE = 0.3
 N_MODES = 32
@@ -221,4 +230,22 @@ def window_topk(cube_grid: Sequence[int], radius: Sequence[int], B: int, heads: 
                 ids = [((a * nh + b2) * nw + c) for a in range(t0, t0 + kt)
                        for b2 in range(h0, h0 + kh) for c in range(w0, w0 + kw)]
                 out[:, :, (ct * nh + ch) * nw + cw] = np.asarray(ids, np.int32)
+    return out
+
+
+def make_sequence_inputs(name: str):
+    """Raster-order q, k, v of a SEQUENCE_WORKLOADS entry, zero-padded to its
+    sequence length: dict(q, k, v) of bf16 bits [B, S, heads, D] plus
+    `real` (tokens before the padding) and `vbs` (int32 per 64-token slot
+    group: 64, then the real tokens of the last groups)."""
+    wl, s_len = SEQUENCE_WORKLOADS[name]
+    d = make_inputs(wl)
+    real = wl.tokens
+    assert s_len % 128 == 0 and s_len >= real
+    out = {"real": real}
+    for n in ("q", "k", "v"):
+        x = np.zeros((wl.B, s_len, wl.heads, wl.D), np.uint16)
+        x[:, :real] = d[n]
+        out[n] = x
+    out["vbs"] = np.clip(real - 64 * np.arange(s_len // 64), 0, 64).astype(np.int32)
     return out
