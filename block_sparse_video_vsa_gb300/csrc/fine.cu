@@ -9,36 +9,44 @@
 // and Sparse Traversal: walk the query block's K/V block list only).
 //
 // sm_103a design (5th-generation tensor cores, TMEM, TMA):
-//  * A work unit is a PAIR of query cubes (2p, 2p+1) of one (batch, head):
-//    128 query rows, one per TMEM lane.  It walks the union of the two cubes'
-//    selected key cubes, two key cubes (128 keys) per step:
-//        S[128 q x 128 keys]  = Q_pair . K_pair^T      (A = Q in TMEM)
-//        O[128 q x D]        += P . V_pair            (A = P in TMEM)
+//  * A work unit is a PAIR of query cubes of one (batch, head): 128 query
+//    rows, one per TMEM lane.  It walks the sorted union of the two cubes'
+//    selected key cubes, two key cubes (128 keys) per step g:
+//        S[128 q x 128 keys]  = Q_pair . K_pair(g)^T    (A = Q in TMEM)
+//        O_{g&1}[128 q x D]  += P(g) . V_pair(g)        (A = P in TMEM)
 //    Both MMAs are M = 128, N = 128 (full tensor-core rate; an M x 64 MMA runs
-//    at half rate), and only the B operands (K, V) are read from shared
-//    memory, which keeps shared-memory bandwidth to about half of its peak.
+//    at half rate), and only the B operands (K, V) come from shared memory.
 //    Query rows of a cube that did not select a key cube get probability 0
 //    for it, so each row attends exactly its own selection.
+//  * Two softmax groups of four warps (one thread per query row) take the
+//    steps in turn: group 0 the even global steps, group 1 the odd ones.
+//    Each group keeps its own running max and sum and accumulates into its
+//    own O (O_0, O_1 in TMEM); the two partial results are merged once per
+//    unit in the epilogue.  So the two groups' softmax work overlaps, and no
+//    row statistics pass between steps of different groups.
+//  * Two warps issue the MMAs: one the Q.K^T stream (QK(g) as soon as S is
+//    free and K has landed), one the P.V stream (PV(g) as soon as P and V
+//    are ready), so the tensor pipe takes each as early as it can.  Ordering
+//    between the streams is explicit: per-group barriers report each P.V's
+//    completion (the softmax writes P(g) once P.V(g - 1) has read P, and
+//    rescales its O once P.V(g - 2) has added into it), and a per-unit
+//    barrier reports that every P.V of the unit has completed (epilogue).
 //  * Persistent grid, one CTA per SM, units dealt round-robin in head-major
 //    order so one head's K/V stays in L2.
 //  * Warp roles (384 threads): warp 0 builds each unit's union list (sorted,
 //    with membership bits and vbs) and is the TMA producer of K; warp 1 owns
-//    TMEM and issues the Q.K^T MMAs; warp 2 is the TMA producer of V; warp 3
-//    issues the P.V MMAs; warps 4..11 run the softmax and stage Q into TMEM.
-//    Each MMA-issuing warp runs its loop as a whole warp and lets lane 0
-//    issue, so its waits and loop state stay warp-uniform.  A query row is
-//    shared by two threads (two warps on the same TMEM lane quarter), one per
-//    key cube of the step; they exchange their row maxima through shared
-//    memory with a 64-thread named barrier, so the running max, the sum and
-//    the lazy rescale of the row's O need no wider synchronisation.
-//  * TMEM (512 columns): S double buffer [0,128) [128,256); P of the current
-//    step (bf16 pairs) [256,320); Q of the current unit [320,384); O
-//    [384,512).  The softmax releases an S buffer as soon as it has loaded
-//    it, so QK runs two steps ahead of PV; P has its own columns, rewritten
-//    for step g + 1 only after PV(g) completes.
-//  * Running max kept in log2 units; O and the sum are rescaled only when a
-//    row's max grows by more than kRescaleThreshold, so exp2 arguments stay
-//    <= the threshold and logits of any finite size are safe.
+//    TMEM and issues Q.K^T; warp 2 is the TMA producer of V; warp 3 issues
+//    P.V; warps 4..7 and 8..11 are the two softmax groups (warp w serves
+//    TMEM lane quarter w % 4).  The group that takes the next unit's first
+//    step stages that unit's Q into TMEM once the current unit's last Q.K^T
+//    has completed.  The first warpgroup hands registers to the softmax
+//    warpgroups (setmaxnreg), which hold a step's 128 logits per thread.
+//  * TMEM (512 columns): S [0,128); P (bf16 pairs) [128,192); Q [192,256);
+//    O_0 [256,384); O_1 [384,512).  The softmax frees S as soon as it has
+//    loaded it, so Q.K^T(g + 1) runs while the softmax of step g works.
+//  * Running max kept in log2 units; a group's O and sum are rescaled only
+//    when a row's max grows by more than kRescaleThreshold, so exp2 arguments
+//    stay <= the threshold and logits of any finite size are safe.
 //  * Every wait is bounded; a wait that runs out raises a CTA abort flag and
 //    the device error word, and each role winds down without deadlock.
 #include <cuda_bf16.h>
@@ -52,10 +60,22 @@ namespace {
 
 constexpr int kKStages = 3;           // K pair slots (QK operand B)
 constexpr int kVStages = 3;           // V pair slots (PV operand B)
-constexpr int kSoftmaxWarps = 8;
+constexpr int kGroupWarps = 4;        // softmax warps per group (one per TMEM lane quarter)
 constexpr int kFirstSoftmaxWarp = 4;
-constexpr int kThreads = (kFirstSoftmaxWarp + kSoftmaxWarps) * 32;  // 12 warps
+constexpr int kThreads = (kFirstSoftmaxWarp + 2 * kGroupWarps) * 32;  // 12 warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Registers per thread: the kernel is compiled for kLaunchRegs (the most 384
+// threads can have); right after setup the first warpgroup (list builder,
+// producers, MMA issuer) gives registers back and the two softmax
+// warpgroups take them (setmaxnreg), so a softmax thread can hold a step's
+// 128 logits.  The shares add up to the launch's total exactly:
+// 128 * kProducerRegs + 256 * kSoftmaxRegs <= 384 * kLaunchRegs (a larger
+// sum would leave setmaxnreg.inc waiting forever); the launcher checks that
+// the kernel was compiled with exactly kLaunchRegs.
+constexpr int kLaunchRegs = 168;
+constexpr int kProducerRegs = 72;
+constexpr int kSoftmaxRegs = 216;
+static_assert(128 * kProducerRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kMaxTopk = 512;
 constexpr int kMaxUnion = 2 * kMaxTopk;
@@ -63,10 +83,11 @@ constexpr int kMaxCubes = 8192;
 constexpr int kBitmapWords = kMaxCubes / 32;
 
 // TMEM columns.
-constexpr int kTmemS = 0;    // two S buffers of 128 columns
-constexpr int kTmemP = 256;  // P of the current step: 128 keys as 64 columns of bf16 pairs
-constexpr int kTmemQ = 320;  // Q of the current unit: D bf16 as D/2 columns of pairs
-constexpr int kTmemO = 384;  // O accumulator (D columns)
+constexpr int kTmemS = 0;     // S of the current step (128 fp32 columns)
+constexpr int kTmemP = 128;   // P: 128 keys as 64 columns of bf16 pairs
+constexpr int kTmemQ = 192;   // Q of the current unit: D bf16 as D/2 columns of pairs
+constexpr int kTmemO0 = 256;  // O of group 0 (D columns)
+constexpr int kTmemO1 = 384;  // O of group 1
 
 // Shared-memory layout (bytes from a 1024-aligned base).
 constexpr int kChunkRows64 = 64 * 128;           // 64 rows x 128 B   = 8 KB
@@ -89,18 +110,20 @@ struct __align__(16) Misc {
     uint64_t k_empty[kKStages];
     uint64_t v_full[kVStages];
     uint64_t v_empty[kVStages];
-    uint64_t s_full[2];
-    uint64_t s_free[2];
-    uint64_t p_full;
-    uint64_t pv_done;
-    uint64_t q_full;
-    uint64_t q_empty;
+    uint64_t s_full[2];   // per softmax group: S of the group's next step is ready
+    uint64_t s_free;      // S has been loaded into registers
+    uint64_t p_full;      // P (and any O rescale) of the step is in TMEM
+    uint64_t pv_grp[2];   // per softmax group: P.V of the group's step has completed
+    uint64_t unit_done;   // every P.V of the unit has completed
+    uint64_t q_full;      // the unit's Q is in TMEM
+    uint64_t q_empty;     // the unit's Q.K^T MMAs have completed
+    uint64_t o_free;      // the unit's O_0 and O_1 have been read by the epilogue
     uint64_t list_full[2];
     uint64_t list_empty[2];
-    uint64_t drain[2];  // per MMA-issuing warp
+    uint64_t drain[2];    // per MMA-issuing warp
     int list_count[2];
-    float xmax[2][2][128];        // [step parity][key half][row]: row maxima exchanged by thread pairs
-    float xsum[2][128];           // [key half][row]: partial row sums for the epilogue
+    float xm[2][2][128];  // [unit parity][group][row]: running max at the unit's end
+    float xl[2][2][128];  // [unit parity][group][row]: sum at the unit's end
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -146,6 +169,14 @@ __device__ __forceinline__ void unit_cubes(const FineParams& p, int b, int h, in
     }
     if (i0 >= p.N) i0 = -1;
     if (i1 >= p.N) i1 = -1;
+}
+
+// Query cube of row r (0..127) of unit u, or -1.
+__device__ __forceinline__ int row_cube(const FineParams& p, int u, int r, int& b, int& h) {
+    int pair, i0, i1;
+    unit_coords(u, p, b, h, pair);
+    unit_cubes(p, b, h, pair, i0, i1);
+    return (r >> 6) ? i1 : i0;
 }
 
 // Builds the sorted union of the two query cubes' selections (one warp).
@@ -230,24 +261,24 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t issued, unsi
     }
 }
 
-// Softmax threads: copy half `hf` of this thread's Q row (or zeros) into TMEM
-// Q buffer qb (D/2 elements = D/4 32-bit columns; D = 64 has one half only).
-__device__ __forceinline__ void stage_q(const FineParams& p, int u, int row_in_pair, uint32_t t_lane, int hf) {
-    int b, h, pair;
-    unit_coords(u, p, b, h, pair);
-    int i0, i1;
-    unit_cubes(p, b, h, pair, i0, i1);
-    const int i = (row_in_pair >> 6) ? i1 : i0;
-    const int D = p.D;
-    const int words = D / 2;  // 32-bit columns of a full row
-    uint32_t w[32];
-    for (int c0 = hf * 32; c0 < words && c0 < hf * 32 + 32; c0 += 32) {
-        if (i >= 0) {
-            const size_t row = (size_t)b * p.N * kCubeTokens + (size_t)i * kCubeTokens + (row_in_pair & 63);
-            const uint4* src = p.q + (row * p.heads + h) * (size_t)(D / 8) + c0 / 4;
+// Softmax thread of row r: copies its whole Q row of unit u (or zeros) into
+// the TMEM Q columns of its lane.
+template <int kD>
+__device__ __forceinline__ void stage_q(const FineParams& p, int u, int r, uint32_t t_lane) {
+    int b, h;
+    const int i = row_cube(p, u, r, b, h);
+    const uint4* src = nullptr;
+    if (i >= 0) {
+        const size_t row = (size_t)b * p.N * kCubeTokens + (size_t)i * kCubeTokens + (r & 63);
+        src = p.q + (row * p.heads + h) * (size_t)(kD / 8);
+    }
+#pragma unroll
+    for (int c0 = 0; c0 < kD / 2; c0 += 32) {
+        uint32_t w[32];
+        if (src) {
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
-                const uint4 x = __ldg(src + v);
+                const uint4 x = __ldg(src + c0 / 4 + v);
                 w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
             }
         } else {
@@ -259,6 +290,18 @@ __device__ __forceinline__ void stage_q(const FineParams& p, int u, int row_in_p
     tmem_wait_st();
 }
 
+// Brings row r's Q row of unit u into L2 ahead of stage_q.
+template <int kD>
+__device__ __forceinline__ void prefetch_q(const FineParams& p, int u, int r) {
+    int b, h;
+    const int i = row_cube(p, u, r, b, h);
+    if (i < 0) return;
+    const size_t row = (size_t)b * p.N * kCubeTokens + (size_t)i * kCubeTokens + (r & 63);
+    const uint4* src = p.q + (row * p.heads + h) * (size_t)(kD / 8);
+#pragma unroll
+    for (int c = 0; c < kD * 2; c += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + c / 16));
+}
+
 __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -267,6 +310,39 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
+}
+
+// Maximum of x[0..63]: four running three-input max chains (few temporaries
+// beside the 128 live logits of the step).
+__device__ __forceinline__ float max64(const float* x) {
+    float a[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+    for (int c = 4; c < 60; c += 8)  // keys 4 .. 59
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[j] = max3(a[j], x[c + j], x[c + 4 + j]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a[j] = fmaxf(a[j], x[60 + j]);  // keys 60 .. 63
+    return fmaxf(max3(a[0], a[1], a[2]), a[3]);
+}
+
+// p = exp2(x * c2 - mb) for 64 keys, packed as 32 bf16 pairs; adds the
+// fp32 values to l.  Packed two-wide fp32 FMA and add (the same roundings as
+// the scalar forms, half the instructions).
+__device__ __forceinline__ void exp64(const float* x, float c2, float mb, uint32_t* pk, float& l) {
+    const float2 c2v = make_float2(c2, c2), nmb = make_float2(-mb, -mb);
+    float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < 64; c += 4) {
+        const float2 a01 = __ffma2_rn(make_float2(x[c], x[c + 1]), c2v, nmb);
+        const float2 a23 = __ffma2_rn(make_float2(x[c + 2], x[c + 3]), c2v, nmb);
+        const float p0 = ex2_approx(a01.x), p1 = ex2_approx(a01.y);
+        const float p2 = ex2_approx(a23.x), p3 = ex2_approx(a23.y);
+        s01 = __fadd2_rn(s01, make_float2(p0, p1));
+        s23 = __fadd2_rn(s23, make_float2(p2, p3));
+        pk[c >> 1] = pack_bf16x2(p0, p1);
+        pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+    }
+    l += (s01.x + s01.y) + (s23.x + s23.y);
 }
 
 template <int kD, bool kGated>
@@ -301,14 +377,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&ms.s_full[s]), 1);
-            mbar_init(smem_u32(&ms.s_free[s]), kSoftmaxWarps);
             mbar_init(smem_u32(&ms.list_full[s]), 1);
-            mbar_init(smem_u32(&ms.list_empty[s]), 1 + 1 + kSoftmaxWarps);  // V producer, MMA, softmax warps
+            mbar_init(smem_u32(&ms.list_empty[s]), 1 + 2 + 2 * kGroupWarps);  // V producer, MMA warps, softmax
         }
-        mbar_init(smem_u32(&ms.p_full), kSoftmaxWarps);
-        mbar_init(smem_u32(&ms.pv_done), 1);
-        mbar_init(smem_u32(&ms.q_full), kSoftmaxWarps);
+        mbar_init(smem_u32(&ms.s_free), kGroupWarps);
+        mbar_init(smem_u32(&ms.p_full), kGroupWarps);
+        mbar_init(smem_u32(&ms.pv_grp[0]), 1);
+        mbar_init(smem_u32(&ms.pv_grp[1]), 1);
+        mbar_init(smem_u32(&ms.unit_done), 1);
+        mbar_init(smem_u32(&ms.q_full), kGroupWarps);
         mbar_init(smem_u32(&ms.q_empty), 1);
+        mbar_init(smem_u32(&ms.o_free), 2 * kGroupWarps);
         mbar_init(smem_u32(&ms.drain[0]), 1);
         mbar_init(smem_u32(&ms.drain[1]), 1);
         ms.abort_flag = 0;
@@ -334,6 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ms.tmem_base;
 
+    if (warp < kFirstSoftmaxWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (warp == 0) {
         // ================================ union lists + TMA producer of K
         const uint64_t pol = l2_policy_evict_last();
@@ -409,15 +490,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1 || warp == 3) {
         // ============================================================ MMA issuers
-        // Two warps issue MMAs, each warp-wide with lane 0 issuing and
-        // committing: warp 1 the QK stream, warp 3 the PV stream.  The streams
-        // touch disjoint TMEM (S vs P and O) and are ordered only through the
-        // softmax: QK(g) writes S buffer g & 1 once the softmax has loaded
-        // S(g - 2) from it (so QK runs up to two steps ahead of the softmax),
-        // and PV(g) reads P(g), which the softmax writes once PV(g - 1) has
-        // completed.  Descriptors are precomputed; each MMA adds a constant to
-        // the start-address field of the low word (no carry: shared addresses
-        // are below 256 KB).
+        // Two warps issue MMAs: warp 1 the Q.K^T stream (QK(g) as soon as S is
+        // free and K has landed), warp 3 the P.V stream (PV(g) as soon as P
+        // and V are ready), so the tensor pipe takes each as early as it can.
+        // Each runs its loop as a whole warp and lets lane 0 issue and commit
+        // (always the same thread, so its commits cover all of its MMAs).
+        // The streams touch disjoint TMEM (S vs P and O) and are ordered only
+        // through the softmax's barriers.  Descriptors are precomputed; each
+        // MMA adds a constant to the start-address field of the low word (no
+        // carry: shared addresses are below 256 KB).
         if (my_units > 0) {
             const uint32_t hi = (uint32_t)(smem_desc_sw128(0, 16, 1024) >> 32);  // SBO, version, swizzle
             bool ok = true;
@@ -428,111 +509,125 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return -1;
                 return __shfl_sync(0xffffffffu, ms.list_count[ul & 1], 0);
             };
+            uint32_t g = 0;  // global step at the start of the unit
             if (warp == 1) {
                 const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
                 const uint32_t lo_k = (uint32_t)smem_desc_sw128(sbase + kOffK, 16, 1024);
                 constexpr int ksteps_qk = D / 16;
-                uint32_t gq = 0;  // QK step (global)
                 for (int ul = 0; ul < my_units && ok; ++ul) {
                     const int cnt = list_count(ul);
                     if (cnt < 0) break;
                     const int nst = (cnt + 1) >> 1;
                     ok = mbar_wait_bounded(smem_u32(&ms.q_full), ul & 1, abort_flag, p.err, kWaitLimitNs);
-                    for (int t = 0; t < nst && ok; ++t, ++gq) {
-                        if (gq >= 2)
-                            ok = mbar_wait_bounded(smem_u32(&ms.s_free[gq & 1]), ((gq >> 1) + 1) & 1, abort_flag,
-                                                   p.err, kWaitLimitNs);
-                        const int slot = gq % kKStages;
+                    for (int t = 0; t < nst && ok; ++t) {
+                        const uint32_t gs = g + t;
+                        if (gs >= 1)  // S of the previous step is in registers
+                            ok = mbar_wait_bounded(smem_u32(&ms.s_free), (gs - 1) & 1, abort_flag, p.err,
+                                                   kWaitLimitNs);
+                        const int slot = gs % kKStages;
                         if (ok)
-                            ok = mbar_wait_bounded(smem_u32(&ms.k_full[slot]), (gq / kKStages) & 1, abort_flag,
+                            ok = mbar_wait_bounded(smem_u32(&ms.k_full[slot]), (gs / kKStages) & 1, abort_flag,
                                                    p.err, kWaitLimitNs);
                         if (!ok) break;
                         const uint32_t b0 = lo_k + ((uint32_t)(slot * kPairBytes) >> 4);
-                        const uint32_t a0 = tmem + kTmemQ;
-                        const uint32_t d_tmem = tmem + kTmemS + (gq & 1) * 128;
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < ksteps_qk; ++kk)
-                            mma_ts_warp(d_tmem, a0 + kk * 8,
+                            mma_ts_warp(tmem + kTmemS, tmem + kTmemQ + kk * 8,
                                         b0 + (((kk >> 2) * kChunkRows128 + (kk & 3) * 32) >> 4), hi, idesc_qk,
                                         kk > 0);
-                        mma_commit_warp(smem_u32(&ms.s_full[gq & 1]));
+                        mma_commit_warp(smem_u32(&ms.s_full[gs & 1]));
                         mma_commit_warp(smem_u32(&ms.k_empty[slot]));
                     }
-                    if (ok) mma_commit_warp(smem_u32(&ms.q_empty));  // the unit's Q is no longer read
+                    if (!ok) break;
+                    mma_commit_warp(smem_u32(&ms.q_empty));  // the unit's Q is no longer read
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[ul & 1]));
+                    g += nst;
                 }
             } else {
                 const uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
                 const uint32_t lo_v = (uint32_t)smem_desc_sw128(sbase + kOffV, kChunkRows128, 1024);
-                uint32_t g = 0;  // PV step (global)
                 for (int ul = 0; ul < my_units && ok; ++ul) {
                     const int cnt = list_count(ul);
                     if (cnt < 0) break;
                     const int nst = (cnt + 1) >> 1;
-                    for (int t = 0; t < nst && ok; ++t, ++g) {
-                        const int slot = g % kVStages;
-                        ok = mbar_wait_bounded(smem_u32(&ms.p_full), g & 1, abort_flag, p.err, kWaitLimitNs) &&
-                             mbar_wait_bounded(smem_u32(&ms.v_full[slot]), (g / kVStages) & 1, abort_flag, p.err,
+                    // The unit's O_0 and O_1 start over once the previous unit's
+                    // epilogue has read them (an empty unit waits too, so that
+                    // unit_done never runs two phases ahead of an epilogue).
+                    if (ul >= 1)
+                        ok = mbar_wait_bounded(smem_u32(&ms.o_free), (ul - 1) & 1, abort_flag, p.err, kWaitLimitNs);
+                    for (int t = 0; t < nst && ok; ++t) {
+                        const uint32_t gs = g + t;
+                        const int slot = gs % kVStages;
+                        ok = mbar_wait_bounded(smem_u32(&ms.p_full), gs & 1, abort_flag, p.err, kWaitLimitNs) &&
+                             mbar_wait_bounded(smem_u32(&ms.v_full[slot]), (gs / kVStages) & 1, abort_flag, p.err,
                                                kWaitLimitNs);
                         if (!ok) break;
                         const uint32_t b0 = lo_v + ((uint32_t)(slot * kPairBytes) >> 4);
-                        const uint32_t a0 = tmem + kTmemP;
+                        const uint32_t d_tmem = tmem + ((gs & 1) ? kTmemO1 : kTmemO0);
+                        const uint32_t acc = t >= 2 ? 1u : 0u;  // a group's first step of the unit overwrites its O
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ts_warp(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv,
-                                        (t > 0 || kk > 0));
+                            mma_ts_warp(d_tmem, tmem + kTmemP + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv,
+                                        acc | (kk > 0 ? 1u : 0u));
                         if (2 * t + 1 < cnt) {  // the second cube of the step (a single-cube step has 64 keys)
 #pragma unroll
                             for (int kk = 4; kk < 8; ++kk)
-                                mma_ts_warp(tmem + kTmemO, a0 + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv, 1u);
+                                mma_ts_warp(d_tmem, tmem + kTmemP + kk * 8, b0 + ((kk * 2048) >> 4), hi, idesc_pv,
+                                            1u);
                         }
-                        mma_commit_warp(smem_u32(&ms.pv_done));
+                        mma_commit_warp(smem_u32(&ms.pv_grp[gs & 1]));
                         mma_commit_warp(smem_u32(&ms.v_empty[slot]));
                     }
-                    // This issuer is done with the unit's list.
+                    if (!ok) break;
+                    mma_commit_warp(smem_u32(&ms.unit_done));  // every P.V of the unit
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[ul & 1]));
+                    g += nst;
                 }
             }
             // Drain: every MMA this warp issued completes before TMEM is released.
-            mma_commit_warp(smem_u32(&ms.drain[warp == 1 ? 0 : 1]));
-            if (lane == 0) mbar_wait_drain_1(smem_u32(&ms.drain[warp == 1 ? 0 : 1]), 0, p.err, kWaitLimitNs);
+            const uint32_t drain = smem_u32(&ms.drain[warp == 1 ? 0 : 1]);
+            mma_commit_warp(drain);
+            if (lane == 0) mbar_wait_drain_1(drain, 0, p.err, kWaitLimitNs);
         }
         __syncwarp();
-    } else if (warp >= kFirstSoftmaxWarp) {
+    }
+    } else {
         // ============================================================ softmax
-        const int sw = warp - kFirstSoftmaxWarp;  // 0..7
-        const int quarter = warp & 3;             // TMEM lane quarter
-        const int hf = sw >> 2;                   // key half of the step: cube 2t + hf
-        const int r = quarter * 32 + lane;        // query row of the pair (0..127)
-        const uint32_t my_bit = 1u << (r >> 6);   // membership bit of this row's cube
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+        const int G = (warp - kFirstSoftmaxWarp) / kGroupWarps;  // steps g with g % 2 == G
+        const int quarter = warp & 3;                             // TMEM lane quarter
+        const int r = quarter * 32 + lane;                        // query row of the pair (0..127)
+        const uint32_t my_bit = 1u << (r >> 6);                   // membership bit of this row's cube
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-        const int dh = D / 2;                     // O columns this thread owns: [hf * dh, hf * dh + dh)
+        const uint32_t o_mine = t_lane + (G ? kTmemO1 : kTmemO0);
         const float c2 = p.scale_log2;
         const float ninf = -INFINITY;
+        constexpr int dh = D / 2;  // output columns this thread writes: [G * dh, G * dh + dh)
         bool ok = true;
-        uint32_t g = 0;
-        if (my_units > 0) {
-            stage_q(p, blockIdx.x, r, t_lane, hf);
+        uint32_t g = 0;   // global step at the start of the current unit
+        uint32_t jg = 0;  // steps this group has taken (phase of s_full[G])
+        if (G == 0 && my_units > 0) {
+            stage_q<D>(p, blockIdx.x, r, t_lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ms.q_full));
         }
+#pragma unroll 1
         for (int ul = 0; ul < my_units; ++ul) {
             const int u = blockIdx.x + ul * gridDim.x;
             const int lb = ul & 1;
             if constexpr (kGated) {
                 // The epilogue reads this thread's half row of both gates (one
                 // 128-byte line each for D = 128): start bringing them into L2.
-                int b, h, pair;
-                unit_coords(u, p, b, h, pair);
-                int i0, i1;
-                unit_cubes(p, b, h, pair, i0, i1);
-                const int i = (r >> 6) ? i1 : i0;
+                int b, h;
+                const int i = row_cube(p, u, r, b, h);
                 if (i >= 0) {
                     const size_t gi = ((size_t)(b * s_pad + i * kCubeTokens + (r & 63)) * p.heads + h) *
-                                          (size_t)(D / 8) + hf * (dh / 8);
+                                          (size_t)(D / 8) + G * (dh / 8);
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(p.gc + gi));
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(p.gf + gi));
                 }
@@ -542,197 +637,215 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t* list = lists + lb * kMaxUnion;
             const int count = ok ? ms.list_count[lb] : 0;
             const int nst = (count + 1) >> 1;
-            // Stages the next unit's Q once this unit's Q is no longer read (its
-            // last QK has completed: after S of its last step, or at once for a
-            // unit with an empty union, which issues no QK).
-            auto stage_next_q = [&]() {
-                if (ul + 1 < my_units && ok) {
-                    ok = mbar_wait_bounded(smem_u32(&ms.q_empty), ul & 1, abort_flag, p.err, kWaitLimitNs);
-                    if (ok) {
-                        tc_fence_after();
-                        stage_q(p, u + gridDim.x, r, t_lane, hf);
-                        tc_fence_before();
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ms.q_full));
-                }
-            };
-            if (nst == 0) stage_next_q();
+            const uint32_t g0 = g;
+            // The group that takes the next unit's first step stages its Q.
+            const bool stager = (((g0 + nst) & 1) == (uint32_t)G) && ul + 1 < my_units;
+            if (stager) prefetch_q<D>(p, u + gridDim.x, r);
             float m = ninf, l = 0.f;
-            for (int t = 0; t < nst; ++t, ++g) {
-                const int e = 2 * t + hf;
-                const uint32_t ent = e < count ? list[e] : 0u;
-                const bool mem = (entry_mask(ent) & my_bit) != 0;  // warp-uniform (row cube)
-                const int vb = entry_vbs(ent);
-                const uint32_t sc = kTmemS + (g & 1) * 128;
-                if (ok) ok = mbar_wait_bounded(smem_u32(&ms.s_full[g & 1]), (g >> 1) & 1, abort_flag, p.err,
-                                               kWaitLimitNs);
+            bool first = true;
+#pragma unroll 1
+            for (int t = (int)((g0 + G) & 1); t < nst; t += 2) {
+                const uint32_t gs = g0 + t;
+                const uint32_t e0 = list[2 * t];
+                const uint32_t e1 = 2 * t + 1 < count ? list[2 * t + 1] : 0u;
+                const bool mem0 = (entry_mask(e0) & my_bit) != 0;  // warp-uniform (row cube)
+                const bool mem1 = (entry_mask(e1) & my_bit) != 0;
+                const int vb0 = entry_vbs(e0), vb1 = entry_vbs(e1);
+                if (ok) ok = mbar_wait_bounded(smem_u32(&ms.s_full[G]), jg & 1, abort_flag, p.err, kWaitLimitNs);
+                ++jg;
                 tc_fence_after();
-                if (t + 1 == nst) stage_next_q();
-                float x[64];
-                if (ok && mem) {
-                    tmem_ld32(t_lane + sc + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-                    tmem_ld32(t_lane + sc + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-                    tmem_wait_ld();
-                }
-                // S(g) is in registers: its buffer may take S(g + 2).
+                float x[128];
+                // All 128 columns are loaded whatever the membership (the
+                // unused half is never read; loading it keeps every value
+                // defined on every path, which the register allocator needs).
+#pragma unroll
+                for (int c = 0; c < 128; c += 32)
+                    tmem_ld32(t_lane + kTmemS + c, *reinterpret_cast<uint32_t(*)[32]>(&x[c]));
+                tmem_wait_ld();
+                // S(g) is in registers: the buffer may take S(g + 1).
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ms.s_free[g & 1]));
-                // Raw row maximum of this half (keys past vbs are -inf), then log2 units.
+                if (lane == 0) mbar_arrive(smem_u32(&ms.s_free));
+                // Raw row maximum over this row's keys (keys past vbs are -inf), then log2 units.
                 float lmax = ninf;
-                if (ok && mem) {
-                    if (vb < kCubeTokens) {
+                if (ok && mem0) {
+                    if (vb0 < kCubeTokens) {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) x[c] = c < vb ? x[c] : ninf;
+                        for (int c = 0; c < 64; ++c) x[c] = c < vb0 ? x[c] : ninf;
                     }
-                    float mm[22];
-#pragma unroll
-                    for (int j = 0; j < 21; ++j) mm[j] = max3(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
-                    mm[21] = x[63];
-#pragma unroll
-                    for (int j = 0; j < 7; ++j) mm[j] = max3(mm[3 * j], mm[3 * j + 1], mm[3 * j + 2]);
-                    lmax = c2 * max3(max3(mm[0], mm[1], mm[2]), max3(mm[3], mm[4], mm[5]), fmaxf(mm[6], mm[21]));
+                    lmax = max64(x);
                 }
-                // Row max over both key cubes of the step (thread pair exchange).
-                ms.xmax[g & 1][hf][r] = lmax;
-                named_sync(1 + quarter, 64);
-                const float rmax = fmaxf(lmax, ms.xmax[g & 1][hf ^ 1][r]);
-                // Lazy running max: rescale O and l only on a jump > threshold
-                // (both threads of the row take the same decision).
+                if (ok && mem1) {
+                    if (vb1 < kCubeTokens) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) x[64 + c] = c < vb1 ? x[64 + c] : ninf;
+                    }
+                    lmax = fmaxf(lmax, max64(x + 64));
+                }
+                lmax *= c2;
+                // Lazy running max: rescale O and l only on a jump > threshold.
                 float alpha = 1.f;
-                if (rmax > m + kRescaleThreshold) {
-                    alpha = (m == ninf) ? 0.f : ex2_approx(m - rmax);
-                    m = rmax;
+                if (lmax > m + kRescaleThreshold) {
+                    alpha = (m == ninf) ? 0.f : ex2_approx(m - lmax);
+                    m = lmax;
                     l *= alpha;
                 }
-                // P = exp2(x c2 - m) as bf16 pairs (this half's 32 P columns).
-                uint32_t pk[32];
-                if (ok && mem) {
-                    const float mb = (m == ninf) ? 0.f : m;
-                    // Packed two-wide fp32 FMA and add (the same roundings as the
-                    // scalar forms, half the instructions).
-                    const float2 c2v = make_float2(c2, c2), nmb = make_float2(-mb, -mb);
-                    float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int c = 0; c < 64; c += 4) {
-                        const float2 a01 = __ffma2_rn(make_float2(x[c], x[c + 1]), c2v, nmb);
-                        const float2 a23 = __ffma2_rn(make_float2(x[c + 2], x[c + 3]), c2v, nmb);
-                        const float p0 = ex2_approx(a01.x), p1 = ex2_approx(a01.y);
-                        const float p2 = ex2_approx(a23.x), p3 = ex2_approx(a23.y);
-                        s01 = __fadd2_rn(s01, make_float2(p0, p1));
-                        s23 = __fadd2_rn(s23, make_float2(p2, p3));
-                        pk[c >> 1] = pack_bf16x2(p0, p1);
-                        pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
-                    }
-                    l += (s01.x + s01.y) + (s23.x + s23.y);
+                // P = exp2(x c2 - m) as bf16 pairs: keys 0..63 in P columns
+                // [0, 32), keys 64..127 in [32, 64).
+                uint32_t pk[64];
+                const float mb = (m == ninf) ? 0.f : m;
+                if (ok && mem0) {
+                    exp64(x, c2, mb, pk, l);
                 } else {
 #pragma unroll
                     for (int c = 0; c < 32; ++c) pk[c] = 0u;
                 }
-                // PV(g - 1) has read the P columns and finished adding into O.
-                if (g > 0 && ok)
-                    ok = mbar_wait_bounded(smem_u32(&ms.pv_done), (g - 1) & 1, abort_flag, p.err, kWaitLimitNs);
+                if (ok && mem1) {
+                    exp64(x + 64, c2, mb, pk + 32, l);
+                } else {
+#pragma unroll
+                    for (int c = 32; c < 64; ++c) pk[c] = 0u;
+                }
+                // P.V(g - 1) (the other group's) has read the P columns.
+                if (gs > 0 && ok)
+                    ok = mbar_wait_bounded(smem_u32(&ms.pv_grp[G ^ 1]), ((gs - 1) >> 1) & 1, abort_flag, p.err,
+                                           kWaitLimitNs);
                 tc_fence_after();
-                if (ok) tmem_st32(t_lane + kTmemP + hf * 32, pk);
-                if (ok && t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                    // Rescale this thread's half of the O row.
+                if (ok) {
+#pragma unroll
+                    for (int c = 0; c < 64; c += 16)
+                        tmem_st16(t_lane + kTmemP + c, *reinterpret_cast<uint32_t(*)[16]>(&pk[c]));
+                }
+                if (ok && !first && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    // Rescale this row of the group's O, once P.V(g - 2) -- the
+                    // last one into it -- has completed.
+                    ok = mbar_wait_bounded(smem_u32(&ms.pv_grp[G]), ((gs - 2) >> 1) & 1, abort_flag, p.err,
+                                           kWaitLimitNs);
+                    tc_fence_after();
 #pragma unroll 1
-                    for (int c0 = hf * dh; c0 < hf * dh + dh; c0 += 32) {
+                    for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t o[32];
-                        tmem_ld32(t_lane + kTmemO + c0, o);
+                        tmem_ld32(o_mine + c0, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
-                        tmem_st32(t_lane + kTmemO + c0, o);
+                        tmem_st32(o_mine + c0, o);
                     }
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&ms.p_full));
+                first = false;
             }
+            if (stager) {
+                // The unit's Q.K^T MMAs have completed: Q may be overwritten.
+                if (ok) ok = mbar_wait_bounded(smem_u32(&ms.q_empty), ul & 1, abort_flag, p.err, kWaitLimitNs);
+                if (ok) {
+                    tc_fence_after();
+                    stage_q<D>(p, u + gridDim.x, r, t_lane);
+                    tc_fence_before();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ms.q_full));
+            }
+            __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[lb]));
             // ------------------------------------------------ unit epilogue
-            int b, h, pair;
-            unit_coords(u, p, b, h, pair);
-            int i0, i1;
-            unit_cubes(p, b, h, pair, i0, i1);
-            const int i = (r >> 6) ? i1 : i0;
-            ms.xsum[hf][r] = l;
-            named_sync(1 + quarter, 64);
-            const float lt = l + ms.xsum[hf ^ 1][r];
-            const uint32_t gl = g - 1;  // last step of the unit
-            // An empty union issued no PV: O holds nothing of this unit, write zeros.
-            if (ok && nst > 0) ok = mbar_wait_bounded(smem_u32(&ms.pv_done), gl & 1, abort_flag, p.err, kWaitLimitNs);
-            if (ok) {
-                tc_fence_after();
-                const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-                const size_t row = (size_t)b * s_pad + (size_t)i * kCubeTokens + (r & 63);
-                uint4* dst = reinterpret_cast<uint4*>(p.out) + (row * p.heads + h) * (size_t)(D / 8);
-                for (int c0 = hf * dh; c0 < hf * dh + dh; c0 += 32) {
-                    uint32_t o[32];
-                    if (nst > 0) {
-                        tmem_ld32(t_lane + kTmemO + c0, o);
-                        tmem_wait_ld();
-                    } else {
+            // Merge the two groups' partial results of each row:
+            //   m = max(m_0, m_1), a_k = 2^(m_k - m), l = a_0 l_0 + a_1 l_1,
+            //   out = (a_0 O_0 + a_1 O_1) / l, lse = (m + log2 l) ln 2.
+            ms.xm[lb][G][r] = m;
+            ms.xl[lb][G][r] = l;
+            named_sync(1 + quarter, 2 * 32);
+            const float mo = ms.xm[lb][G ^ 1][r], lo = ms.xl[lb][G ^ 1][r];
+            const float m0 = G ? mo : m, l0 = G ? lo : l;
+            const float m1 = G ? m : mo, l1 = G ? l : lo;
+            // A group that took no step of this unit holds no O for it.
+            const bool had0 = nst > 0 && (((g0 & 1) == 0) || nst >= 2);
+            const bool had1 = nst > 0 && (((g0 & 1) == 1) || nst >= 2);
+            const float mt = fmaxf(m0, m1);
+            const float a0 = (m0 == ninf) ? 0.f : ex2_approx(m0 - mt);
+            const float a1 = (m1 == ninf) ? 0.f : ex2_approx(m1 - mt);
+            const float lt = a0 * l0 + a1 * l1;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const float s0 = a0 * inv, s1 = a1 * inv;
+            int b, h;
+            const int i = row_cube(p, u, r, b, h);
+            const bool wr = ok && i >= 0;
+            const size_t row = wr ? (size_t)b * s_pad + (size_t)i * kCubeTokens + (r & 63) : 0;
+            uint4* dst = reinterpret_cast<uint4*>(p.out) + (row * p.heads + h) * (size_t)(D / 8) + G * (dh / 8);
+            // Gated: the coarse term g_c * O_c of this thread's columns and the
+            // fine gate g_f, loaded before the wait for the unit's last P.V.
+            float ct[kGated ? dh : 1];
+            uint32_t gfw[kGated ? dh / 2 : 1];
+            if constexpr (kGated) {
+                if (wr) {
+                    const float4* ocr = reinterpret_cast<const float4*>(
+                        p.oc + (((size_t)b * p.heads + h) * p.N + i) * D + G * dh);
+                    const size_t gi = (row * p.heads + h) * (size_t)(D / 8) + G * (dh / 8);
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) o[q] = 0u;
-                    }
-                    if (kGated && i >= 0) {
-                        // Gated sum with the coarse-stage output of the row's cube.  All
-                        // of the chunk's gate and coarse values are loaded before the
-                        // first store (the stores could alias them for the compiler).
-                        const float4* ocr = reinterpret_cast<const float4*>(
-                            p.oc + (((size_t)b * p.heads + h) * p.N + i) * D + c0);
-                        const size_t gi = (row * p.heads + h) * (size_t)(D / 8) + c0 / 8;
-                        uint4 gcv[4], gfv[4];
-                        float4 cv4[8];
+                    for (int v = 0; v < dh / 8; ++v) {
+                        const uint4 gc = __ldcs(p.gc + gi + v), gf = __ldcs(p.gf + gi + v);
+                        const float4 ca = __ldg(ocr + 2 * v), cb = __ldg(ocr + 2 * v + 1);
+                        const uint32_t gcw[4] = {gc.x, gc.y, gc.z, gc.w};
+                        const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+                        gfw[4 * v] = gf.x; gfw[4 * v + 1] = gf.y; gfw[4 * v + 2] = gf.z; gfw[4 * v + 3] = gf.w;
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            gcv[v] = __ldcs(p.gc + gi + v);
-                            gfv[v] = __ldcs(p.gf + gi + v);
-                        }
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) cv4[v] = __ldg(ocr + v);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const float cv[8] = {cv4[2 * v].x, cv4[2 * v].y, cv4[2 * v].z, cv4[2 * v].w,
-                                                 cv4[2 * v + 1].x, cv4[2 * v + 1].y, cv4[2 * v + 1].z,
-                                                 cv4[2 * v + 1].w};
-                            const uint32_t gcw[4] = {gcv[v].x, gcv[v].y, gcv[v].z, gcv[v].w};
-                            const uint32_t gfw[4] = {gfv[v].x, gfv[v].y, gfv[v].z, gfv[v].w};
-                            uint32_t pw[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float f0 = __uint_as_float(o[8 * v + 2 * e]) * inv_l;
-                                const float f1 = __uint_as_float(o[8 * v + 2 * e + 1]) * inv_l;
-                                const float r0 = fmaf(__uint_as_float(gcw[e] << 16), cv[2 * e],
-                                                      __uint_as_float(gfw[e] << 16) * f0);
-                                const float r1 = fmaf(__uint_as_float(gcw[e] & 0xFFFF0000u), cv[2 * e + 1],
-                                                      __uint_as_float(gfw[e] & 0xFFFF0000u) * f1);
-                                pw[e] = pack_bf16x2(r0, r1);
-                            }
-                            __stcs(dst + c0 / 8 + v, make_uint4(pw[0], pw[1], pw[2], pw[3]));
-                        }
-                    } else if (i >= 0) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-                            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-                            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-                            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-                            __stcs(dst + c0 / 8 + v, w);
+                        for (int e = 0; e < 4; ++e) {
+                            ct[8 * v + 2 * e] = __uint_as_float(gcw[e] << 16) * cv[2 * e];
+                            ct[8 * v + 2 * e + 1] = __uint_as_float(gcw[e] & 0xFFFF0000u) * cv[2 * e + 1];
                         }
                     }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < dh; ++c) ct[c] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < dh / 2; ++c) gfw[c] = 0u;
                 }
-                if (p.lse && i >= 0 && hf == 0)
-                    p.lse[((size_t)b * p.heads + h) * s_pad + (size_t)i * kCubeTokens + (r & 63)] =
-                        lt > 0.f ? (m + __log2f(lt)) * 0.69314718055994531f : ninf;
             }
+            // Every P.V of the unit has completed.
+            if (ok) ok = mbar_wait_bounded(smem_u32(&ms.unit_done), ul & 1, abort_flag, p.err, kWaitLimitNs);
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < dh; c0 += 32) {
+                uint32_t oa[32], ob[32];
+                // Loaded whatever had0/had1 say (values of a group without a step
+                // are never used): defined on every path, as the allocator needs.
+                tmem_ld32(t_lane + kTmemO0 + G * dh + c0, oa);
+                tmem_ld32(t_lane + kTmemO1 + G * dh + c0, ob);
+                tmem_wait_ld();
+                uint32_t pw[16];
+#pragma unroll
+                for (int q = 0; q < 32; q += 2) {
+                    float f[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float va = (ok && had0) ? __uint_as_float(oa[q + e]) : 0.f;
+                        const float vb = (ok && had1) ? __uint_as_float(ob[q + e]) : 0.f;
+                        f[e] = fmaf(s0, va, s1 * vb);
+                    }
+                    if constexpr (kGated) {
+                        const uint32_t gw = gfw[(c0 + q) >> 1];
+                        f[0] = fmaf(__uint_as_float(gw << 16), f[0], ct[c0 + q]);
+                        f[1] = fmaf(__uint_as_float(gw & 0xFFFF0000u), f[1], ct[c0 + q + 1]);
+                    }
+                    pw[q >> 1] = pack_bf16x2(f[0], f[1]);
+                }
+                if (wr) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        __stcs(dst + c0 / 8 + v, make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]));
+                }
+            }
+            // O_0 and O_1 have been read: the next unit's P.V may overwrite them.
             tc_fence_before();
-            named_sync(1 + quarter, 64);  // xsum is rewritten by the next unit's epilogue
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ms.o_free));
+            if (wr && p.lse && G == 0)
+                p.lse[((size_t)b * p.heads + h) * s_pad + (size_t)i * kCubeTokens + (r & 63)] =
+                    lt > 0.f ? (mt + __log2f(lt)) * 0.69314718055994531f : ninf;
+            g = g0 + nst;
         }
     }
 
@@ -815,6 +928,13 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
                              : (D == 64 ? fine_fwd_kernel<64, false> : fine_fwd_kernel<128, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
+    // The setmaxnreg split is sized for a launch of exactly kLaunchRegs
+    // registers per thread; any other count would leave the softmax warps'
+    // setmaxnreg.inc waiting forever, so refuse to launch.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
     const int grid = p.num_units < num_sms ? p.num_units : num_sms;
     kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, p);
     note_launches(1);

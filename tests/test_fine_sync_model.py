@@ -3,21 +3,25 @@ checked on the CPU.
 
 Each warp role of one CTA is a generator that yields its waits in program
 order: mbarrier parity waits (with the phase the code means to wait for),
-named-barrier syncs, and arrivals; MMA commits arrive after random delays;
-the scheduler picks warps in random order.  Over random unit sequences
-(including units with an empty union) the test checks that every run ends
-(no deadlock) and that no parity wait ever passes before the phase it stands
-for has completed: a parity wait cannot tell phase p from phase p + 2, so a
-barrier more than one phase away from a waiter would let the wait pass early
-(or never), and the kernel relies on every barrier staying within one phase.
+named-barrier syncs, arrivals and data-hazard checks.  Each MMA-issuing warp
+commits into its own queue whose arrivals land in issue order after random
+delays (a tcgen05.commit completes once every earlier MMA of its thread has),
+and the scheduler picks warps in random order.  Over random unit sequences
+(including units with an empty union) the test checks that every run ends (no
+deadlock), that no parity wait ever passes before the phase it stands for has
+completed (a parity wait cannot tell phase p from phase p + 2, so the kernel
+relies on every barrier staying within one phase of each waiter), and that
+the TMEM hazards hold: P is rewritten only after the P.V that read it, a
+group's O is rescaled only after the last P.V into it, and the epilogue
+reads O only after the unit's last P.V.
 
 The model follows the kernel's roles: warp 0 builds the unit lists and loads
-K into a 3-slot ring, warp 1 issues Q.K^T into two S buffers, warp 2 loads V
-into a 3-slot ring, warp 3 issues P.V, and eight softmax warps (two per TMEM
-lane quarter, one per key cube of a step) exchange row maxima through a named
-barrier, hand P to the P.V warp and stage the next unit's Q.  A planted
-protocol -- the same softmax split into warps that take alternate steps but
-still wait for the previous step's P.V on one barrier -- must be caught.
+K into a 3-slot ring, warp 1 issues Q.K^T into the one S buffer, warp 2 loads
+V into a 3-slot ring, warp 3 issues P.V into the O of the step's group, and
+two softmax groups of four warps (one per TMEM lane quarter) take the even
+and the odd steps, stage the next unit's Q, and merge their results in a
+per-unit epilogue through a named barrier per lane quarter.  Planted
+protocol mistakes must be caught.
 """
 import random
 
@@ -39,30 +43,37 @@ class MBar:
 
 
 class Cta:
-    def __init__(self, softmax_counts):
+    def __init__(self, shared_s_full=False):
         self.mb = {}
         for i in range(3):
             for n in ("k_full", "k_empty", "v_full", "v_empty"):
                 self.mb[f"{n}{i}"] = MBar(1)
         for i in range(2):
-            self.mb[f"s_full{i}"] = MBar(1)
-            self.mb[f"s_free{i}"] = MBar(softmax_counts)
             self.mb[f"list_full{i}"] = MBar(1)
-            self.mb[f"list_empty{i}"] = MBar(10)  # V producer, P.V warp, 8 softmax warps
-        self.mb["p_full"] = MBar(softmax_counts)
-        for n in ("pv_done", "pv_done0", "pv_done1", "q_empty"):
+            self.mb[f"list_empty{i}"] = MBar(11)  # V producer, both MMA warps, 8 softmax warps
+            self.mb[f"pv_grp{i}"] = MBar(1)
+        self.shared_s_full = shared_s_full
+        self.mb["s_full0"] = MBar(1)
+        self.mb["s_full1"] = MBar(1)
+        for n in ("s_free", "p_full", "q_full"):
+            self.mb[n] = MBar(4)
+        for n in ("q_empty", "unit_done"):
             self.mb[n] = MBar(1)
-        self.mb["q_full"] = MBar(8)
+        self.mb["o_free"] = MBar(8)
         self.count = [0, 0]
-        self.commits = []
+        self.queues = {}
 
-    def commit(self, name, rng):
-        self.commits.append([name, rng.randint(0, 6)])
+    def commit(self, issuer, name, rng):
+        self.queues.setdefault(issuer, []).append([name, rng.randint(0, 6)])
 
 
 def wait(name, phase):
     """A parity wait for `phase` of barrier `name`."""
     return ("wait", name, phase & 1, phase)
+
+
+def check(cond, what):
+    return ("check", cond, what)
 
 
 def producer_k(c, units):
@@ -99,108 +110,95 @@ def producer_v(c, units):
 def mma_qk(c, units, rng):
     g = 0
     for ul, nst in enumerate(units):
-        yield wait(f"list_full{ul & 1}", ul >> 1)
+        lb = ul & 1
+        yield wait(f"list_full{lb}", ul >> 1)
         yield wait("q_full", ul)
-        for _ in range(nst):
-            if g >= 2:
-                yield wait(f"s_free{g & 1}", (g >> 1) - 1)
-            yield wait(f"k_full{g % 3}", g // 3)
-            c.commit(f"s_full{g & 1}", rng)
-            c.commit(f"k_empty{g % 3}", rng)
-            g += 1
-        c.commit("q_empty", rng)
-
-
-def mma_pv(c, units, rng, per_parity):
-    g = 0
-    for ul, nst in enumerate(units):
-        lb = ul & 1
-        yield wait(f"list_full{lb}", ul >> 1)
-        for _ in range(nst):
-            yield wait("p_full", g)
-            yield wait(f"v_full{g % 3}", g // 3)
-            c.commit(f"pv_done{g & 1}" if per_parity else "pv_done", rng)
-            c.commit(f"v_empty{g % 3}", rng)
-            g += 1
-        c.mb[f"list_empty{lb}"].arrive()
-
-
-def softmax_kernel(c, units, warp):
-    """The softmax warps as the kernel runs them: both warps of a quarter on every step."""
-    quarter = warp & 3
-    bar = ("nbar", 1 + quarter)
-    g = 0
-    c.mb["q_full"].arrive()  # the first unit's Q
-    for ul, nst in enumerate(units):
-        lb = ul & 1
-        yield wait(f"list_full{lb}", ul >> 1)
-        more = ul + 1 < len(units)
-        if nst == 0 and more:
-            yield wait("q_empty", ul)
-            c.mb["q_full"].arrive()
         for t in range(nst):
-            yield wait(f"s_full{g & 1}", g >> 1)
-            if t + 1 == nst and more:
-                yield wait("q_empty", ul)
-                c.mb["q_full"].arrive()
-            c.mb[f"s_free{g & 1}"].arrive()
-            yield bar  # row-max exchange with the other key cube's thread
-            if g > 0:
-                yield wait("pv_done", g - 1)
-            c.mb["p_full"].arrive()
-            g += 1
-        c.mb[f"list_empty{lb}"].arrive()
-        yield bar  # partial sums
-        if nst > 0:
-            yield wait("pv_done", g - 1)
-        yield bar
-
-
-def softmax_alternating(c, units, warp):
-    """Planted protocol: warp parity p takes the steps g with g % 2 == p and
-    waits for P.V(g - 1) on the single pv_done barrier."""
-    par = (warp - 4) >> 2
-    g = 0
-    c.mb["q_full"].arrive()
-    for ul, nst in enumerate(units):
-        lb = ul & 1
-        yield wait(f"list_full{lb}", ul >> 1)
-        more = ul + 1 < len(units)
-        last_owner = (g + nst - 1) & 1 if nst else -1
-        for t in range((g + par) & 1, nst, 2):
             gs = g + t
-            yield wait(f"s_full{gs & 1}", gs >> 1)
-            if t + 1 == nst and more:
-                yield wait("q_empty", ul)
-                c.mb["q_full"].arrive()
-            c.mb[f"s_free{gs & 1}"].arrive()
-            if gs > 0:
-                yield wait("pv_done", gs - 1)
-            c.mb["p_full"].arrive()
-        if (nst == 0 or last_owner != par) and more:
-            yield wait("q_empty", ul)
-            c.mb["q_full"].arrive()
+            if gs >= 1:
+                yield wait("s_free", gs - 1)
+            yield wait(f"k_full{gs % 3}", gs // 3)
+            c.commit("qk", "s_full0" if c.shared_s_full else f"s_full{gs & 1}", rng)
+            c.commit("qk", f"k_empty{gs % 3}", rng)
+        c.commit("qk", "q_empty", rng)
         c.mb[f"list_empty{lb}"].arrive()
-        if nst > 0:
-            yield wait("pv_done", g + nst - 1)
         g += nst
 
 
-def run(units, seed, softmax=softmax_kernel, softmax_counts=8, per_parity=False):
+def mma_pv(c, units, rng, gate_empty=True):
+    g = 0
+    for ul, nst in enumerate(units):
+        lb = ul & 1
+        yield wait(f"list_full{lb}", ul >> 1)
+        if ul >= 1 and (nst > 0 or gate_empty):
+            yield wait("o_free", ul - 1)
+        for t in range(nst):
+            gs = g + t
+            yield wait("p_full", gs)
+            yield wait(f"v_full{gs % 3}", gs // 3)
+            c.commit("pv", f"pv_grp{gs & 1}", rng)
+            c.commit("pv", f"v_empty{gs % 3}", rng)
+        c.commit("pv", "unit_done", rng)
+        c.mb[f"list_empty{lb}"].arrive()
+        g += nst
+
+
+def softmax(c, units, warp, rng, p_waits_own=False):
+    quarter = warp & 3
+    G = (warp - 4) >> 2
+    bar = ("nbar", 1 + quarter)
+    g = jg = 0
+    if G == 0 and units:
+        c.mb["q_full"].arrive()  # the first unit's Q
+    for ul, nst in enumerate(units):
+        lb = ul & 1
+        yield wait(f"list_full{lb}", ul >> 1)
+        first = True
+        for t in range((g + G) & 1, nst, 2):
+            gs = g + t
+            yield wait("s_full0" if c.shared_s_full else f"s_full{G}", jg if not c.shared_s_full else gs)
+            jg += 1
+            c.mb["s_free"].arrive()
+            if gs > 0 and not p_waits_own:  # P: P.V(gs - 1), the other group's, has read it
+                yield wait(f"pv_grp{G ^ 1}", (gs - 1) >> 1)
+            elif gs > 1:  # planted: waits for this group's own previous P.V instead
+                yield wait(f"pv_grp{G}", (gs - 2) >> 1)
+            yield check(lambda gs=gs: gs == 0 or c.mb[f"pv_grp{(gs - 1) & 1}"].done > (gs - 1) >> 1,
+                        f"P({gs}) written before P.V({gs - 1}) completed")
+            if not first and rng.random() < 0.5:  # a row's max grew: rescale this group's O
+                yield wait(f"pv_grp{G}", (gs - 2) >> 1)
+                yield check(lambda gs=gs: c.mb[f"pv_grp{gs & 1}"].done > (gs - 2) >> 1,
+                            f"O rescaled before P.V({gs - 2}) completed")
+            c.mb["p_full"].arrive()
+            first = False
+        if ((g + nst) & 1) == G and ul + 1 < len(units):  # stage the next unit's Q
+            yield wait("q_empty", ul)
+            c.mb["q_full"].arrive()
+        c.mb[f"list_empty{lb}"].arrive()
+        yield bar  # (m, l) exchange with the other group's warp of this quarter
+        yield wait("unit_done", ul)
+        yield check(lambda e0=(g + nst + 1) >> 1, e1=(g + nst) >> 1:
+                    c.mb["pv_grp0"].done >= e0 and c.mb["pv_grp1"].done >= e1,
+                    "epilogue before the unit's last P.V")
+        c.mb["o_free"].arrive()
+        g += nst
+
+
+def run(units, seed, gate_empty=True, shared_s_full=False, p_waits_own=False):
     rng = random.Random(seed)
-    c = Cta(softmax_counts)
+    c = Cta(shared_s_full)
     warps = {0: producer_k(c, units), 1: mma_qk(c, units, rng), 2: producer_v(c, units),
-             3: mma_pv(c, units, rng, per_parity)}
+             3: mma_pv(c, units, rng, gate_empty)}
     for w in range(4, 12):
-        warps[w] = softmax(c, units, w)
+        warps[w] = softmax(c, units, w, random.Random(seed * 31 + (w & 3)), p_waits_own)
     blocked, finished = {}, set()
     nbar_count, nbar_gen = {}, {}
     while len(finished) < len(warps):
-        for item in list(c.commits):
-            item[1] -= 1
-            if item[1] < 0:
-                c.commits.remove(item)
-                c.mb[item[0]].arrive()
+        for q in c.queues.values():  # each issuer's commits arrive in issue order
+            if q:
+                q[0][1] -= 1
+                if q[0][1] < 0:
+                    c.mb[q.pop(0)[0]].arrive()
         order = [w for w in warps if w not in finished]
         rng.shuffle(order)
         moved = False
@@ -227,7 +225,10 @@ def run(units, seed, softmax=softmax_kernel, softmax_counts=8, per_parity=False)
                     blocked[w] = op
                 elif c.mb[op[1]].done <= op[3]:
                     return f"early pass: warp {w} waited for phase {op[3]} of {op[1]}"
-            elif op[0] == "nbar":  # bar.sync id, 64: the two warps of a quarter
+            elif op[0] == "check":
+                if not op[1]():
+                    return f"hazard: warp {w}: {op[2]}"
+            elif op[0] == "nbar":  # bar.sync id, 64: one warp of each group, same quarter
                 bid = op[1]
                 g0 = nbar_gen.get(bid, 0)
                 nbar_count[bid] = nbar_count.get(bid, 0) + 1
@@ -236,7 +237,7 @@ def run(units, seed, softmax=softmax_kernel, softmax_counts=8, per_parity=False)
                 else:
                     blocked[w] = ("nbar", bid, g0)
             break
-        if not moved and not c.commits:
+        if not moved and not any(c.queues.values()):
             return "deadlock: " + ", ".join(f"warp {w} at {blocked.get(w)}" for w in sorted(warps)
                                             if w not in finished)
     return "ok"
@@ -244,7 +245,7 @@ def run(units, seed, softmax=softmax_kernel, softmax_counts=8, per_parity=False)
 
 def unit_sequences(n, seed):
     rng = random.Random(seed)
-    return [[rng.choice([0, 1, 2, 3, 5, 39, 40]) for _ in range(rng.randint(1, 6))] for _ in range(n)]
+    return [[rng.choice([0, 1, 2, 3, 4, 5, 39, 40]) for _ in range(rng.randint(1, 7))] for _ in range(n)]
 
 
 def test_kernel_protocol_never_deadlocks_or_passes_early():
@@ -252,13 +253,19 @@ def test_kernel_protocol_never_deadlocks_or_passes_early():
         assert run(units, seed=i) == "ok", units
 
 
-@pytest.mark.parametrize("units", [[0], [0, 0, 3], [1], [1, 0, 1], [2, 40, 0, 41]])
+@pytest.mark.parametrize("units", [[0], [0, 0, 3], [1], [1, 0, 1], [2, 40, 0, 41], [0, 0, 0], [3, 0, 0, 2]])
 def test_kernel_protocol_edge_units(units):
     for seed in range(50):
         assert run(units, seed) == "ok"
 
 
-def test_model_catches_a_wait_that_can_pass_early():
-    bad = [run(units, seed=i, softmax=softmax_alternating, softmax_counts=4)
-           for i, units in enumerate(unit_sequences(200, 2))]
-    assert any(r.startswith("early pass") for r in bad)
+@pytest.mark.parametrize("mistake", ["gate_empty", "shared_s_full", "p_waits_own"])
+def test_model_catches_planted_mistakes(mistake):
+    """An empty unit that does not wait for the previous epilogue (unit_done
+    then runs two phases ahead), one S-ready barrier for both groups (the odd
+    group's first wait passes before the even step completes), and a P
+    write that waits for the group's own previous P.V instead of the other
+    group's (P is single-buffered) must each be caught."""
+    kw = {"gate_empty": False} if mistake == "gate_empty" else {mistake: True}
+    bad = [run(units, seed=i, **kw) for i, units in enumerate(unit_sequences(200, 2))]
+    assert any(r != "ok" for r in bad)
