@@ -218,7 +218,14 @@ def stage_bytes(wl):
 
 
 LABELS = {"wan": "Wan2.2-shape VSA", "wan_outlier": "Wan2.2-shape VSA with an outlier head (logits ~1e3)",
-          "hunyuan": "HunyuanVideo-shape VSA"}
+          "hunyuan": "HunyuanVideo-shape VSA",
+          "blocks128": "Wan2.1-shape sequence in 128-token blocks (mean-pool CDF selector + fine stage)"}
+
+# Cumulative-share threshold of the block selector for the blocks128 workload:
+# with tau = 0.4608 the oracle's selector keeps 30.0% of the key blocks of the
+# synthetic 32,768-token, 12-head call (found by bisection on the oracle), the
+# 70% sparsity point of the pages' kernel-time sweep.
+BLOCKS_TAU = 0.4608
 
 
 def config_of(wl):
@@ -237,6 +244,141 @@ def step_bytes(wl):
     untiled = wl.B * wl.T * wl.H * wl.W * wl.heads * wl.D * 2
     tiled = wl.B * wl.s_pad * wl.heads * wl.D * 2
     return 4 * untiled + 4 * tiled
+
+
+# --------------------------------------------------------- blocks128
+def blocks_flops(counts, D: int) -> float:
+    """Effective fine-stage FLOPs of a cube table: 4 * 64 * 64 * D per (query
+    cube, listed key cube), i.e. 4 * S * k * 64 * D * heads for uniform k."""
+    return 4.0 * 64 * 64 * D * float(np.asarray(counts, np.int64).sum())
+
+
+def run_blocks(args, rank, world, dist):
+    """One step = the block selector (pool + select) and the fine stage on its
+    table, for q, k, v [1, 32768, 12, 128] in 128-token blocks."""
+    import torch
+
+    import block_sparse_video_vsa_gb300 as vsa
+    from block_sparse_video_vsa_gb300 import synth
+
+    wl, s_len = synth.SEQUENCE_WORKLOADS["blocks128"]
+    inputs = synth.make_sequence_inputs("blocks128")
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v = (dev_bf16(inputs[n]) for n in ("q", "k", "v"))
+    vbs = torch.from_numpy(inputs["vbs"]).to(dev)
+    B, S, H, D = q.shape
+    nc = S // 64
+    ws = torch.empty((vsa.block_select_workspace_bytes(B, S, H, D),), dtype=torch.uint8, device=dev)
+    tbl = torch.empty((B, H, nc, nc), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, H, nc), dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(marks=None, qin=None, kin=None, vin=None, oout=None):
+        qin = q if qin is None else qin
+        kin = k if kin is None else kin
+        vin = v if vin is None else vin
+        oout = out if oout is None else oout
+        if marks is not None:
+            marks[0].record(stream)
+        vsa.block_select(qin, kin, BLOCKS_TAU, wl.sm_scale, workspace=ws, out=tbl, counts=cnt)
+        if marks is not None:
+            marks[1].record(stream)
+        vsa.sparse_attn_fwd(qin, kin, vin, tbl, vbs, wl.sm_scale, out=oout, lse=lse, counts=cnt)
+        if marks is not None:
+            marks[2].record(stream)
+
+    clk = ClockSampler(torch.cuda.current_device())
+    with clk:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        if vsa.device_error(reset=True):
+            raise RuntimeError("device error word set during warm-up")
+        counts_host = cnt.cpu().numpy()
+        marks = [[ev() for _ in range(3)] for _ in range(args.steps)]
+        start, end = ev(), ev()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.monotonic()
+        n0 = vsa.kernel_launches()
+        start.record(stream)
+        for s in range(args.steps):
+            step(marks[s])
+        end.record(stream)
+        launches = vsa.kernel_launches() - n0
+        torch.cuda.synchronize()
+        clk.window = (t0, time.monotonic())
+    if dist:
+        dist.barrier()
+    if vsa.device_error(reset=True):
+        raise RuntimeError("device error word set during the timed run")
+    ms_step = max_over_ranks(start.elapsed_time(end), dist, dev) / args.steps
+    stage = {"block_select": [m[0].elapsed_time(m[1]) for m in marks],
+             "sparse_attn_fwd": [m[1].elapsed_time(m[2]) for m in marks]}
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_leg(step, inputs, q, k, v, out, args, stream, dist, dev)
+    flops = blocks_flops(counts_host, D)
+    burst, sustained, hbm, peak_kind = load_peaks()
+    fine_ms = statistics.mean(stage["sparse_attn_fwd"])
+    fine_tflops = flops / (fine_ms * 1e-3) / 1e12
+    sparsity = 1.0 - counts_host.mean() / nc
+    sel_bytes = 2 * B * S * H * D * 2  # q and k read once by the pooling pass
+    result = {
+        "metric": METRIC, "value": whole_job_throughput(world, flops, ms_step), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{LABELS['blocks128']}: q, k, v [{B}, {S}, {H}, {D}], tau={BLOCKS_TAU} "
+                               f"(sparsity {sparsity:.3f})",
+                   "B": B, "seq_len": S, "heads": H, "head_dim": D, "block_tokens": 128, "tau": BLOCKS_TAU,
+                   "sparsity": sparsity, "fine_flops": flops,
+                   "l2": f"q, k, v, out ({4 * B * S * H * D * 2 / 1e9:.2f} GB) exceed the 126 MB L2; no flush"},
+        "fine_kernel": {"ms_per_call_mean": fine_ms, "ms_per_call_median": statistics.median(stage["sparse_attn_fwd"]),
+                        "effective_tflops": fine_tflops, "frac_of_burst_peak": fine_tflops / burst,
+                        "frac_of_sustained_peak": fine_tflops / sustained},
+        "stages_ms_median": {k2: statistics.median(v2) for k2, v2 in stage.items()},
+        "stages_hbm_gbs": {"block_select": sel_bytes / (statistics.median(stage["block_select"]) * 1e-3) / 1e9},
+        "hbm_peak_gbs": hbm,
+        "roofline": {"bound": "tensor", "achieved": fine_tflops, "peak": burst, "unit": "TFLOP/s",
+                     "frac": fine_tflops / burst, "traffic": None, "peak_kind": f"{peak_kind} dense bf16 burst",
+                     "kernel": "fine_fwd_kernel (vsa_sparse_attn_fwd with the selector's counts)"},
+        "e2e": None if e2e is None else {
+            "value": whole_job_throughput(world, flops, e2e[0]), "unit": UNIT, "ms_per_step": e2e[0],
+            "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2]},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_blocks_sample(inputs, tbl.cpu().numpy(), counts_host, wl, args.cpu_budget)
+    return result
+
+
+def cpu_blocks_sample(inputs, table, counts, wl, budget_s):
+    """The oracle's fine stage on random query cubes of the blocks128 table."""
+    import oracle
+    rng = np.random.default_rng(0)
+    nthreads = oracle.default_threads()
+    total = counts.size
+    flat = counts.reshape(-1)
+    done, flops, elapsed, used = 0, 0.0, 0.0, 0
+    while elapsed < budget_s and done < total:
+        units = rng.choice(total, size=max(nthreads, 8), replace=False).astype(np.int64)
+        t0 = time.perf_counter()
+        _, _, used = oracle.fine_counts(inputs["q"], inputs["k"], inputs["v"], table, counts, inputs["vbs"],
+                                        wl.sm_scale, units)
+        elapsed += time.perf_counter() - t0
+        done += units.size
+        flops += blocks_flops(flat[units], wl.D)
+    return {"value": flops / elapsed / 1e12, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"fine stage on {done} random query cubes of {total} ({elapsed:.1f} s, {used} threads)"}
 
 
 # ------------------------------------------------------------------ ours
@@ -340,13 +482,24 @@ def run_ours(args, wl, inputs, rank, world, dist):
     if args.no_e2e:
         nxt = time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream)
         return ms_step, stage, clk.summary(), None, 0, 0, launches, nxt
-    # ---- end to end through host buffers (pinned), copies inside the timed region.
-    # Every step copies its q, k, v from pinned host memory and reads its output
-    # back; the copies run on their own streams, double-buffered, so the upload of
-    # step i + 1 and the read-back of step i - 1 overlap the compute of step i.
+    e2e_ms, h2d, d2h = e2e_leg(step, inputs, q, k, v, out, args, stream, dist, dev)
+    # The next rows are timed last, after the end-to-end leg, on the step's tensors.
+    nxt = time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream)
+    return ms_step, stage, clk.summary(), e2e_ms, h2d, d2h, launches, nxt
+
+
+def e2e_leg(step, inputs, q, k, v, out, args, stream, dist, dev):
+    """End to end through host buffers (pinned), copies inside the timed region.
+
+    Every step copies its q, k, v from pinned host memory and reads its output
+    back; the copies run on their own streams, double-buffered, so the upload of
+    step i + 1 and the read-back of step i - 1 overlap the compute of step i.
+    `step(qin=, kin=, vin=, oout=)` enqueues one step on `stream`.  Returns
+    (ms per step, host-to-device bytes per step, device-to-host bytes per step)."""
+    import torch
     qh, kh, vh = (torch.from_numpy(inputs[n].view(np.int16)).view(torch.bfloat16).pin_memory()
                   for n in ("q", "k", "v"))
-    ohs = [torch.empty(qh.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    ohs = [torch.empty(tuple(out.shape), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     dq = [q, torch.empty_like(q)]
     dk = [k, torch.empty_like(k)]
     dv = [v, torch.empty_like(v)]
@@ -385,7 +538,7 @@ def run_ours(args, wl, inputs, rank, world, dist):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    e0, e1 = ev(), ev()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     e2e_run(e2e_steps, first=e0)
     e1.record(stream)
@@ -395,11 +548,7 @@ def run_ours(args, wl, inputs, rank, world, dist):
     if not torch.equal(ohs[last], douts[last].cpu()):
         raise RuntimeError("end-to-end read-back differs from the device result")
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
-    h2d = 3 * qh.numel() * 2
-    d2h = ohs[0].numel() * 2
-    # The next rows are timed last, after the end-to-end leg, on the step's tensors.
-    nxt = time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream)
-    return ms_step, stage, clk.summary(), e2e_ms, h2d, d2h, launches, nxt
+    return e2e_ms, 3 * qh.numel() * 2, ohs[0].numel() * 2
 
 
 def max_over_ranks(x: float, dist, device) -> float:
@@ -482,6 +631,8 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     from block_sparse_video_vsa_gb300 import synth
+    if args.workload == "blocks128":
+        return main_blocks(args, rank, world, local_rank)
     wl = synth.WORKLOADS[args.workload]
     if args.topk > 0:
         wl = wl.with_topk(args.topk)
@@ -543,6 +694,59 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         tflops, cores, desc, _ = cpu_oracle_sample(wl, inputs, args.cpu_budget)
         result["cpu_baseline"] = {"value": tflops, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main_blocks(args, rank, world, local_rank):
+    """--workload blocks128 (the reference arm times the oracle's fine stage on it)."""
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        from block_sparse_video_vsa_gb300 import synth
+        import oracle
+        wl, s_len = synth.SEQUENCE_WORKLOADS["blocks128"]
+        inputs = synth.make_sequence_inputs("blocks128")
+        idx, cnt, _ = oracle.block_select_cdf(inputs["q"], inputs["k"], 128, BLOCKS_TAU, wl.sm_scale)
+        table, counts = oracle.blocks_to_cube_lut(idx, cnt)
+        times, flops, used = [], 0.0, 0
+        rng = np.random.default_rng(1)
+        per_step = 2 * oracle.default_threads()
+        for s in range(args.warmup + args.steps):
+            units = rng.choice(counts.size, size=per_step, replace=False).astype(np.int64)
+            t0 = time.perf_counter()
+            _, _, used = oracle.fine_counts(inputs["q"], inputs["k"], inputs["v"], table, counts, inputs["vbs"],
+                                            wl.sm_scale, units)
+            if s >= args.warmup:
+                times.append(time.perf_counter() - t0)
+                flops += blocks_flops(counts.reshape(-1)[units], wl.D)
+        value = flops / sum(times) / 1e12
+        desc = f"fine stage on {per_step} random query cubes of {counts.size} per step"
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{LABELS['blocks128']}: tau={BLOCKS_TAU}"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    from block_sparse_video_vsa_gb300 import build as vbuild
+    if not vbuild.up_to_date() and rank == 0:
+        vbuild.build()
+    if dist:
+        dist.barrier()
+    result = run_blocks(args, rank, world, dist)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist:

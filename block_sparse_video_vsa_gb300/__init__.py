@@ -25,7 +25,7 @@ __all__ = [
     "VsaError", "library", "num_cubes", "tile", "untile", "coarse_workspace_bytes", "coarse_select",
     "sparse_attn_fwd", "validate_indices", "device_error", "debug_wait_timeout", "pipeline",
     "coarse_attn", "coarse_attn_workspace_bytes", "pair_cubes", "pair_workspace_bytes", "kernel_launches",
-    "table_from_csr",
+    "table_from_csr", "block_select", "block_select_workspace_bytes", "sparse_attn_fwd_peak", "all_cubes",
 ]
 
 _STATUS = {0: "VSA_OK", 1: "VSA_ERR_INVALID_ARG", 2: "VSA_ERR_UNSUPPORTED", 3: "VSA_ERR_ALIGNMENT",
@@ -77,6 +77,8 @@ def _declare(lib):
     lib.vsa_pair_cubes.argtypes = [_p, _i32, _i32, _i32, _i32, _p, _p, _p]
     lib.vsa_validate_indices.restype = ctypes.c_int
     lib.vsa_validate_indices.argtypes = [_p, _p, _i32, _i32, _i32, _i32, _p, _p]
+    lib.vsa_validate_indices_ex.restype = ctypes.c_int
+    lib.vsa_validate_indices_ex.argtypes = [_p, _p, _p, _i32, _i32, _i32, _i32, _p, _p]
     lib.vsa_device_error.restype = ctypes.c_int
     lib.vsa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), _i32]
     lib.vsa_debug_wait_timeout.restype = ctypes.c_int
@@ -84,12 +86,19 @@ def _declare(lib):
     lib.vsa_sparse_attn_fwd_gated.restype = ctypes.c_int
     lib.vsa_sparse_attn_fwd_gated.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32,
                                               ctypes.c_float, _p, _p, _p, _p, _p, _p]
+    lib.vsa_sparse_attn_fwd_peak.restype = ctypes.c_int
+    lib.vsa_sparse_attn_fwd_peak.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32,
+                                             ctypes.c_float, _p, _p, _p, _p]
     lib.vsa_coarse_attn_workspace_bytes.restype = ctypes.c_size_t
     lib.vsa_coarse_attn_workspace_bytes.argtypes = [_i32] * 4
     lib.vsa_coarse_attn.restype = ctypes.c_int
     lib.vsa_coarse_attn.argtypes = [_p, _p, _p, _p, _i32, _i32, _i32, _i32, ctypes.c_float, _p, _p, _p]
     lib.vsa_table_from_csr.restype = ctypes.c_int
-    lib.vsa_table_from_csr.argtypes = [_p, _p, ctypes.c_int64, _i32, _p, _p]
+    lib.vsa_table_from_csr.argtypes = [_p, _p, ctypes.c_int64, ctypes.c_int64, _i32, _i32, _p, _p]
+    lib.vsa_block_select_workspace_bytes.restype = ctypes.c_size_t
+    lib.vsa_block_select_workspace_bytes.argtypes = [_i32] * 4
+    lib.vsa_block_select.restype = ctypes.c_int
+    lib.vsa_block_select.argtypes = [_p, _p, _i32, _i32, _i32, _i32, ctypes.c_float, ctypes.c_float, _p, _p, _p, _p]
     lib.vsa_kernel_launches.restype = ctypes.c_uint64
     lib.vsa_kernel_launches.argtypes = []
     return lib
@@ -142,9 +151,13 @@ def _grid(grid, heads: int, D: int) -> VsaGrid:
 
 
 def num_cubes(grid: Sequence[int]) -> int:
-    """Cubes covering a (B, T, H, W) grid: ceil(T/4) * ceil(H/4) * ceil(W/4)."""
-    _, T, H, W = (int(v) for v in grid)
-    return -(-T // 4) * -(-H // 4) * -(-W // 4)
+    """Cubes covering a (B, T, H, W) grid (vsa_num_cubes)."""
+    B, T, H, W = (int(v) for v in grid)
+    g = VsaGrid(B, T, H, W, 1, 8)  # heads and D do not enter the count
+    n = int(library().vsa_num_cubes(ctypes.byref(g)))
+    if n < 0:
+        raise ValueError(f"grid sizes must be positive, got {tuple(grid)}")
+    return n
 
 
 def tile(x, grid, out=None, vbs=None, stream=None):
@@ -297,6 +310,86 @@ def sparse_attn_fwd(qt, kt, vt, topk_idx, vbs, sm_scale: float = 0.0, out=None, 
     return out, lse
 
 
+def block_select_workspace_bytes(B: int, S: int, heads: int, D: int) -> int:
+    return int(library().vsa_block_select_workspace_bytes(B, S, heads, D))
+
+
+def block_select(q, k, tau: float, sm_scale: float = 0.0, workspace=None, out=None, counts=None, stream=None):
+    """Mean-pool block selector with a cumulative threshold on a token sequence
+    q, k bf16 [B, S, heads, D] (S a multiple of 128) -> (cube table int32
+    [B, heads, S / 64, S / 64], counts int32 [B, heads, S / 64]) for
+    sparse_attn_fwd(..., counts=counts) with the default pairing."""
+    torch = _torch()
+    _need(q, torch.bfloat16, "q")
+    _need(k, torch.bfloat16, "k")
+    B, S, heads, D = q.shape
+    if k.shape != q.shape or S % 128:
+        raise ValueError("q and k must share a [B, S, heads, D] shape with S a multiple of 128")
+    nbytes = block_select_workspace_bytes(B, S, heads, D)
+    if workspace is None:
+        workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=q.device)
+    _need(workspace, torch.uint8, "workspace")
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    nc = S // 64
+    if out is None:
+        out = torch.empty((B, heads, nc, nc), dtype=torch.int32, device=q.device)
+    if counts is None:
+        counts = torch.empty((B, heads, nc), dtype=torch.int32, device=q.device)
+    _need(out, torch.int32, "out")
+    _need(counts, torch.int32, "counts")
+    if tuple(out.shape) != (B, heads, nc, nc) or tuple(counts.shape) != (B, heads, nc):
+        raise ValueError("out must be [B, heads, S / 64, S / 64] and counts [B, heads, S / 64]")
+    _check(library().vsa_block_select(q.data_ptr(), k.data_ptr(), B, S, heads, D, float(tau), float(sm_scale),
+                                      workspace.data_ptr(), out.data_ptr(), counts.data_ptr(), _stream(stream)),
+           "vsa_block_select")
+    return out, counts
+
+
+def sparse_attn_fwd_peak(qt, kt, vt, topk_idx, vbs, sm_scale: float = 0.0, out=None, lse=None, max_prob=None,
+                         pairs=None, counts=None, stream=None):
+    """sparse_attn_fwd that also returns each row's largest softmax weight
+    (vsa_sparse_attn_fwd_peak) -> (out, lse, max_prob fp32 [B, heads, 64*N])."""
+    torch = _torch()
+    for t, n in ((qt, "qt"), (kt, "kt"), (vt, "vt")):
+        _need(t, torch.bfloat16, n)
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(vbs, torch.int32, "vbs")
+    B, S, heads, D = qt.shape
+    if kt.shape != qt.shape or vt.shape != qt.shape or S % 64:
+        raise ValueError("qt/kt/vt must share a tiled [B, 64*N, heads, D] shape")
+    N = S // 64
+    if topk_idx.dim() != 4 or tuple(topk_idx.shape[:3]) != (B, heads, N):
+        raise ValueError("topk_idx must be [B, heads, N, topk]")
+    out = torch.empty_like(qt) if out is None else out
+    lse = torch.empty((B, heads, S), dtype=torch.float32, device=qt.device) if lse is None else lse
+    max_prob = torch.empty((B, heads, S), dtype=torch.float32, device=qt.device) if max_prob is None else max_prob
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    _need(max_prob, torch.float32, "max_prob")
+    if pairs is not None:
+        _need(pairs, torch.int32, "pairs")
+        if tuple(pairs.shape) != (B, heads, (N + 1) // 2):
+            raise ValueError("pairs must be [B, heads, (N + 1) // 2]")
+    if counts is not None:
+        _need(counts, torch.int32, "counts")
+        if tuple(counts.shape) != (B, heads, N):
+            raise ValueError("counts must be [B, heads, N]")
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    _check(library().vsa_sparse_attn_fwd_peak(qt.data_ptr(), kt.data_ptr(), vt.data_ptr(), topk_idx.data_ptr(),
+                                              ptr(counts), vbs.data_ptr(), ptr(pairs), B, N, heads, D,
+                                              topk_idx.shape[3], float(sm_scale), out.data_ptr(), lse.data_ptr(),
+                                              max_prob.data_ptr(), _stream(stream)), "vsa_sparse_attn_fwd_peak")
+    return out, lse, max_prob
+
+
+def all_cubes(B: int, heads: int, ncubes: int, device=None):
+    """The dense selection: every cube for every query cube, int32 [B, heads, N, N]."""
+    torch = _torch()
+    row = torch.arange(ncubes, dtype=torch.int32, device=device)
+    return row.expand(B, heads, ncubes, ncubes).contiguous()
+
+
 def coarse_attn_workspace_bytes(B: int, heads: int, ncubes: int, D: int) -> int:
     return int(library().vsa_coarse_attn_workspace_bytes(B, heads, ncubes, D))
 
@@ -323,31 +416,45 @@ def coarse_attn(qt, kt, vt, vbs, sm_scale: float = 0.0, workspace=None, out=None
     return out
 
 
-def validate_indices(topk_idx, vbs, stream=None) -> int:
-    """Runs the index validator; returns its flag (0 = valid).  Synchronises."""
+def validate_indices(topk_idx, vbs, counts=None, stream=None) -> int:
+    """Runs the index validator; returns its flag (0 = valid).  Synchronises.
+
+    With `counts` (int32 [B, heads, N]) only each row's first counts entries
+    are checked (vsa_validate_indices_ex)."""
     torch = _torch()
     _need(topk_idx, torch.int32, "topk_idx")
     _need(vbs, torch.int32, "vbs")
     B, heads, N, topk = topk_idx.shape
+    if counts is not None:
+        _need(counts, torch.int32, "counts")
+        if tuple(counts.shape) != (B, heads, N):
+            raise ValueError("counts must be [B, heads, N]")
     flag = torch.zeros((1,), dtype=torch.int32, device=topk_idx.device)
-    _check(library().vsa_validate_indices(topk_idx.data_ptr(), vbs.data_ptr(), B, heads, N, topk,
-                                          flag.data_ptr(), _stream(stream)), "vsa_validate_indices")
+    _check(library().vsa_validate_indices_ex(topk_idx.data_ptr(), counts.data_ptr() if counts is not None else None,
+                                             vbs.data_ptr(), B, heads, N, topk, flag.data_ptr(), _stream(stream)),
+           "vsa_validate_indices_ex")
     return int(flag.item())
 
 
-def table_from_csr(lut_ptr, kv_idx, width: int, shape=None):
+def table_from_csr(lut_ptr, kv_idx, width: int, ncubes: int, shape=None):
     """Host-side: a compressed-row block table (int64 offsets `lut_ptr`
-    [rows + 1], int32 indices `kv_idx`) -> (table int32 [rows, width] with -1
-    after each row's entries, counts int32 [rows]), as numpy arrays; `shape`
-    (B, heads, ncubes) reshapes them for sparse_attn_fwd(..., counts=...)."""
+    [rows + 1], int32 indices `kv_idx`, each in [0, ncubes)) -> (table int32
+    [rows, width] with -1 after each row's entries, counts int32 [rows]), as
+    numpy arrays; `shape` (B, heads, ncubes) reshapes them for
+    sparse_attn_fwd(..., counts=...)."""
     import numpy as np
     lut_ptr = np.ascontiguousarray(lut_ptr, dtype=np.int64)
     kv_idx = np.ascontiguousarray(kv_idx, dtype=np.int32)
+    if lut_ptr.ndim != 1 or lut_ptr.shape[0] < 2:
+        raise ValueError("lut_ptr must be 1-D with rows + 1 >= 2 entries")
+    if kv_idx.ndim != 1 or kv_idx.size < lut_ptr[-1]:
+        raise ValueError(f"kv_idx holds {kv_idx.size} entries, lut_ptr[-1] needs {int(lut_ptr[-1])}")
     rows = lut_ptr.shape[0] - 1
-    table = np.empty((max(rows, 0), width), np.int32)
-    counts = np.empty((max(rows, 0),), np.int32)
-    _check(library().vsa_table_from_csr(lut_ptr.ctypes.data, kv_idx.ctypes.data if kv_idx.size else None, rows,
-                                        int(width), table.ctypes.data, counts.ctypes.data), "vsa_table_from_csr")
+    table = np.empty((rows, width), np.int32)
+    counts = np.empty((rows,), np.int32)
+    _check(library().vsa_table_from_csr(lut_ptr.ctypes.data, kv_idx.ctypes.data if kv_idx.size else None,
+                                        kv_idx.size, rows, int(width), int(ncubes), table.ctypes.data,
+                                        counts.ctypes.data), "vsa_table_from_csr")
     if shape is not None:
         table = table.reshape(tuple(shape) + (width,))
         counts = counts.reshape(tuple(shape))

@@ -1,5 +1,6 @@
 // C ABI of the VSA library: argument validation on the host, then dispatch
-// to the kernels of tile.cu, coarse.cu, pair.cu, fine.cu and coarse_attn.cu
+// to the kernels of tile.cu, coarse.cu, pair.cu, fine.cu, coarse_attn.cu and
+// block_select.cu
 // (coarse_noalloc.cu holds the allocation-free coarse entry point).  See
 // include/vsa.h for the contract of each entry point.
 #include <math.h>
@@ -24,6 +25,12 @@ bool g_ctx_ok[kMaxDevices];
 }  // namespace
 
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+// Element counts that index int32 loops in the kernels must stay below 2^31.
+bool sizes_fit(int64_t B, int64_t rows, int64_t heads, int64_t D) {
+    const int64_t lim = (int64_t)1 << 31;
+    return heads * D < lim / 64 && B * rows < lim && B * heads * rows / 64 < lim;
+}
 
 cudaError_t get_dev_ctx(DevCtx* out) {
     int dev = 0;
@@ -64,12 +71,6 @@ bool grid_ok(const vsa_grid* g) {
 
 int64_t cubes_of(const vsa_grid* g) {
     return (int64_t)((g->T + 3) / 4) * ((g->H + 3) / 4) * ((g->W + 3) / 4);
-}
-
-// Element counts that index int32 loops in the kernels must stay below 2^31.
-bool sizes_fit(int64_t B, int64_t rows, int64_t heads, int64_t D) {
-    const int64_t lim = (int64_t)1 << 31;
-    return heads * D < lim / 64 && B * rows < lim && B * heads * rows / 64 < lim;
 }
 
 }  // namespace
@@ -142,11 +143,15 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
                                    static_cast<cudaStream_t>(stream)));
 }
 
-vsa_status vsa_sparse_attn_fwd_gated(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
-                                     const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int32_t B,
-                                     int32_t ncubes, int32_t heads, int32_t D, int32_t topk, float sm_scale,
-                                     const float* coarse_out, const void* gate_c, const void* gate_f, void* out,
-                                     float* lse, vsa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Every fine-stage entry point: validation, then one launch of the fine kernel.
+vsa_status fine_entry(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx, const int32_t* counts,
+                      const int32_t* vbs, const uint32_t* pairs, int32_t B, int32_t ncubes, int32_t heads, int32_t D,
+                      int32_t topk, float sm_scale, const float* coarse_out, const void* gate_c, const void* gate_f,
+                      void* out, float* lse, float* max_prob, vsa_stream_t stream) {
     if (!qt || !kt || !vt || !topk_idx || !vbs || !out) return VSA_ERR_INVALID_ARG;
     const bool gated = coarse_out || gate_c || gate_f;
     if (gated && (!coarse_out || !gate_c || !gate_f)) return VSA_ERR_INVALID_ARG;
@@ -162,6 +167,7 @@ vsa_status vsa_sparse_attn_fwd_gated(const void* qt, const void* kt, const void*
         (reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(vbs) & 3u) ||
         (reinterpret_cast<uintptr_t>(pairs) & 3u) || (reinterpret_cast<uintptr_t>(counts) & 3u) ||
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+        (max_prob && (reinterpret_cast<uintptr_t>(max_prob) & 3u)) ||
         (gated && (!aligned16(coarse_out) || !aligned16(gate_c) || !aligned16(gate_f))))
         return VSA_ERR_ALIGNMENT;
     DevCtx ctx;
@@ -170,9 +176,32 @@ vsa_status vsa_sparse_attn_fwd_gated(const void* qt, const void* kt, const void*
     if (fine_smem_bytes() > ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
     return from_cuda(launch_fine(qt, kt, vt, topk_idx, counts, vbs, pairs, B, ncubes, heads, D, topk, sm_scale,
-                                 coarse_out, gate_c, gate_f, out, lse, ctx.err, ctx.num_sms,
+                                 coarse_out, gate_c, gate_f, out, lse, max_prob, ctx.err, ctx.num_sms,
                                  static_cast<cudaStream_t>(stream)));
 }
+
+}  // namespace
+
+extern "C" {
+
+vsa_status vsa_sparse_attn_fwd_gated(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                                     const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int32_t B,
+                                     int32_t ncubes, int32_t heads, int32_t D, int32_t topk, float sm_scale,
+                                     const float* coarse_out, const void* gate_c, const void* gate_f, void* out,
+                                     float* lse, vsa_stream_t stream) {
+    return fine_entry(qt, kt, vt, topk_idx, counts, vbs, pairs, B, ncubes, heads, D, topk, sm_scale, coarse_out,
+                      gate_c, gate_f, out, lse, nullptr, stream);
+}
+
+vsa_status vsa_sparse_attn_fwd_peak(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
+                                    const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int32_t B,
+                                    int32_t ncubes, int32_t heads, int32_t D, int32_t topk, float sm_scale, void* out,
+                                    float* lse, float* max_prob, vsa_stream_t stream) {
+    if (!max_prob) return VSA_ERR_INVALID_ARG;
+    return fine_entry(qt, kt, vt, topk_idx, counts, vbs, pairs, B, ncubes, heads, D, topk, sm_scale, nullptr, nullptr,
+                      nullptr, out, lse, max_prob, stream);
+}
+
 
 vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                                   const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int32_t B,
@@ -220,6 +249,29 @@ vsa_status vsa_sparse_attn_fwd(const void* qt, const void* kt, const void* vt, c
                                   sm_scale, out, lse, stream);
 }
 
+size_t vsa_block_select_workspace_bytes(int32_t B, int32_t S, int32_t heads, int32_t D) {
+    if (B <= 0 || heads <= 0 || S <= 0 || S % 128 || (D != 64 && D != 128)) return 0;
+    return block_select_workspace_bytes(B, heads, S / 128, D);
+}
+
+vsa_status vsa_block_select(const void* q, const void* k, int32_t B, int32_t S, int32_t heads, int32_t D, float tau,
+                            float sm_scale, void* workspace, int32_t* cube_idx, int32_t* cube_counts,
+                            vsa_stream_t stream) {
+    if (!q || !k || !workspace || !cube_idx || !cube_counts) return VSA_ERR_INVALID_ARG;
+    if (B <= 0 || S <= 0 || heads <= 0 || S % 128) return VSA_ERR_INVALID_ARG;
+    if (!(tau > 0.f && tau <= 1.f) || !(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return VSA_ERR_UNSUPPORTED;
+    if (S / 128 > block_select_max_blocks() || B > 65535 || heads > 65535 ||
+        !sizes_fit(B, S, heads, D))
+        return VSA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(cube_idx) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cube_counts) & 3u))
+        return VSA_ERR_ALIGNMENT;
+    if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
+    return from_cuda(launch_block_select(q, k, B, S, heads, D, tau, sm_scale, workspace, cube_idx, cube_counts,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 size_t vsa_pair_workspace_bytes(int32_t B, int32_t heads, int32_t ncubes, int32_t topk) {
     if (B <= 0 || heads <= 0 || ncubes <= 0 || topk <= 0) return 0;
     return pair_workspace_bytes(B, heads, ncubes, topk);
@@ -242,17 +294,23 @@ vsa_status vsa_pair_cubes(const int32_t* topk_idx, int32_t B, int32_t ncubes, in
                                  ctx.max_smem_optin, static_cast<cudaStream_t>(stream)));
 }
 
-vsa_status vsa_validate_indices(const int32_t* topk_idx, const int32_t* vbs, int32_t B, int32_t heads,
-                                int32_t ncubes, int32_t topk, int32_t* dev_flag, vsa_stream_t stream) {
+vsa_status vsa_validate_indices_ex(const int32_t* topk_idx, const int32_t* counts, const int32_t* vbs, int32_t B,
+                                   int32_t heads, int32_t ncubes, int32_t topk, int32_t* dev_flag,
+                                   vsa_stream_t stream) {
     if (!topk_idx || !vbs || !dev_flag) return VSA_ERR_INVALID_ARG;
     if (B <= 0 || heads <= 0 || ncubes <= 0 || topk <= 0) return VSA_ERR_INVALID_ARG;
     if (ncubes > validate_max_cubes() || (int64_t)B * heads * ncubes >= ((int64_t)1 << 31))
         return VSA_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(vbs) & 3u) ||
-        (reinterpret_cast<uintptr_t>(dev_flag) & 3u))
+        (reinterpret_cast<uintptr_t>(counts) & 3u) || (reinterpret_cast<uintptr_t>(dev_flag) & 3u))
         return VSA_ERR_ALIGNMENT;
-    return from_cuda(launch_validate(topk_idx, vbs, B * heads * ncubes, ncubes, topk, dev_flag,
+    return from_cuda(launch_validate(topk_idx, counts, vbs, B * heads * ncubes, ncubes, topk, dev_flag,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status vsa_validate_indices(const int32_t* topk_idx, const int32_t* vbs, int32_t B, int32_t heads,
+                                int32_t ncubes, int32_t topk, int32_t* dev_flag, vsa_stream_t stream) {
+    return vsa_validate_indices_ex(topk_idx, nullptr, vbs, B, heads, ncubes, topk, dev_flag, stream);
 }
 
 vsa_status vsa_device_error(uint32_t* out, int32_t reset) {
@@ -277,15 +335,19 @@ vsa_status vsa_debug_wait_timeout(int64_t limit_ns, int32_t* dev_result, vsa_str
 
 uint64_t vsa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
-vsa_status vsa_table_from_csr(const int64_t* lut_ptr, const int32_t* kv_idx, int64_t rows, int32_t width,
-                              int32_t* table, int32_t* counts) {
-    if (!lut_ptr || !table || !counts || rows <= 0 || width <= 0) return VSA_ERR_INVALID_ARG;
+vsa_status vsa_table_from_csr(const int64_t* lut_ptr, const int32_t* kv_idx, int64_t nnz, int64_t rows,
+                              int32_t width, int32_t ncubes, int32_t* table, int32_t* counts) {
+    if (!lut_ptr || !table || !counts || rows <= 0 || width <= 0 || nnz < 0 || ncubes <= 0)
+        return VSA_ERR_INVALID_ARG;
     if (lut_ptr[0] != 0) return VSA_ERR_INVALID_ARG;
     for (int64_t r = 0; r < rows; ++r) {
         const int64_t n = lut_ptr[r + 1] - lut_ptr[r];
         if (n < 0 || n > width) return VSA_ERR_INVALID_ARG;
     }
+    if (lut_ptr[rows] > nnz) return VSA_ERR_INVALID_ARG;  // the offsets run past kv_idx
     if (lut_ptr[rows] > 0 && !kv_idx) return VSA_ERR_INVALID_ARG;
+    for (int64_t e = 0; e < lut_ptr[rows]; ++e)
+        if (kv_idx[e] < 0 || kv_idx[e] >= ncubes) return VSA_ERR_INDEX_RANGE;
     for (int64_t r = 0; r < rows; ++r) {
         const int64_t b = lut_ptr[r];
         const int32_t n = (int32_t)(lut_ptr[r + 1] - b);

@@ -583,6 +583,7 @@ constexpr int kValWarps = 4;
 constexpr int kValMaxCubes = 65536;
 
 __global__ void __launch_bounds__(kValWarps * 32) validate_kernel(const int32_t* __restrict__ idx,
+                                                                  const int32_t* __restrict__ counts,
                                                                   const int32_t* __restrict__ vbs,
                                                                   int rows, int ncubes, int topk,
                                                                   int32_t* flag) {
@@ -598,7 +599,15 @@ __global__ void __launch_bounds__(kValWarps * 32) validate_kernel(const int32_t*
         for (int w = lane; w < words; w += 32) my[w] = 0u;
         __syncwarp();
         const int32_t* p = idx + (size_t)row * topk;
-        for (int t = lane; t < topk; t += 32) {
+        int n = topk;  // entries in use: the row's count, when counts are given
+        if (counts) {
+            n = counts[row];
+            if (n < 0 || n > topk) {
+                f |= 8;
+                n = n < 0 ? 0 : topk;
+            }
+        }
+        for (int t = lane; t < n; t += 32) {
             const int j = p[t];
             if (j < 0 || j >= ncubes) {
                 f |= 1;
@@ -717,8 +726,8 @@ cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, in
     return cudaGetLastError();
 }
 
-cudaError_t launch_validate(const int32_t* idx, const int32_t* vbs, int rows, int ncubes, int topk,
-                            int32_t* flag, cudaStream_t stream) {
+cudaError_t launch_validate(const int32_t* idx, const int32_t* counts, const int32_t* vbs, int rows, int ncubes,
+                            int topk, int32_t* flag, cudaStream_t stream) {
     const int words = (ncubes + 31) / 32;
     const size_t smem = (size_t)kValWarps * words * 4;
     int blocks = (rows + kValWarps - 1) / kValWarps;
@@ -727,7 +736,7 @@ cudaError_t launch_validate(const int32_t* idx, const int32_t* vbs, int rows, in
     cudaError_t e = cudaFuncSetAttribute(validate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    validate_kernel<<<blocks, kValWarps * 32, smem, stream>>>(idx, vbs, rows, ncubes, topk, flag);
+    validate_kernel<<<blocks, kValWarps * 32, smem, stream>>>(idx, counts, vbs, rows, ncubes, topk, flag);
     note_launches(1);
     return cudaGetLastError();
 }

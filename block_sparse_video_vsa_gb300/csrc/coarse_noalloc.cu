@@ -10,9 +10,12 @@
 //
 // The scratch is one file-scope device array of kScratchBytes (64 MiB).
 // Every GPU that loads this library reserves it for the life of the process.
-// Its device address is looked up once per device (cudaGetSymbolAddress,
-// with that device current) on the first call made on that device; make that
-// first call before any stream capture.  All calls on a device share the one
+// Its device address is looked up with cudaGetSymbolAddress (with the
+// device current) on every call made outside a stream capture, so a device
+// reset, which reloads the module and may move the array, is picked up by
+// the next call; a call made while its stream is capturing uses the address
+// found by the last call on that device outside a capture, so make one call
+// on each device before capturing.  All calls on a device share the one
 // array: calls whose kernels overlap on the GPU (e.g. on two streams at once)
 // race on it and must be serialised by the caller.  The array keeps whatever
 // the last call left; the kernels here overwrite every byte they read, so no
@@ -37,19 +40,24 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices];
 
-// Device address of the scratch array on the current device (set up on the
-// first call per device).
-cudaError_t scratch_for_current_device(void** out) {
+// Device address of the scratch array on the current device: looked up
+// afresh unless `stream` is capturing, then the last address found.
+cudaError_t scratch_for_current_device(cudaStream_t stream, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_coarse_scratch);
         if (e != cudaSuccess) return e;
         g_scratch_ptr[dev] = p;
+    } else if (!g_scratch_ptr[dev]) {
+        return cudaErrorStreamCaptureUnsupported;
     }
     *out = g_scratch_ptr[dev];
     return cudaSuccess;
@@ -68,7 +76,7 @@ extern "C" vsa_status vsa_coarse_select_noalloc(const void* qt, const void* kt, 
     if (B <= 0 || ncubes <= 0 || heads <= 0 || topk <= 0 || topk > ncubes) return VSA_ERR_INVALID_ARG;
     if (!(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return VSA_ERR_UNSUPPORTED;
-    if (ncubes > 4096) return VSA_ERR_UNSUPPORTED;
+    if (ncubes > 4096 || !sizes_fit(B, (int64_t)ncubes * 64, heads, D)) return VSA_ERR_UNSUPPORTED;
     // The problem must fit the fixed scratch array: scores through memory when
     // that path is the default and its score matrix fits, else the fused path.
     bool split = coarse_split_default(ncubes, D);
@@ -81,7 +89,7 @@ extern "C" vsa_status vsa_coarse_select_noalloc(const void* qt, const void* kt, 
     if (coarse_smem_bytes(ncubes, D, split) > (size_t)ctx.max_smem_optin)
         return VSA_ERR_UNSUPPORTED;
     void* scratch = nullptr;
-    if (scratch_for_current_device(&scratch) != cudaSuccess) return VSA_ERR_CUDA;
+    if (scratch_for_current_device(static_cast<cudaStream_t>(stream), &scratch) != cudaSuccess) return VSA_ERR_CUDA;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
     return launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, scratch, topk_idx, split,
                          static_cast<cudaStream_t>(stream)) == cudaSuccess

@@ -77,7 +77,7 @@ constexpr int kProducerRegs = 72;
 constexpr int kSoftmaxRegs = 216;
 static_assert(128 * kProducerRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kMaxTopk = 512;
+constexpr int kMaxTopk = 1024;
 constexpr int kMaxUnion = 2 * kMaxTopk;
 constexpr int kMaxCubes = 8192;
 constexpr int kBitmapWords = kMaxCubes / 32;
@@ -124,6 +124,7 @@ struct __align__(16) Misc {
     int list_count[2];
     float xm[2][2][128];  // [unit parity][group][row]: running max at the unit's end
     float xl[2][2][128];  // [unit parity][group][row]: sum at the unit's end
+    float xt[2][2][128];  // [unit parity][group][row]: exact row maximum (log2 units)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -143,6 +144,7 @@ struct FineParams {
     const uint4* gf;
     __nv_bfloat16* out;
     float* lse;
+    float* max_prob;     // [B * heads][S_pad] largest softmax weight of each row, or null
     unsigned int* err;
     int B, N, heads, D, topk;
     int npairs;          // ceil(N / 2)
@@ -642,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool stager = (((g0 + nst) & 1) == (uint32_t)G) && ul + 1 < my_units;
             if (stager) prefetch_q<D>(p, u + gridDim.x, r);
             float m = ninf, l = 0.f;
+            float mx = ninf;  // exact row maximum of this group's steps (m lags it by up to the threshold)
             bool first = true;
 #pragma unroll 1
             for (int t = (int)((g0 + G) & 1); t < nst; t += 2) {
@@ -683,6 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lmax = fmaxf(lmax, max64(x + 64));
                 }
                 lmax *= c2;
+                mx = fmaxf(mx, lmax);
                 // Lazy running max: rescale O and l only on a jump > threshold.
                 float alpha = 1.f;
                 if (lmax > m + kRescaleThreshold) {
@@ -757,8 +761,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             //   out = (a_0 O_0 + a_1 O_1) / l, lse = (m + log2 l) ln 2.
             ms.xm[lb][G][r] = m;
             ms.xl[lb][G][r] = l;
+            ms.xt[lb][G][r] = mx;
             named_sync(1 + quarter, 2 * 32);
             const float mo = ms.xm[lb][G ^ 1][r], lo = ms.xl[lb][G ^ 1][r];
+            const float m_true = fmaxf(mx, ms.xt[lb][G ^ 1][r]);
             const float m0 = G ? mo : m, l0 = G ? lo : l;
             const float m1 = G ? m : mo, l1 = G ? l : lo;
             // A group that took no step of this unit holds no O for it.
@@ -842,9 +848,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ms.o_free));
-            if (wr && p.lse && G == 0)
-                p.lse[((size_t)b * p.heads + h) * s_pad + (size_t)i * kCubeTokens + (r & 63)] =
-                    lt > 0.f ? (mt + __log2f(lt)) * 0.69314718055994531f : ninf;
+            if (wr && G == 0) {
+                const size_t at = ((size_t)b * p.heads + h) * s_pad + (size_t)i * kCubeTokens + (r & 63);
+                const float lse2 = lt > 0.f ? mt + __log2f(lt) : ninf;  // log2 units
+                if (p.lse) p.lse[at] = lt > 0.f ? lse2 * 0.69314718055994531f : ninf;
+                // The largest softmax weight of the row: 2^(exact max - lse).
+                if (p.max_prob) p.max_prob[at] = lt > 0.f ? ex2_approx(m_true - lse2) : 0.f;
+            }
             g = g0 + nst;
         }
     }
@@ -898,8 +908,8 @@ int fine_max_cubes() { return kMaxCubes; }
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                         const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int B, int ncubes,
                         int heads, int D, int topk, float sm_scale, const float* coarse_out, const void* gate_c,
-                        const void* gate_f, void* out, float* lse, unsigned int* err, int num_sms,
-                        cudaStream_t stream) {
+                        const void* gate_f, void* out, float* lse, float* max_prob, unsigned int* err,
+                        int num_sms, cudaStream_t stream) {
     CUtensorMap mk, mv;
     const int rows = B * ncubes * kCubeTokens;
     if (!make_map(&mk, kt, rows, heads, D, true) || !make_map(&mv, vt, rows, heads, D, true))
@@ -915,6 +925,7 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     p.q = static_cast<const uint4*>(qt);
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;
+    p.max_prob = max_prob;
     p.err = err;
     p.B = B;
     p.N = ncubes;

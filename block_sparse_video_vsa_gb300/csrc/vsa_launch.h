@@ -12,6 +12,8 @@ namespace vsa {
 
 // api.cu: counts kernel launches (n kernels enqueued by the caller).
 void note_launches(int n);
+// api.cu: element counts that index int32 loops in the kernels stay below 2^31.
+bool sizes_fit(int64_t B, int64_t rows, int64_t heads, int64_t D);
 
 // tile.cu
 cudaError_t launch_tile(const vsa_grid& g, int ncubes, const void* x, void* xt, int32_t* vbs,
@@ -26,8 +28,8 @@ int coarse_rows_per_block(int ncubes, int D);
 cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes, int heads,
                           int D, int topk, float sm_scale, void* workspace, int32_t* topk_idx,
                           bool split, cudaStream_t stream);
-cudaError_t launch_validate(const int32_t* idx, const int32_t* vbs, int rows, int ncubes, int topk,
-                            int32_t* flag, cudaStream_t stream);
+cudaError_t launch_validate(const int32_t* idx, const int32_t* counts, const int32_t* vbs, int rows, int ncubes,
+                            int topk, int32_t* flag, cudaStream_t stream);
 int validate_max_cubes();
 cudaError_t launch_debug_wait(long long limit_ns, int32_t* result, unsigned int* err, cudaStream_t stream);
 
@@ -38,14 +40,21 @@ int fine_max_cubes();
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                         const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int B, int ncubes,
                         int heads, int D, int topk, float sm_scale, const float* coarse_out, const void* gate_c,
-                        const void* gate_f, void* out, float* lse, unsigned int* err, int num_sms,
-                        cudaStream_t stream);
+                        const void* gate_f, void* out, float* lse, float* max_prob, unsigned int* err,
+                        int num_sms, cudaStream_t stream);
 
 // coarse_attn.cu
 size_t coarse_attn_workspace_bytes(int B, int heads, int ncubes, int D);
 cudaError_t launch_coarse_attn(const void* qt, const void* kt, const void* vt, const int32_t* vbs, int B,
                                int ncubes, int heads, int D, float sm_scale, void* workspace, float* out,
                                cudaStream_t stream);
+
+// block_select.cu
+size_t block_select_workspace_bytes(int B, int heads, int nb, int D);
+int block_select_max_blocks();
+cudaError_t launch_block_select(const void* q, const void* k, int B, int S, int heads, int D, float tau,
+                                float sm_scale, void* workspace, int32_t* cube_idx, int32_t* cube_counts,
+                                cudaStream_t stream);
 
 // pair.cu
 int pair_words(int ncubes);

@@ -233,19 +233,24 @@ def window_topk(cube_grid: Sequence[int], radius: Sequence[int], B: int, heads: 
     return out
 
 
-def make_sequence_inputs(name: str):
-    """Raster-order q, k, v of a SEQUENCE_WORKLOADS entry, zero-padded to its
-    sequence length: dict(q, k, v) of bf16 bits [B, S, heads, D] plus
-    `real` (tokens before the padding) and `vbs` (int32 per 64-token slot
-    group: 64, then the real tokens of the last groups)."""
-    wl, s_len = SEQUENCE_WORKLOADS[name]
+def sequence_inputs(wl: Workload, s_len: int):
+    """Raster-order q, k, v of workload `wl` zero-padded to `s_len` tokens (a
+    multiple of 128): dict(q, k, v) of bf16 bits [B, s_len, heads, D] plus
+    `real` (tokens before the padding), `vbs` (int32 per 64-token slot group:
+    64, then the real tokens of the last groups) and `extreme`."""
     d = make_inputs(wl)
     real = wl.tokens
     assert s_len % 128 == 0 and s_len >= real
-    out = {"real": real}
+    out = {"real": real, "extreme": d["extreme"]}
     for n in ("q", "k", "v"):
         x = np.zeros((wl.B, s_len, wl.heads, wl.D), np.uint16)
         x[:, :real] = d[n]
         out[n] = x
     out["vbs"] = np.clip(real - 64 * np.arange(s_len // 64), 0, 64).astype(np.int32)
     return out
+
+
+def make_sequence_inputs(name: str):
+    """sequence_inputs of a SEQUENCE_WORKLOADS entry."""
+    wl, s_len = SEQUENCE_WORKLOADS[name]
+    return sequence_inputs(wl, s_len)

@@ -14,7 +14,9 @@
  *   4. vsa_untile          the inverse permutation of step 1.
  * and, beside them, the coarse stage's own attention output
  * (vsa_coarse_attn) and its gated sum with the fine output
- * (vsa_sparse_attn_fwd_gated).
+ * (vsa_sparse_attn_fwd_gated), and a mean-pool block selector with a
+ * cumulative threshold for sequences in 128-token blocks
+ * (vsa_block_select).
  *
  * Sources (page title, section):
  *   [VSA-AMD] "VSA: Accelerating Video Diffusion Inference with Sparse
@@ -25,6 +27,10 @@
  *             Reference": Shapes, Operator contract.
  *   [STA]     "FastVideo Guide: Sliding Tile Attention": Implementation
  *             (tile partition and inverse permutation).
+ *   [INT8-WAN] "Optimizing block-sparse INT8 attention and multi-expert step
+ *             caching for Wan 2.2": Decoupling Block Selection from Sparse
+ *             CUDA Kernels, Dynamic Sparsity Budgeting via Softmax
+ *             Normalizer Registers.
  *
  * Conventions shared by every entry point
  *   - Layout: token tensors are BSHD, i.e. [B, S, heads, D] row-major,
@@ -159,11 +165,18 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
  * the device.  The paper has no counterpart; it is a deployment variant.
  * Same arguments, results and errors as vsa_coarse_select, except:
  *   - the scratch is a 64 MiB device array inside the library, reserved on
- *     every GPU that loads the library until the process exits; problems
- *     whose vsa_coarse_workspace_bytes exceeds 64 MiB return
- *     VSA_ERR_UNSUPPORTED;
- *   - the first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture;
+ *     every GPU that loads the library until the process exits.  The
+ *     problem uses the score-matrix form of the selection when that is
+ *     vsa_coarse_select's choice and its workspace (the value
+ *     vsa_coarse_workspace_bytes returns) fits in 64 MiB; otherwise the
+ *     fused form, whose workspace is 16 * B * heads * ncubes * D
+ *     + 8 * B * heads * ncubes bytes.  VSA_ERR_UNSUPPORTED when that too
+ *     exceeds 64 MiB, or the fused form's shared memory does not fit;
+ *   - every call made outside a stream capture looks up the array's device
+ *     address (cudaGetSymbolAddress, with the call's device current), so a
+ *     device reset is picked up; a call made while its stream is capturing
+ *     reuses the address its device's last such lookup found (VSA_ERR_CUDA
+ *     if there was none), so make one call per device before capturing;
  *   - all calls on a device share the array, so calls whose kernels overlap
  *     on the GPU race and must be serialised by the caller;
  *   - no cudaMalloc, cudaFree or other allocating routine is called.
@@ -190,7 +203,7 @@ vsa_status vsa_coarse_select_noalloc(const void* qt, const void* kt, const int32
  *   vbs        : int32 [ncubes], each in [0, 64]
  *   out        : bf16 [B, 64*ncubes, heads, D] (written in full)
  *   lse        : fp32 [B, heads, 64*ncubes] (written), or NULL
- * Limits: D in {64, 128}; 1 <= topk <= min(ncubes, 512); ncubes <= 8192;
+ * Limits: D in {64, 128}; 1 <= topk <= min(ncubes, 1024); ncubes <= 8192;
  * 64*ncubes*B < 2^31.
  * Index validity is a precondition (check with vsa_validate_indices).
  */
@@ -254,6 +267,25 @@ vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt
                                   float sm_scale, void* out, float* lse, vsa_stream_t stream);
 
 /*
+ * vsa_sparse_attn_fwd_ex that also returns each row's peakedness ([INT8-WAN]
+ * Dynamic Sparsity Budgeting via Softmax Normalizer Registers: with m the
+ * row's largest logit and l = sum_x exp(s_x - m), 1 / l is the row's largest
+ * softmax weight):
+ *   max_prob_r = exp(m_r - lse_r),  m_r = the largest attended s_x of row r,
+ * formed from the exact row maximum the kernel tracks beside its lazily
+ * updated softmax offset.  A row with no attended key gets 0.
+ *   max_prob : fp32 [B, heads, 64*ncubes] (written; required)
+ * Other arguments, limits and errors as for vsa_sparse_attn_fwd_ex (lse may
+ * be NULL).
+ */
+vsa_status vsa_sparse_attn_fwd_peak(const void* qt, const void* kt, const void* vt,
+                                    const int32_t* topk_idx, const int32_t* counts,
+                                    const int32_t* vbs, const uint32_t* pairs, int32_t B,
+                                    int32_t ncubes, int32_t heads, int32_t D, int32_t topk,
+                                    float sm_scale, void* out, float* lse, float* max_prob,
+                                    vsa_stream_t stream);
+
+/*
  * Coarse-stage attention output ([VSA-AMD] Two-Stage Architecture, Stage 1:
  * each cube is mean-pooled into cube-level Qc, Kc, Vc and attends cube to
  * cube; the final output gates the coarse and fine outputs together):
@@ -300,6 +332,43 @@ vsa_status vsa_sparse_attn_fwd_gated(const void* qt, const void* kt, const void*
                                      vsa_stream_t stream);
 
 /*
+ * Mean-pool block selector with a cumulative threshold ([INT8-WAN]
+ * "Optimizing block-sparse INT8 attention and multi-expert step caching for
+ * Wan 2.2", Decoupling Block Selection from Sparse CUDA Kernels), for token
+ * sequences attended in contiguous 128-token blocks (no cube grid):
+ *   qbar_i, kbar_j = means of the 128 token rows of block i of q, j of k
+ *                    (all 128 rows, padding included; fp32),
+ *   S_ij           = qbar_i . kbar_j,
+ *   row i keeps its key blocks in descending S_ij (equal scores: lower index
+ *   first) until their share of softmax_j(sm_scale * S_ij) reaches tau: at
+ *   least one block, all of them if the share never reaches tau.
+ * Scores, weights and the share are formed in fp32, so a block whose
+ * cumulative share lies within rounding of tau, or whose score ties another
+ * within rounding, may be decided the other way than in exact arithmetic.
+ * The result is written as the fine stage's cube-level table: block j is the
+ * 64-token slot groups 2j and 2j + 1, and query groups 2i and 2i + 1 (block i)
+ * both list the groups of every kept block, ascending, then -1; their count
+ * is twice the kept blocks.  Pass it to vsa_sparse_attn_fwd_ex with
+ * topk = S / 64, these counts, pairs = NULL (the default pairs (2u, 2u + 1)
+ * are then exactly the blocks) and vbs = the real tokens of each 64-token
+ * group (64, or fewer in a zero-padded tail).
+ *   q, k        : bf16 [B, S, heads, D] in the sequence's token order;
+ *                 S a multiple of 128
+ *   tau         : in (0, 1]
+ *   sm_scale    : <= 0 selects 1 / sqrt(D)
+ *   workspace   : vsa_block_select_workspace_bytes(B, S, heads, D) bytes
+ *                 (the fp32 block means), 16-byte aligned, overwritten
+ *   cube_idx    : int32 [B, heads, S / 64, S / 64] (written in full)
+ *   cube_counts : int32 [B, heads, S / 64] (written)
+ * Limits: S <= 32768 (256 blocks); D in {64, 128}; B, heads <= 65535.
+ * Two kernel launches (pooling, selection).
+ */
+size_t vsa_block_select_workspace_bytes(int32_t B, int32_t S, int32_t heads, int32_t D);
+vsa_status vsa_block_select(const void* q, const void* k, int32_t B, int32_t S, int32_t heads, int32_t D,
+                            float tau, float sm_scale, void* workspace, int32_t* cube_idx,
+                            int32_t* cube_counts, vsa_stream_t stream);
+
+/*
  * Debug aid for the block-sparse encoding ([VSA-AMD] Block-Sparse Encoding):
  * checks every topk_idx entry is in [0, ncubes), that no row repeats an
  * index, and that every vbs entry is in [0, 64].  ORs into *dev_flag (device
@@ -311,6 +380,19 @@ vsa_status vsa_sparse_attn_fwd_gated(const void* qt, const void* kt, const void*
 vsa_status vsa_validate_indices(const int32_t* topk_idx, const int32_t* vbs, int32_t B,
                                 int32_t heads, int32_t ncubes, int32_t topk, int32_t* dev_flag,
                                 vsa_stream_t stream);
+
+/*
+ * vsa_validate_indices for a table with per-row counts (the variable-length
+ * encoding vsa_sparse_attn_fwd_ex takes): row r is checked on its first
+ * counts[r] entries only, so padding entries (vsa_table_from_csr writes -1)
+ * are not flagged.  A count outside [0, topk] sets flag bit 8 and the row is
+ * checked on its entries clamped to that range.  counts: int32
+ * [B, heads, ncubes] (device), or NULL for topk everywhere (the same check as
+ * vsa_validate_indices).
+ */
+vsa_status vsa_validate_indices_ex(const int32_t* topk_idx, const int32_t* counts, const int32_t* vbs,
+                                   int32_t B, int32_t heads, int32_t ncubes, int32_t topk,
+                                   int32_t* dev_flag, vsa_stream_t stream);
 
 /*
  * Reads (and with reset != 0 clears) the library's device error word on the
@@ -345,17 +427,21 @@ uint64_t vsa_kernel_launches(void);
  * are host memory; synchronous; no CUDA call.
  *   lut_ptr : int64 [rows + 1], lut_ptr[0] = 0, non-decreasing: row r owns
  *             kv_idx[lut_ptr[r] .. lut_ptr[r + 1])
- *   kv_idx  : int32 [lut_ptr[rows]] (may be NULL when that is 0)
+ *   kv_idx  : int32 [nnz] (may be NULL when lut_ptr[rows] is 0)
+ *   nnz     : the number of entries kv_idx holds; lut_ptr[rows] <= nnz
  *   rows    : B * heads * ncubes, in the row order of topk_idx
  *   width   : the table width (topk); every row must hold <= width entries
+ *   ncubes  : cubes per (batch, head); every used entry must be in
+ *             [0, ncubes)
  *   table   : int32 [rows, width] (written): each row's entries, then -1
  *   counts  : int32 [rows] (written): lut_ptr[r + 1] - lut_ptr[r]
- * Returns VSA_ERR_INVALID_ARG (and writes nothing) on a null pointer,
- * non-positive sizes, lut_ptr[0] != 0, a decreasing offset or a row longer
- * than width.
+ * Returns VSA_ERR_INVALID_ARG on a null pointer, non-positive sizes,
+ * lut_ptr[0] != 0, a decreasing offset, a row longer than width or offsets
+ * that run past nnz, and VSA_ERR_INDEX_RANGE on an entry outside
+ * [0, ncubes); in both cases nothing is written.
  */
-vsa_status vsa_table_from_csr(const int64_t* lut_ptr, const int32_t* kv_idx, int64_t rows, int32_t width,
-                              int32_t* table, int32_t* counts);
+vsa_status vsa_table_from_csr(const int64_t* lut_ptr, const int32_t* kv_idx, int64_t nnz, int64_t rows,
+                              int32_t width, int32_t ncubes, int32_t* table, int32_t* counts);
 
 #ifdef __cplusplus
 }

@@ -39,7 +39,9 @@ def test_header_declares_the_entry_points():
               "vsa_validate_indices", "vsa_device_error", "vsa_debug_wait_timeout",
               "vsa_pair_cubes", "vsa_pair_workspace_bytes", "vsa_sparse_attn_fwd_paired",
               "vsa_sparse_attn_fwd_ex", "vsa_sparse_attn_fwd_gated", "vsa_coarse_attn",
-              "vsa_coarse_attn_workspace_bytes", "vsa_kernel_launches", "vsa_table_from_csr"):
+              "vsa_coarse_attn_workspace_bytes", "vsa_kernel_launches", "vsa_table_from_csr",
+              "vsa_validate_indices_ex", "vsa_coarse_select_noalloc", "vsa_block_select",
+              "vsa_block_select_workspace_bytes", "vsa_sparse_attn_fwd_peak"):
         assert n in names
 
 
@@ -192,6 +194,8 @@ def test_refused_calls_launch_nothing(lib):
 def test_validator_and_debug_validation(lib):
     assert lib.vsa_validate_indices(None, A, 1, 1, 12, 3, A, None) == INVALID
     assert lib.vsa_validate_indices(A, A, 1, 1, 100000, 3, A, None) == UNSUPPORTED
+    assert lib.vsa_validate_indices_ex(None, None, A, 1, 1, 12, 3, A, None) == INVALID
+    assert lib.vsa_validate_indices_ex(A, A + 2, A, 1, 1, 12, 3, A, None) == ALIGNMENT
     assert lib.vsa_debug_wait_timeout(10, A, None) == INVALID
     assert lib.vsa_debug_wait_timeout(10 ** 6, None, None) == INVALID
     assert lib.vsa_device_error(None, 0) == INVALID
@@ -213,7 +217,7 @@ def test_table_from_csr_matches_the_padded_layout():
     lengths[:2] = [0, width]
     lut_ptr = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
     kv_idx = rng.integers(0, N, size=int(lut_ptr[-1])).astype(np.int32)
-    table, counts = vsa.table_from_csr(lut_ptr, kv_idx, width, shape=(B, heads, N))
+    table, counts = vsa.table_from_csr(lut_ptr, kv_idx, width, N, shape=(B, heads, N))
     assert table.shape == (B, heads, N, width) and counts.shape == (B, heads, N)
     flat, cnt = table.reshape(rows, width), counts.reshape(rows)
     for r in range(rows):
@@ -224,9 +228,52 @@ def test_table_from_csr_matches_the_padded_layout():
 
 def test_table_from_csr_refuses_bad_offsets(lib):
     import numpy as np
-    ok_idx = np.zeros(8, np.int32)
+    ok_idx = np.zeros(16, np.int32)
     for bad in ([1, 2, 3], [0, 3, 2], [0, 9, 9]):  # nonzero start, decreasing, row longer than width
         with pytest.raises(vsa.VsaError):
-            vsa.table_from_csr(np.array(bad, np.int64), ok_idx, 4)
-    table, counts = vsa.table_from_csr(np.array([0, 0, 0], np.int64), np.zeros(0, np.int32), 2)
+            vsa.table_from_csr(np.array(bad, np.int64), ok_idx, 4, 6)
+    table, counts = vsa.table_from_csr(np.array([0, 0, 0], np.int64), np.zeros(0, np.int32), 2, 6)
     assert (table == -1).all() and (counts == 0).all()
+
+
+def test_table_from_csr_refuses_short_or_out_of_range_indices(lib):
+    import ctypes
+    import numpy as np
+    lut_ptr = np.array([0, 2, 4], np.int64)
+    with pytest.raises(ValueError, match="kv_idx"):  # the wrapper: kv_idx shorter than lut_ptr[-1]
+        vsa.table_from_csr(lut_ptr, np.zeros(3, np.int32), 2, 6)
+    with pytest.raises(ValueError, match="lut_ptr"):
+        vsa.table_from_csr(np.array([0], np.int64), np.zeros(0, np.int32), 2, 6)
+    # the C entry point itself: nnz below the last offset, and entries outside [0, ncubes)
+    idx = np.array([0, 1, 2, 3], np.int32)
+    table = np.empty((2, 2), np.int32)
+    counts = np.empty(2, np.int32)
+    args = lambda nnz, ncubes, kv: (lut_ptr.ctypes.data, kv.ctypes.data, nnz, 2, 2, ncubes,  # noqa: E731
+                                    table.ctypes.data, counts.ctypes.data)
+    assert lib.vsa_table_from_csr(*args(3, 6, idx)) == INVALID
+    assert lib.vsa_table_from_csr(*args(4, 3, idx)) == 4  # VSA_ERR_INDEX_RANGE: entry 3 >= ncubes
+    assert lib.vsa_table_from_csr(*args(4, 6, np.array([0, -1, 2, 3], np.int32))) == 4
+    assert lib.vsa_table_from_csr(*args(4, 4, idx)) == 0
+    assert table.tolist() == [[0, 1], [2, 3]] and counts.tolist() == [2, 2]
+    with pytest.raises(vsa.VsaError):
+        vsa.table_from_csr(lut_ptr, np.array([0, 1, 7, 3], np.int32), 2, 6)
+
+
+def test_block_select_validation(lib):
+    f = lib.vsa_block_select
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 2 + [ctypes.c_int32] * 4 + [ctypes.c_float] * 2 + [ctypes.c_void_p] * 4
+    ok = (A, A, 1, 1024, 2, 64, 0.5, 0.0, A, A, A, None)
+    bad = lambda i, v: tuple(v if n == i else x for n, x in enumerate(ok))  # noqa: E731
+    assert f(*bad(0, None)) == INVALID
+    assert f(*bad(3, 1000)) == INVALID            # S not a multiple of 128
+    assert f(*bad(6, 0.0)) == INVALID             # tau outside (0, 1]
+    assert f(*bad(6, 1.5)) == INVALID
+    assert f(*bad(5, 96)) == UNSUPPORTED          # D
+    assert f(*bad(3, 32768 + 128)) == UNSUPPORTED  # more than 256 blocks
+    assert f(*bad(8, A + 4)) == ALIGNMENT
+    w = lib.vsa_block_select_workspace_bytes
+    w.restype = ctypes.c_size_t
+    w.argtypes = [ctypes.c_int32] * 4
+    assert w(1, 32768, 12, 128) == 2 * 12 * 256 * 128 * 4
+    assert w(1, 1000, 12, 128) == 0

@@ -38,3 +38,27 @@ def test_validator_flags():
     vb = vbs.copy()
     vb[4] = 65
     assert vsa.validate_indices(i32_dev(good), i32_dev(vb)) & 4
+
+
+def test_validator_with_counts_accepts_a_table_from_compressed_rows():
+    """A table written by vsa_table_from_csr (-1 after each row's entries)
+    validates cleanly with its counts, and still fails without them; a bad
+    entry inside a row's count and a count above topk are both flagged."""
+    rng = np.random.default_rng(11)
+    B, heads, N, width = 1, 2, 12, 5
+    rows = B * heads * N
+    lengths = rng.integers(0, width + 1, size=rows)
+    lengths[:2] = [0, width]
+    lut_ptr = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    kv_idx = np.concatenate([rng.choice(N, size=n, replace=False) for n in lengths]).astype(np.int32)
+    table, counts = vsa.table_from_csr(lut_ptr, kv_idx, width, N, shape=(B, heads, N))
+    vbs = i32_dev(np.full(N, 64, np.int32))
+    assert vsa.validate_indices(i32_dev(table), vbs, counts=i32_dev(counts)) == 0
+    assert vsa.validate_indices(i32_dev(table), vbs) & 1  # the -1 padding, checked as entries
+    bad = table.copy()
+    r = np.argwhere(counts > 0)[0]
+    bad[tuple(r)][0] = N
+    assert vsa.validate_indices(i32_dev(bad), vbs, counts=i32_dev(counts)) & 1
+    big = counts.copy()
+    big.reshape(-1)[0] = width + 1
+    assert vsa.validate_indices(i32_dev(table), vbs, counts=i32_dev(big)) & 8
