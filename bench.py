@@ -48,9 +48,16 @@ WORKLOAD = "wan"
 # was taken from: if fine.cu no longer hashes to `source_sha256`, the traffic is reported
 # as null.
 FINE_TRAFFIC = {
-    "bytes_per_launch": (247.384320e6 + 68.041216e6) * 40 / 8,
+    "bytes_per_launch": (248.616448e6 + 69.268992e6) * 40 / 8,
     "capture": "profiles/fine_fwd_kernel_wan.md",
-    "source_sha256": "8d013deaba8423e25a16d6a81854c84a156f75636f33b45f6956c9b445e693cd",
+    "source_sha256": "44a48d3b787e04f3baab5a4c55a8735929e36a67452d91c811afb17921d14bda",
+}
+# The same for the 128-token-block workload, from a capture of one whole
+# 12-head launch (no scaling).
+FINE_TRAFFIC_BLOCKS = {
+    "bytes_per_launch": 339.878144e6 + 90.351360e6,
+    "capture": "profiles/fine_fwd_kernel_blocks128.md",
+    "source_sha256": "44a48d3b787e04f3baab5a4c55a8735929e36a67452d91c811afb17921d14bda",
 }
 
 
@@ -134,13 +141,26 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ CPU oracle
+def host_cores():
+    """Logical CPUs listed in /proc/cpuinfo (None where it is unreadable)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            return sum(1 for line in f if line.startswith("processor"))
+    except OSError:
+        return None
+
+
 def cpu_oracle_sample(wl, inputs, budget_s: float = 15.0, seed: int = 0):
-    """Times the oracle's fine stage (>99.9% of its work) on sampled query
-    cubes of the workload; returns (effective TFLOPS, threads, description)."""
+    """The oracle pipeline on the host cores: tile (q, k, v) and the coarse
+    selection in full, the fine stage (>99.9% of the work) on random query
+    cubes for about `budget_s` seconds with every thread, then on a fixed
+    subset with one thread.  Returns the cpu_baseline object."""
     import oracle
+    t0 = time.perf_counter()
     qt, vbs = oracle.tile(inputs["q"], wl.grid)
     kt, _ = oracle.tile(inputs["k"], wl.grid)
     vt, _ = oracle.tile(inputs["v"], wl.grid)
+    t_tile = time.perf_counter() - t0
     t0 = time.perf_counter()
     idx = oracle.coarse(qt, kt, vbs, wl.topk, wl.sm_scale)
     t_coarse = time.perf_counter() - t0
@@ -156,10 +176,24 @@ def cpu_oracle_sample(wl, inputs, budget_s: float = 15.0, seed: int = 0):
         _, _, used = oracle.fine(qt, kt, vt, idx, vbs, wl.sm_scale, units)
         elapsed += time.perf_counter() - t0
         done_units += batch
+    per_unit = elapsed / done_units
     tflops = done_units * flops_per_unit / elapsed / 1e12
-    desc = (f"fine stage on {done_units} random query cubes of {units_total} "
-            f"({elapsed:.1f} s, {used} threads); full coarse stage took {t_coarse:.1f} s (untimed)")
-    return tflops, used, desc, elapsed / done_units
+    one = np.arange(8, dtype=np.int64)  # fixed subset: the first 8 query cubes of head 0
+    t0 = time.perf_counter()
+    oracle.fine(qt, kt, vt, idx, vbs, wl.sm_scale, one, nthreads=1)
+    t_one = time.perf_counter() - t0
+    fine_full_s = per_unit * units_total
+    desc = (f"tile of q, k, v and the coarse selection in full; the fine stage on {done_units} random "
+            f"query cubes of {units_total} ({elapsed:.1f} s, {used} threads), its whole-call time "
+            f"extrapolated from that sample")
+    return {"value": tflops, "unit": UNIT, "cores": used, "kind": "oracle", "sample": desc,
+            "host_cpus": host_cores(),
+            "stage_seconds": {"tile_qkv": t_tile, "coarse_select": t_coarse,
+                              "fine_extrapolated": fine_full_s,
+                              "whole_call_extrapolated": t_tile + t_coarse + fine_full_s},
+            "one_thread": {"units": int(one.size), "seconds": t_one,
+                           "tflops": one.size * flops_per_unit / t_one / 1e12,
+                           "subset": "the first 8 query cubes of head 0"}}
 
 
 def reference_arm(args, wl, inputs):
@@ -197,12 +231,15 @@ def reference_arm(args, wl, inputs):
     }
 
 
-def fine_traffic():
+def fine_traffic(record=None):
+    """DRAM bytes per launch of the fine kernel from its ncu capture, or None
+    once fine.cu no longer hashes to the source the capture was taken from."""
     import hashlib
+    record = FINE_TRAFFIC if record is None else record
     path = os.path.join(HERE, "block_sparse_video_vsa_gb300", "csrc", "fine.cu")
     with open(path, "rb") as f:
         digest = hashlib.sha256(f.read()).hexdigest()
-    return FINE_TRAFFIC["bytes_per_launch"] if digest == FINE_TRAFFIC["source_sha256"] else None
+    return record["bytes_per_launch"] if digest == record["source_sha256"] else None
 
 
 def stage_bytes(wl):
@@ -348,7 +385,8 @@ def run_blocks(args, rank, world, dist):
         "stages_hbm_gbs": {"block_select": sel_bytes / (statistics.median(stage["block_select"]) * 1e-3) / 1e9},
         "hbm_peak_gbs": hbm,
         "roofline": {"bound": "tensor", "achieved": fine_tflops, "peak": burst, "unit": "TFLOP/s",
-                     "frac": fine_tflops / burst, "traffic": None, "peak_kind": f"{peak_kind} dense bf16 burst",
+                     "frac": fine_tflops / burst, "traffic": fine_traffic(FINE_TRAFFIC_BLOCKS),
+                     "peak_kind": f"{peak_kind} dense bf16 burst",
                      "kernel": "fine_fwd_kernel (vsa_sparse_attn_fwd with the selector's counts)"},
         "e2e": None if e2e is None else {
             "value": whole_job_throughput(world, flops, e2e[0]), "unit": UNIT, "ms_per_step": e2e[0],
@@ -593,6 +631,7 @@ def time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream,
         return statistics.median(ts)
 
     ca_ms = median_ms(lambda: vsa.coarse_attn(qt, kt, vt, vbs, wl.sm_scale, workspace=ws, out=oc))
+    quality = selection_quality(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, stream)
     fg_ms = median_ms(lambda: vsa.sparse_attn_fwd(qt, kt, vt, idx, vbs, wl.sm_scale, out=ot, lse=lse, pairs=pairs,
                                                   coarse_out=oc, gate_c=gc, gate_f=gf))
     if vsa.device_error(reset=True):
@@ -606,7 +645,40 @@ def time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream,
         "sparse_attn_fwd_gated": {"ms_median": fg_ms, "effective_tflops": wl.fine_flops() / (fg_ms * 1e-3) / 1e12,
                                   "extra_hbm_bytes": 2 * wl.B * wl.s_pad * wl.heads * wl.D * 2,
                                   "note": "fine stage + gate_c * coarse + gate_f * fine in the epilogue"},
+        "quality": quality,
     }
+
+
+def selection_quality(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, stream):
+    """Quality of the coarse selection against dense attention, measured with
+    the fine stage itself: the dense reference selects every cube (topk = N).
+    recall = mean over real query rows of exp(lse_selected - lse_dense), the
+    share of each row's dense softmax mass its selection captures; rel_l1 =
+    mean |o_sparse - o_dense| / mean |o_dense| over real rows; max_prob = the
+    mean largest softmax weight of the selected rows."""
+    N = wl.ncubes
+    if N > 1024:
+        return None  # the fine stage takes at most 1024 cubes per row
+    dense = vsa.all_cubes(wl.B, wl.heads, N, device=qt.device)
+    o_s, lse_s, mp = vsa.sparse_attn_fwd_peak(qt, kt, vt, idx, vbs, wl.sm_scale, pairs=pairs)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    o_d, lse_d = vsa.sparse_attn_fwd(qt, kt, vt, dense, vbs, wl.sm_scale)  # warm-up
+    a.record(stream)
+    o_d, lse_d = vsa.sparse_attn_fwd(qt, kt, vt, dense, vbs, wl.sm_scale, out=o_d, lse=lse_d)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if vsa.device_error(reset=True):
+        raise RuntimeError("device error word set during the dense reference run")
+    real = (torch.arange(64, device=qt.device)[None, :] < vbs[:, None]).reshape(-1)  # [S_pad] real slots
+    cm = torch.exp(lse_s.double() - lse_d.double())[..., real]
+    diff = (o_s.float() - o_d.float()).abs()[:, real]
+    dense_flops = 4.0 * wl.B * wl.s_pad * N * 64 * wl.D * wl.heads
+    return {"recall_captured_mass_mean": float(cm.mean()), "recall_captured_mass_p05": float(cm.quantile(0.05)),
+            "rel_l1_vs_dense": float(diff.mean() / o_d.float().abs()[:, real].mean()),
+            "max_prob_mean": float(mp[..., real].double().mean()),
+            "dense_reference_ms": a.elapsed_time(b),
+            "dense_reference_tflops": dense_flops / (a.elapsed_time(b) * 1e-3) / 1e12,
+            "note": "dense reference = the fine stage with every cube selected; real query rows only"}
 
 
 def main():
@@ -692,8 +764,7 @@ def main():
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        tflops, cores, desc, _ = cpu_oracle_sample(wl, inputs, args.cpu_budget)
-        result["cpu_baseline"] = {"value": tflops, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        result["cpu_baseline"] = cpu_oracle_sample(wl, inputs, args.cpu_budget)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist:
