@@ -246,10 +246,12 @@ def stage_bytes(wl):
     """Algorithmic HBM bytes per call of the memory-bound stages."""
     real = wl.B * wl.tokens * wl.heads * wl.D * 2
     tiled = wl.B * wl.s_pad * wl.heads * wl.D * 2
+    cubes = wl.B * wl.heads * wl.ncubes
+    pooled = 16 * cubes * wl.D + 8 * cubes              # means + residuals of q, k (fp32), norms
     return {
-        "tile_qk": 2 * (real + tiled),                       # read raster rows, write every slot
+        "tile_qk_pool": 2 * (real + tiled) + pooled,        # read raster rows, write every slot + statistics
         "tile_v": real + tiled,                              # side stream, beside the pairing
-        "coarse_select": 2 * tiled + 4 * wl.B * wl.heads * wl.ncubes * wl.topk,  # read q, k; write idx
+        "coarse_select": 8 * cubes * wl.D + 8 * cubes + 4 * cubes * wl.topk,  # read means, norms; write idx
         "untile": 2 * real,                                  # read real slots, write raster rows
     }
 
@@ -458,11 +460,12 @@ def run_ours(args, wl, inputs, rank, world, dist):
         oout = out if oout is None else oout
         if marks is not None:
             marks[0].record(stream)
-        vsa.tile(qin, grid, out=qt, vbs=vbs)
-        vsa.tile(kin, grid, out=kt, vbs=vbs2)
+        # q and k are tiled and pooled in one pass; the selection starts from
+        # the pooled statistics the tiling left in the workspace.
+        vsa.tile_pool(qin, kin, grid, qt=qt, kt=kt, vbs=vbs, workspace=ws)
         if marks is not None:
             marks[1].record(stream)
-        vsa.coarse_select(qt, kt, vbs, wl.topk, wl.sm_scale, workspace=ws, out=idx)
+        vsa.coarse_select_pooled(ws, vbs, wl.B, wl.heads, wl.D, wl.topk, wl.sm_scale, out=idx)
         ev_coarse.record(stream)
         if marks is not None:
             marks[2].record(stream)
@@ -512,7 +515,7 @@ def run_ours(args, wl, inputs, rank, world, dist):
     ms_total = max_over_ranks(start.elapsed_time(end), dist, dev)
     ms_step = ms_total / args.steps
     stage = {name: [marks[s][i].elapsed_time(marks[s][i + 1]) for s in range(args.steps)]
-             for i, name in enumerate(["tile_qk", "coarse_select", "pair_cubes", "sparse_attn_fwd", "untile"])}
+             for i, name in enumerate(["tile_qk_pool", "coarse_select", "pair_cubes", "sparse_attn_fwd", "untile"])}
     stage["tile_v"] = [marks[s][6].elapsed_time(marks[s][7]) for s in range(args.steps)]  # side stream
     if vsa.device_error(reset=True):
         raise RuntimeError("device error word set during the timed run")

@@ -62,6 +62,10 @@ def _declare(lib):
     lib.vsa_coarse_workspace_bytes.argtypes = [_i32] * 4
     lib.vsa_coarse_select.restype = ctypes.c_int
     lib.vsa_coarse_select.argtypes = [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _p, _p, _p]
+    lib.vsa_tile_pool.restype = ctypes.c_int
+    lib.vsa_tile_pool.argtypes = [ctypes.POINTER(VsaGrid), _p, _p, _p, _p, _p, _p, _p]
+    lib.vsa_coarse_select_pooled.restype = ctypes.c_int
+    lib.vsa_coarse_select_pooled.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _p, _p, _p]
     lib.vsa_sparse_attn_fwd.restype = ctypes.c_int
     lib.vsa_sparse_attn_fwd.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_float,
                                         _p, _p, _p]
@@ -221,6 +225,66 @@ def coarse_select(qt, kt, vbs, topk: int, sm_scale: float = 0.0, workspace=None,
     _check(library().vsa_coarse_select(qt.data_ptr(), kt.data_ptr(), vbs.data_ptr(), B, N, heads, D, int(topk),
                                        float(sm_scale), workspace.data_ptr(), out.data_ptr(), _stream(stream)),
            "vsa_coarse_select")
+    return out
+
+
+def tile_pool(q, k, grid, qt=None, kt=None, vbs=None, workspace=None, stream=None):
+    """Tile q and k and pool their cubes in one pass (vsa_tile_pool).
+
+    Returns (qt, kt, vbs, workspace); pass vbs and workspace to
+    coarse_select_pooled for the same top-k as coarse_select(qt, kt, vbs, ...)."""
+    torch = _torch()
+    _need(q, torch.bfloat16, "q")
+    _need(k, torch.bfloat16, "k")
+    if k.shape != q.shape:
+        raise ValueError("q and k must share a [B, T*H*W, heads, D] shape")
+    B, S, heads, D = q.shape
+    g = _grid(grid, heads, D)
+    if (g.B, g.T * g.H * g.W) != (B, S):
+        raise ValueError("q shape does not match the grid")
+    N = num_cubes(grid)
+    shape = (B, 64 * N, heads, D)
+    if qt is None:
+        qt = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
+    if kt is None:
+        kt = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
+    if vbs is None:
+        vbs = torch.empty((N,), dtype=torch.int32, device=q.device)
+    nbytes = coarse_workspace_bytes(B, heads, N, D)
+    if workspace is None:
+        workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=q.device)
+    for t, n in ((qt, "qt"), (kt, "kt")):
+        _need(t, torch.bfloat16, n)
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{n} must be {shape}")
+    _need(vbs, torch.int32, "vbs")
+    _need(workspace, torch.uint8, "workspace")
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    _check(library().vsa_tile_pool(ctypes.byref(g), q.data_ptr(), k.data_ptr(), qt.data_ptr(), kt.data_ptr(),
+                                   vbs.data_ptr(), workspace.data_ptr(), _stream(stream)), "vsa_tile_pool")
+    return qt, kt, vbs, workspace
+
+
+def coarse_select_pooled(workspace, vbs, B: int, heads: int, D: int, topk: int, sm_scale: float = 0.0, out=None,
+                         stream=None):
+    """Top-k key cubes per query cube from the statistics tile_pool wrote
+    -> int32 [B, heads, N, topk] (N = vbs.numel())."""
+    torch = _torch()
+    _need(vbs, torch.int32, "vbs")
+    _need(workspace, torch.uint8, "workspace")
+    N = vbs.numel()
+    nbytes = coarse_workspace_bytes(B, heads, N, D)
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    if out is None:
+        out = torch.empty((B, heads, N, int(topk)), dtype=torch.int32, device=vbs.device)
+    _need(out, torch.int32, "out")
+    if tuple(out.shape) != (B, heads, N, int(topk)):
+        raise ValueError("out must be [B, heads, N, topk]")
+    _check(library().vsa_coarse_select_pooled(vbs.data_ptr(), int(B), N, int(heads), int(D), int(topk),
+                                              float(sm_scale), workspace.data_ptr(), out.data_ptr(),
+                                              _stream(stream)), "vsa_coarse_select_pooled")
     return out
 
 
@@ -485,10 +549,10 @@ def pipeline(q, k, v, grid, topk: int, sm_scale: float = 0.0, stream=None):
     """Whole hot path on raster inputs: tile -> coarse select -> (pairing) -> sparse attention -> untile.
 
     Returns (out raster bf16, lse fp32 [B, heads, 64*N] in cube-major order, topk_idx)."""
-    qt, vbs = tile(q, grid, stream=stream)
-    kt, _ = tile(k, grid, vbs=_torch().empty_like(vbs), stream=stream)
+    qt, kt, vbs, ws = tile_pool(q, k, grid, stream=stream)
     vt, _ = tile(v, grid, vbs=_torch().empty_like(vbs), stream=stream)
-    idx = coarse_select(qt, kt, vbs, topk, sm_scale, stream=stream)
+    B, _, heads, D = q.shape
+    idx = coarse_select_pooled(ws, vbs, B, heads, D, topk, sm_scale, stream=stream)
     pairs = pair_cubes(idx, stream=stream)
     ot, lse = sparse_attn_fwd(qt, kt, vt, idx, vbs, sm_scale, pairs=pairs, stream=stream)
     return untile(ot, grid, stream=stream), lse, idx

@@ -139,8 +139,42 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
     const size_t smem = coarse_smem_bytes(ncubes, D, split);
     if (smem > (size_t)ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
-    return from_cuda(launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, workspace, topk_idx, split,
+    return from_cuda(launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, workspace, topk_idx, split, false,
                                    static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status vsa_tile_pool(const vsa_grid* g, const void* q, const void* k, void* qt, void* kt, int32_t* vbs,
+                         void* workspace, vsa_stream_t stream) {
+    if (!grid_ok(g) || !q || !k || !qt || !kt || !workspace) return VSA_ERR_INVALID_ARG;
+    if (g->D != 64 && g->D != 128) return VSA_ERR_UNSUPPORTED;
+    const int64_t N = cubes_of(g);
+    if (N > 4096 || !sizes_fit(g->B, N * 64, g->heads, g->D) || (int64_t)g->T * g->H * g->W >= ((int64_t)1 << 31))
+        return VSA_ERR_UNSUPPORTED;
+    if ((int64_t)g->B * N > 2147483647 || g->heads > 65535) return VSA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(qt) || !aligned16(kt) || !aligned16(workspace) ||
+        (vbs && (reinterpret_cast<uintptr_t>(vbs) & 3u)))
+        return VSA_ERR_ALIGNMENT;
+    return from_cuda(launch_tile_pool(*g, (int)N, q, k, qt, kt, vbs, workspace, static_cast<cudaStream_t>(stream)));
+}
+
+vsa_status vsa_coarse_select_pooled(const int32_t* vbs, int32_t B, int32_t ncubes, int32_t heads, int32_t D,
+                                    int32_t topk, float sm_scale, void* workspace, int32_t* topk_idx,
+                                    vsa_stream_t stream) {
+    if (!vbs || !workspace || !topk_idx) return VSA_ERR_INVALID_ARG;
+    if (B <= 0 || ncubes <= 0 || heads <= 0 || topk <= 0 || topk > ncubes) return VSA_ERR_INVALID_ARG;
+    if (!(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return VSA_ERR_UNSUPPORTED;
+    if (ncubes > 4096 || !sizes_fit(B, (int64_t)ncubes * 64, heads, D)) return VSA_ERR_UNSUPPORTED;
+    if (!aligned16(workspace) || !aligned16(vbs) || (reinterpret_cast<uintptr_t>(topk_idx) & 3u))
+        return VSA_ERR_ALIGNMENT;
+    DevCtx ctx;
+    cudaError_t e = get_dev_ctx(&ctx);
+    if (e != cudaSuccess) return VSA_ERR_CUDA;
+    const bool split = coarse_split_default(ncubes, D);
+    if (coarse_smem_bytes(ncubes, D, split) > (size_t)ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
+    if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
+    return from_cuda(launch_coarse(nullptr, nullptr, vbs, B, ncubes, heads, D, topk, sm_scale, workspace, topk_idx,
+                                   split, true, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

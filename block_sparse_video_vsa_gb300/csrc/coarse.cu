@@ -6,61 +6,33 @@
 // cubes per query cube; Generating Sparsity Patterns -- pool, score einsum,
 // top-k over the last axis) with the score scaled by sm_scale.
 //
-// Pipeline (two kernels):
+// Pipeline:
 //  1. pool_kernel -- per (batch, cube, q|k): channel sums over the vbs real
 //     tokens, accumulated error-free as fp32 (hi, lo) pairs (TwoSum), stored
 //     as the fp32 mean m = fl(fl(hi + lo) / vbs) and the fp32 residual
 //     r = (hi + lo) - m * vbs (TwoProduct, exact up to one rounding), plus the
-//     fp32 norm of every cube's mean vector per head.  HBM bound: reads each
-//     tiled tensor once.
+//     fp32 norm of every cube's mean vector per head (pool_sum.cuh).  HBM
+//     bound: reads each tiled tensor once.  Skipped when tile_pool_kernel
+//     (tile.cu) already wrote the same statistics while tiling q and k.
 //  2. score_topk_kernel -- per (batch, head, block of R query cubes): fp32
 //     scores against every key cube (FFMA; key means streamed into shared
 //     memory by asynchronous copies, double buffered), then per row a bitwise radix
 //     select of the k-th largest score.  Scores within a proven fp32 error
 //     bound of that boundary are re-ranked in fp64 with the exact cube sums
-//     m * vbs + r, so the set matches exact-arithmetic top-k.
+//     m * vbs + r, so the set matches exact-arithmetic top-k.  From 256 cubes
+//     the scores go through memory instead (score_gemm_kernel, then
+//     select_kernel, one warp per row, with the same selection).
 #include <float.h>
 
 #include <type_traits>
 
-#include "vsa_common.cuh"
+#include "pool_sum.cuh"
 
 namespace vsa {
 
 namespace {
 
 // ------------------------------------------------------------------ pooling
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-    s = a + b;
-    const float bb = s - a;
-    e = (a - (s - bb)) + (b - bb);
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ void accumulate8(const uint4 w, float (&hi)[8], float (&lo)[8]) {
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        float s, err;
-        two_sum(hi[2 * e], bf16_lo(ww[e]), s, err);
-        hi[2 * e] = s;
-        lo[2 * e] += err;
-        two_sum(hi[2 * e + 1], bf16_hi(ww[e]), s, err);
-        hi[2 * e + 1] = s;
-        lo[2 * e + 1] += err;
-    }
-}
-
-// Workspace planes (floats): mean [2][B][heads][ncubes][D] (q then k),
-// residual likewise, then norm [2][B][heads][ncubes].
-struct PoolOut {
-    float* mean;
-    float* resid;
-    float* norm;
-};
-
 // grid: (B * ncubes, 2 [q, k]); threads stride over the 8-channel vectors of
 // a token row (heads * D / 8 of them); D / 8 consecutive threads hold one
 // head's row, so the norm is a reduction over that lane group.
@@ -72,9 +44,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint4* __restrict__ qt,
     const int which = blockIdx.y;
     const uint4* src = which == 0 ? qt : kt;
     const int row_vecs = heads * D / 8;
-    const int gsz = D / 8;
     const int vb = min(max(vbs[c], 0), kCubeTokens);
-    const float fv = (float)vb;
     const size_t s_pad = (size_t)ncubes * kCubeTokens;
     const uint4* base = src + ((size_t)b * s_pad + (size_t)c * kCubeTokens) * row_vecs;
     for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) {
@@ -90,34 +60,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint4* __restrict__ qt,
             for (int u = 0; u < 8; ++u) accumulate8(w[u], hi, lo);
         }
         for (; r < vb; ++r) accumulate8(__ldcs(base + (size_t)r * row_vecs + v), hi, lo);
-        float m[8], rr[8];
-        float s2 = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            if (vb > 0) {
-                m[e] = (hi[e] + lo[e]) / fv;
-                const float p = m[e] * fv;
-                const float pe = fmaf(m[e], fv, -p);  // m * vb = p + pe exactly
-                rr[e] = (hi[e] - p) + (lo[e] - pe);
-            } else {
-                m[e] = rr[e] = 0.f;
-            }
-            s2 = fmaf(m[e], m[e], s2);
-        }
-        const int ch = v * 8;
-        const int h = ch / D;
-        const int d = ch - h * D;
-        const size_t row = (((size_t)which * B + b) * heads + h) * ncubes + c;
-        const size_t off = row * D + d;
-        *reinterpret_cast<float4*>(o.mean + off) = make_float4(m[0], m[1], m[2], m[3]);
-        *reinterpret_cast<float4*>(o.mean + off + 4) = make_float4(m[4], m[5], m[6], m[7]);
-        *reinterpret_cast<float4*>(o.resid + off) = make_float4(rr[0], rr[1], rr[2], rr[3]);
-        *reinterpret_cast<float4*>(o.resid + off + 4) = make_float4(rr[4], rr[5], rr[6], rr[7]);
-        // Whole lane groups are active together (row_vecs and blockDim are
-        // multiples of gsz), so the xor partners below are always active.
-        const unsigned act = __activemask();
-        for (int x = 1; x < gsz; x <<= 1) s2 += __shfl_xor_sync(act, s2, x);
-        if ((v & (gsz - 1)) == 0) o.norm[row] = sqrtf(s2);
+        pool_finish(hi, lo, vb, v, which, b, c, o, B, ncubes, heads, D);
     }
 }
 
@@ -667,20 +610,19 @@ size_t coarse_smem_bytes(int N, int D, bool split) {
 
 cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes,
                           int heads, int D, int topk, float sm_scale, void* workspace,
-                          int32_t* topk_idx, bool split, cudaStream_t stream) {
-    float* ws = static_cast<float*>(workspace);
+                          int32_t* topk_idx, bool split, bool pooled, cudaStream_t stream) {
     const size_t half = (size_t)B * heads * ncubes * D;  // one [B][heads][N][D] plane
-    PoolOut po;
-    po.mean = ws;                  // q, then k
-    po.resid = ws + 2 * half;      // q, then k
-    po.norm = ws + 4 * half;       // q [B][heads][N], then k
-    const int row_vecs = heads * D / 8;
-    dim3 pg(B * ncubes, 2);
-    pool_kernel<<<pg, row_vecs < 256 ? ((row_vecs + 31) / 32) * 32 : 256, 0, stream>>>(
-        static_cast<const uint4*>(qt), static_cast<const uint4*>(kt), vbs, po, B, ncubes, heads, D);
-    note_launches(1);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const PoolOut po = pool_planes(workspace, B, heads, ncubes, D);
+    cudaError_t e;
+    if (!pooled) {
+        const int row_vecs = heads * D / 8;
+        dim3 pg(B * ncubes, 2);
+        pool_kernel<<<pg, row_vecs < 256 ? ((row_vecs + 31) / 32) * 32 : 256, 0, stream>>>(
+            static_cast<const uint4*>(qt), static_cast<const uint4*>(kt), vbs, po, B, ncubes, heads, D);
+        note_launches(1);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
 
     ScoreArgs a;
     a.qm = po.mean;

@@ -91,7 +91,7 @@ extern "C" vsa_status vsa_coarse_select_noalloc(const void* qt, const void* kt, 
     void* scratch = nullptr;
     if (scratch_for_current_device(static_cast<cudaStream_t>(stream), &scratch) != cudaSuccess) return VSA_ERR_CUDA;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
-    return launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, scratch, topk_idx, split,
+    return launch_coarse(qt, kt, vbs, B, ncubes, heads, D, topk, sm_scale, scratch, topk_idx, split, false,
                          static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? VSA_OK
                : VSA_ERR_CUDA;

@@ -347,7 +347,7 @@ __device__ __forceinline__ void exp64(const float* x, float c2, float mb, uint32
     l += (s01.x + s01.y) + (s23.x + s23.y);
 }
 
-template <int kD, bool kGated>
+template <int kD, bool kGated, bool kPeak>
 __global__ void __launch_bounds__(kThreads, 1)
     fine_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     FineParams p) {
@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lmax = fmaxf(lmax, max64(x + 64));
                 }
                 lmax *= c2;
-                mx = fmaxf(mx, lmax);
+                if constexpr (kPeak) mx = fmaxf(mx, lmax);
                 // Lazy running max: rescale O and l only on a jump > threshold.
                 float alpha = 1.f;
                 if (lmax > m + kRescaleThreshold) {
@@ -761,10 +761,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             //   out = (a_0 O_0 + a_1 O_1) / l, lse = (m + log2 l) ln 2.
             ms.xm[lb][G][r] = m;
             ms.xl[lb][G][r] = l;
-            ms.xt[lb][G][r] = mx;
+            if constexpr (kPeak) ms.xt[lb][G][r] = mx;
             named_sync(1 + quarter, 2 * 32);
             const float mo = ms.xm[lb][G ^ 1][r], lo = ms.xl[lb][G ^ 1][r];
-            const float m_true = fmaxf(mx, ms.xt[lb][G ^ 1][r]);
+            const float m_true = kPeak ? fmaxf(mx, ms.xt[lb][G ^ 1][r]) : ninf;
             const float m0 = G ? mo : m, l0 = G ? lo : l;
             const float m1 = G ? m : mo, l1 = G ? l : lo;
             // A group that took no step of this unit holds no O for it.
@@ -853,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float lse2 = lt > 0.f ? mt + __log2f(lt) : ninf;  // log2 units
                 if (p.lse) p.lse[at] = lt > 0.f ? lse2 * 0.69314718055994531f : ninf;
                 // The largest softmax weight of the row: 2^(exact max - lse).
-                if (p.max_prob) p.max_prob[at] = lt > 0.f ? ex2_approx(m_true - lse2) : 0.f;
+                if constexpr (kPeak) p.max_prob[at] = lt > 0.f ? ex2_approx(m_true - lse2) : 0.f;
             }
             g = g0 + nst;
         }
@@ -935,8 +935,13 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     p.npairs = (ncubes + 1) / 2;
     p.num_units = B * heads * p.npairs;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
-    auto kernel = coarse_out ? (D == 64 ? fine_fwd_kernel<64, true> : fine_fwd_kernel<128, true>)
-                             : (D == 64 ? fine_fwd_kernel<64, false> : fine_fwd_kernel<128, false>);
+    // The exact row maximum behind max_prob is tracked only in the peak
+    // instantiation (it costs about 1% of the ungated kernel's time); the peak
+    // entry point runs ungated.
+    if (max_prob && coarse_out) return cudaErrorInvalidValue;
+    auto kernel = coarse_out ? (D == 64 ? fine_fwd_kernel<64, true, false> : fine_fwd_kernel<128, true, false>)
+                  : max_prob ? (D == 64 ? fine_fwd_kernel<64, false, true> : fine_fwd_kernel<128, false, true>)
+                             : (D == 64 ? fine_fwd_kernel<64, false, false> : fine_fwd_kernel<128, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     // The setmaxnreg split is sized for a launch of exactly kLaunchRegs

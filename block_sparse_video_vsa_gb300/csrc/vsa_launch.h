@@ -19,6 +19,8 @@ bool sizes_fit(int64_t B, int64_t rows, int64_t heads, int64_t D);
 cudaError_t launch_tile(const vsa_grid& g, int ncubes, const void* x, void* xt, int32_t* vbs,
                         cudaStream_t stream);
 cudaError_t launch_untile(const vsa_grid& g, int ncubes, const void* yt, void* y, cudaStream_t stream);
+cudaError_t launch_tile_pool(const vsa_grid& g, int ncubes, const void* q, const void* k, void* qt, void* kt,
+                             int32_t* vbs, void* workspace, cudaStream_t stream);
 
 // coarse.cu
 bool coarse_split_default(int ncubes, int D);
@@ -27,7 +29,7 @@ size_t coarse_smem_bytes(int N, int D, bool split);
 int coarse_rows_per_block(int ncubes, int D);
 cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, int B, int ncubes, int heads,
                           int D, int topk, float sm_scale, void* workspace, int32_t* topk_idx,
-                          bool split, cudaStream_t stream);
+                          bool split, bool pooled, cudaStream_t stream);
 cudaError_t launch_validate(const int32_t* idx, const int32_t* counts, const int32_t* vbs, int rows, int ncubes,
                             int topk, int32_t* flag, cudaStream_t stream);
 int validate_max_cubes();

@@ -7,6 +7,8 @@
  *                          count vbs;
  *   2. vsa_coarse_select   cube mean-pool of Q and K, cube-to-cube scores and
  *                          the top-k key/value cubes per query cube;
+ *      (vsa_tile_pool + vsa_coarse_select_pooled: steps 1 and 2 with one
+ *                          read of q and k; same results)
  *   3. vsa_sparse_attn_fwd non-causal block-sparse attention over the selected
  *                          cubes, padded tokens masked (bf16 out + fp32 LSE);
  *      (vsa_pair_cubes     optional schedule for step 3: which query cubes
@@ -156,6 +158,36 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
                              int32_t ncubes, int32_t heads, int32_t D, int32_t topk,
                              float sm_scale, void* workspace, int32_t* topk_idx,
                              vsa_stream_t stream);
+
+/*
+ * Steps 1 and 2 with one read of q and k: vsa_tile of q and of k in a single
+ * launch that also writes, into `workspace`, the pooled cube statistics the
+ * coarse selection starts from (the same bits vsa_coarse_select computes from
+ * the tiled tensors), then vsa_coarse_select_pooled scores and selects from
+ * them without reading qt and kt again.  Same sources as vsa_tile and
+ * vsa_coarse_select; no counterpart of its own on the pages: it fuses two of
+ * their steps.
+ *   q, k      : raster bf16 [B, T*H*W, heads, D]        (read)
+ *   qt, kt    : tiled bf16 [B, 64*ncubes, heads, D]    (written as vsa_tile)
+ *   vbs       : int32 [ncubes] or NULL                  (written as vsa_tile)
+ *   workspace : vsa_coarse_workspace_bytes(B, heads, ncubes, D) bytes,
+ *               16-byte aligned; its pooled-statistics head is written
+ * Limits: D in {64, 128}; ncubes <= 4096 (those of vsa_coarse_select).
+ */
+vsa_status vsa_tile_pool(const vsa_grid* g, const void* q, const void* k, void* qt, void* kt, int32_t* vbs,
+                         void* workspace, vsa_stream_t stream);
+
+/*
+ * vsa_coarse_select on statistics vsa_tile_pool left in `workspace` (same
+ * B, heads, ncubes, D; nothing else may have written the workspace since):
+ * the same topk_idx bits, without reading the tiled q and k.
+ *   vbs       : int32 [ncubes] as vsa_tile_pool wrote it
+ *   workspace : the buffer vsa_tile_pool wrote (read; its score area written)
+ *   other arguments, results and errors as vsa_coarse_select.
+ */
+vsa_status vsa_coarse_select_pooled(const int32_t* vbs, int32_t B, int32_t ncubes, int32_t heads, int32_t D,
+                                    int32_t topk, float sm_scale, void* workspace, int32_t* topk_idx,
+                                    vsa_stream_t stream);
 
 /*
  * vsa_coarse_select without a workspace argument, for callers that cannot
