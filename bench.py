@@ -250,7 +250,7 @@ def stage_bytes(wl):
     pooled = 16 * cubes * wl.D + 8 * cubes              # means + residuals of q, k (fp32), norms
     return {
         "tile_qk_pool": 2 * (real + tiled) + pooled,        # read raster rows, write every slot + statistics
-        "tile_v": real + tiled,                              # side stream, beside the pairing
+        "tile_v": real + tiled,                              # side stream, beside the coarse selection
         "coarse_select": 8 * cubes * wl.D + 8 * cubes + 4 * cubes * wl.topk,  # read means, norms; write idx
         "untile": 2 * real,                                  # read real slots, write raster rows
     }
@@ -449,9 +449,11 @@ def run_ours(args, wl, inputs, rank, world, dist):
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
     # Tiling v needs neither the coarse selection nor the pairing, so it runs on
-    # a side stream while the pairing kernels (one CTA per head) run.
+    # a side stream beside the coarse selection (a latency-bound GEMM and
+    # per-row selection, which leave HBM bandwidth to spare); the pairing
+    # kernels (one CTA per head) then run alone.
     side = torch.cuda.Stream()
-    ev_coarse, ev_v = torch.cuda.Event(), torch.cuda.Event()
+    ev_qk, ev_v = torch.cuda.Event(), torch.cuda.Event()
 
     def step(marks=None, qin=None, kin=None, vin=None, oout=None):
         qin = q if qin is None else qin
@@ -463,13 +465,8 @@ def run_ours(args, wl, inputs, rank, world, dist):
         # q and k are tiled and pooled in one pass; the selection starts from
         # the pooled statistics the tiling left in the workspace.
         vsa.tile_pool(qin, kin, grid, qt=qt, kt=kt, vbs=vbs, workspace=ws)
-        if marks is not None:
-            marks[1].record(stream)
-        vsa.coarse_select_pooled(ws, vbs, wl.B, wl.heads, wl.D, wl.topk, wl.sm_scale, out=idx)
-        ev_coarse.record(stream)
-        if marks is not None:
-            marks[2].record(stream)
-        side.wait_event(ev_coarse)
+        ev_qk.record(stream)
+        side.wait_event(ev_qk)
         with torch.cuda.stream(side):
             if marks is not None:
                 marks[6].record(side)
@@ -477,6 +474,11 @@ def run_ours(args, wl, inputs, rank, world, dist):
             if marks is not None:
                 marks[7].record(side)
             ev_v.record(side)
+        if marks is not None:
+            marks[1].record(stream)
+        vsa.coarse_select_pooled(ws, vbs, wl.B, wl.heads, wl.D, wl.topk, wl.sm_scale, out=idx)
+        if marks is not None:
+            marks[2].record(stream)
         vsa.pair_cubes(idx, workspace=pws, out=pairs)
         if marks is not None:
             marks[3].record(stream)
@@ -516,7 +518,7 @@ def run_ours(args, wl, inputs, rank, world, dist):
     ms_step = ms_total / args.steps
     stage = {name: [marks[s][i].elapsed_time(marks[s][i + 1]) for s in range(args.steps)]
              for i, name in enumerate(["tile_qk_pool", "coarse_select", "pair_cubes", "sparse_attn_fwd", "untile"])}
-    stage["tile_v"] = [marks[s][6].elapsed_time(marks[s][7]) for s in range(args.steps)]  # side stream
+    stage["tile_v"] = [marks[s][6].elapsed_time(marks[s][7]) for s in range(args.steps)]  # side stream, beside coarse
     if vsa.device_error(reset=True):
         raise RuntimeError("device error word set during the timed run")
 

@@ -84,18 +84,34 @@ __device__ __forceinline__ unsigned long long d2key(double f) {
 
 // Key of the k-th largest score of a row (warp-wide): the largest T with
 // count(key >= T) >= k, found bit by bit from the top.  The row's keys are
-// held in registers (KPL per lane, N <= 32 * KPL); slots past N hold 0,
-// which no candidate threshold (>= 1) counts.
+// held in registers (KPL per lane: lane l, slot q holds column l + 32 q);
+// slots past N hold 0, which no candidate threshold (>= 1) counts.  The bits
+// every real key shares (the common prefix of the row's largest and smallest
+// keys) are taken as they are: with all keys >= that prefix, the count there
+// is N >= k, so the search starts below it.  The search stops early once the
+// keys still possible, [T, T + 2^rem), span at most `stop_width` as floats;
+// `rem` returns the number of undecided low bits (0: T is exact).
 template <int KPL>
-__device__ __forceinline__ uint32_t kth_key(const float* row, int N, int k, int lane) {
-    uint32_t key[KPL];
+__device__ __forceinline__ uint32_t kth_key_regs(const uint32_t (&key)[KPL], int N, int k, int lane,
+                                                 float stop_width, int& rem) {
+    uint32_t kmx = 0u, kmn = 0xFFFFFFFFu;
 #pragma unroll
     for (int q = 0; q < KPL; ++q) {
-        const int j = lane + 32 * q;
-        key[q] = j < N ? f2key(row[j]) : 0u;
+        kmx = max(kmx, key[q]);
+        if (lane + 32 * q < N) kmn = min(kmn, key[q]);
     }
-    uint32_t T = 0;
-    for (int bit = 31; bit >= 0; --bit) {
+    kmx = __reduce_max_sync(0xffffffffu, kmx);
+    kmn = __reduce_min_sync(0xffffffffu, kmn);
+    const int free_bits = 32 - __clz(kmx ^ kmn);  // bits below the common prefix
+    uint32_t T = free_bits == 32 ? 0u : (kmx >> free_bits) << free_bits;
+    rem = 0;
+#pragma unroll 1
+    for (int bit = free_bits - 1; bit >= 0; --bit) {
+        // Bits bit .. 0 are open: the k-th key lies in [T, T | (2^(bit+1) - 1)].
+        if (key2f(T | ((2u << bit) - 1u)) - key2f(T) <= stop_width) {
+            rem = bit + 1;
+            break;
+        }
         const uint32_t cand = T | (1u << bit);
         int cnt[4] = {0, 0, 0, 0};  // four independent chains (latency)
 #pragma unroll
@@ -105,8 +121,9 @@ __device__ __forceinline__ uint32_t kth_key(const float* row, int N, int k, int 
     }
     return T;
 }
-// Same search reading the row from shared memory on every pass (long rows).
-__device__ __noinline__ uint32_t kth_key_smem(const float* row, int N, int k, int lane) {
+// Same search reading the row from memory on every pass (rows longer than
+// the register-held cases).
+__device__ __noinline__ uint32_t kth_key_mem(const float* row, int N, int k, int lane) {
     uint32_t T = 0;
     for (int bit = 31; bit >= 0; --bit) {
         const uint32_t cand = T | (1u << bit);
@@ -116,6 +133,17 @@ __device__ __noinline__ uint32_t kth_key_smem(const float* row, int N, int k, in
         if (cnt >= k) T = cand;
     }
     return T;
+}
+
+// Loads a score row's keys into registers (slot q of this lane: column
+// lane + 32 q; 0 past N).
+template <int KPL>
+__device__ __forceinline__ void load_row_keys(const float* row, int N, int lane, uint32_t (&key)[KPL]) {
+#pragma unroll
+    for (int q = 0; q < KPL; ++q) {
+        const int j = lane + 32 * q;
+        key[q] = j < N ? f2key(row[j]) : 0u;
+    }
 }
 
 // Byte offsets of the score kernel's shared-memory regions.
@@ -174,53 +202,80 @@ __device__ double precise_score(const double* __restrict__ qsum, const ScoreArgs
     return (double)a.sm_scale * acc * inv_vq / (double)vk;
 }
 
+// precise_score with the D products spread over the warp (lane l takes
+// channels l, l + 32, ...; the partial sums are added in a butterfly): the
+// fp64 chain per lane is D / 32 long instead of D.  The value of lane 0 is
+// returned in every lane's copy only for lane 0; callers store lane 0's.
+template <int D>
+__device__ double precise_score_warp(const double* __restrict__ qsum, const ScoreArgs& a, size_t hrow, int j,
+                                     double inv_vq, int lane) {
+    const int vk = clamp_vbs(a.vbs[j]);
+    const float* km = a.km + hrow + (size_t)j * D;
+    const float* kr = a.kr + hrow + (size_t)j * D;
+    double acc = 0.0;
+#pragma unroll
+    for (int d = lane; d < D; d += 32) acc = fma(qsum[d], fma((double)km[d], (double)vk, (double)kr[d]), acc);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return vk > 0 ? (double)a.sm_scale * acc * inv_vq / (double)vk : 0.0;
+}
+
 // Top-k of one score row (one warp): the k-th largest fp32 score by bitwise
 // search, then the scores within the fp32 error band of that boundary are
 // re-ranked in fp64 from the exact cube sums; the selected cube ids are
-// written in ascending order.  `row` (shared or global memory) is scratch:
-// band members are overwritten with +inf (chosen) or -inf.  kMaxCase bounds
-// the register-held search (N <= 128 * kMaxCase); longer rows are searched in
-// place.
-template <int D, int kMaxCase>
-__device__ void select_row(float* row, const ScoreArgs& a, size_t bh, size_t hrow, int i, float qnorm_i,
-                           float kmax_all, double* qsum, double* cs, int* cj, int lane) {
+// written in ascending order.  With 0 < KPL <= 32 the row's keys are in
+// `key` (load_row_keys; N <= 32 * KPL) and every pass reads them there; with
+// KPL > 32 they are loaded for the k-th search only (the registers they take
+// are released before the other passes, which read the row from memory); with
+// KPL == 0 every pass reads memory.  `row` (shared or global memory) is
+// scratch: re-ranked band members are overwritten with +inf (chosen) or -inf.
+__host__ __device__ constexpr bool keys_in_regs(int kpl) { return kpl > 0 && kpl <= 32; }
+template <int D, int KPL>
+__device__ void select_row(float* row, uint32_t (&key)[keys_in_regs(KPL) ? KPL : 1], const ScoreArgs& a,
+                           size_t bh, size_t hrow, int i, float qnorm_i, float kmax_all, double* qsum, double* cs,
+                           int* cj, int lane) {
+    constexpr bool kRegs = keys_in_regs(KPL);
     const int N = a.N;
     const int k = a.topk;
-    uint32_t T;
-    switch ((N + 127) / 128) {  // register slots per lane: N / 32 rounded up to a multiple of 4
-        case 1: T = kth_key<4>(row, N, k, lane); break;
-        case 2: T = kth_key<8>(row, N, k, lane); break;
-        case 3: T = kth_key<12>(row, N, k, lane); break;
-        case 4: T = kth_key<16>(row, N, k, lane); break;
-        case 5: T = kth_key<20>(row, N, k, lane); break;
-        case 6: T = kth_key<24>(row, N, k, lane); break;
-        case 7: T = kth_key<28>(row, N, k, lane); break;
-        case 8: T = kth_key<32>(row, N, k, lane); break;
-        default:
-            if constexpr (kMaxCase >= 16) {
-                const int c = (N + 127) / 128;
-                if (c <= 10) T = kth_key<40>(row, N, k, lane);
-                else if (c <= 12) T = kth_key<48>(row, N, k, lane);
-                else if (c <= 14) T = kth_key<56>(row, N, k, lane);
-                else if (c <= 16) T = kth_key<64>(row, N, k, lane);
-                else T = kth_key_smem(row, N, k, lane);
-            } else {
-                T = kth_key_smem(row, N, k, lane);
-            }
-            break;
-    }
-    const float tau = key2f(T);
     // Error bound of an fp32 score against the exact one (dot of rounded
     // means with fp32 accumulation, then the scale): (D + 8) u |q||k|,
-    // doubled for margin; the band is twice that around tau.
+    // doubled for margin (eps).  Every score within eps of the exact one, the
+    // fp32 k-th largest tau within eps of the exact k-th: a score above
+    // tau + 2 eps is in the exact top-k, one below tau - 2 eps is not, and the
+    // ones between (the band) are re-ranked exactly.  The k-th search may stop
+    // with tau known only to [tau_lo, tau_hi] (width <= eps); the band then
+    // runs from tau_lo - 2 eps to tau_hi + 2 eps, which holds the exact one's.
     const float eps = 2.f * (float)(D + 8) * 5.9604645e-8f * a.sm_scale * qnorm_i * kmax_all;
+    uint32_t T;
+    int rem = 0;
+    if constexpr (kRegs) {
+        T = kth_key_regs<KPL>(key, N, k, lane, eps, rem);
+    } else if constexpr (KPL > 0) {
+        uint32_t kk[KPL];
+        load_row_keys<KPL>(row, N, lane, kk);
+        T = kth_key_regs<KPL>(kk, N, k, lane, eps, rem);
+    } else {
+        T = kth_key_mem(row, N, k, lane);
+    }
+    const float tau_lo = key2f(T);
+    const float tau_hi = key2f(rem > 0 ? T | ((1u << (rem - 1)) * 2u - 1u) : T);
     const float band = 2.f * eps + 1e-30f;
-    const float lo = tau - band, hi = tau + band;
+    const float lo = tau_lo - band, hi = tau_hi + band;
     int cA = 0, cC = 0;
-    for (int j = lane; j < N; j += 32) {
-        const float s = row[j];
-        cA += s > hi;
-        cC += (s >= lo) && (s <= hi);
+    if constexpr (kRegs) {
+#pragma unroll
+        for (int q = 0; q < KPL; ++q) {
+            const float s = key2f(key[q]);
+            const bool real = lane + 32 * q < N;
+            cA += real && s > hi;
+            cC += real && s >= lo && s <= hi;
+        }
+    } else {
+        for (int j = lane; j < N; j += 32) {
+            const float s = row[j];
+            cA += s > hi;
+            cC += (s >= lo) && (s <= hi);
+        }
     }
     cA = __reduce_add_sync(0xffffffffu, cA);
     cC = __reduce_add_sync(0xffffffffu, cC);
@@ -236,15 +291,30 @@ __device__ void select_row(float* row, const ScoreArgs& a, size_t bh, size_t hro
         const double inv_vq = vq > 0 ? 1.0 / (double)vq : 0.0;
         if (cC <= kCandCap) {
             int pos = 0;
-            for (int j0b = 0; j0b < N; j0b += 32) {
-                const int j = j0b + lane;
-                const bool inC = j < N && row[j] >= lo && row[j] <= hi;
-                const unsigned m = __ballot_sync(0xffffffffu, inC);
-                if (inC) cj[pos + __popc(m & ((1u << lane) - 1u))] = j;
-                pos += __popc(m);
+            if constexpr (kRegs) {
+#pragma unroll
+                for (int q = 0; q < KPL; ++q) {
+                    const int j = lane + 32 * q;
+                    const float s = key2f(key[q]);
+                    const bool inC = j < N && s >= lo && s <= hi;
+                    const unsigned m = __ballot_sync(0xffffffffu, inC);
+                    if (inC) cj[pos + __popc(m & ((1u << lane) - 1u))] = j;
+                    pos += __popc(m);
+                }
+            } else {
+                for (int j0b = 0; j0b < N; j0b += 32) {
+                    const int j = j0b + lane;
+                    const bool inC = j < N && row[j] >= lo && row[j] <= hi;
+                    const unsigned m = __ballot_sync(0xffffffffu, inC);
+                    if (inC) cj[pos + __popc(m & ((1u << lane) - 1u))] = j;
+                    pos += __popc(m);
+                }
             }
             __syncwarp();
-            for (int c = lane; c < cC; c += 32) cs[c] = precise_score<D>(qsum, a, hrow, cj[c], inv_vq);
+            for (int c = 0; c < cC; ++c) {  // warp-uniform: one candidate at a time, the warp's lanes on its channels
+                const double sc = precise_score_warp<D>(qsum, a, hrow, cj[c], inv_vq, lane);
+                if (lane == 0) cs[c] = sc;
+            }
             __syncwarp();
             // rank among candidates: (score desc, index asc); chosen if rank < need.
             for (int c = lane; c < cC; c += 32) {
@@ -290,25 +360,46 @@ __device__ void select_row(float* row, const ScoreArgs& a, size_t bh, size_t hro
             }
             __syncwarp();
         }
+        if constexpr (kRegs) {
+            // The band members' decisions (+inf / -inf) back into the keys.
+#pragma unroll
+            for (int q = 0; q < KPL; ++q) {
+                const int j = lane + 32 * q;
+                const float s = key2f(key[q]);
+                if (j < N && s >= lo && s <= hi) key[q] = f2key(row[j]);
+            }
+        }
     }
     // Emit the selected set in ascending cube index.  After re-ranking the
     // band members hold +inf (chosen) or -inf (not chosen).
     int32_t* out = a.topk_idx + (bh * N + i) * (size_t)k;
     int pos = 0;
     const unsigned below = (1u << lane) - 1u;
-    for (int j0b = 0; j0b < N; j0b += 128) {  // four 32-wide slices per pass: loads batched
-        bool sel[4];
+    if constexpr (kRegs) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int j = j0b + 32 * q + lane;
-            const float x = j < N ? row[j] : -INFINITY;
-            sel[q] = j < N && (x > hi || (take_band && x >= lo));
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const unsigned m = __ballot_sync(0xffffffffu, sel[q]);
-            if (sel[q]) out[pos + __popc(m & below)] = j0b + 32 * q + lane;
+        for (int q = 0; q < KPL; ++q) {
+            const int j = lane + 32 * q;
+            const float x = key2f(key[q]);
+            const bool sel = j < N && (x > hi || (take_band && x >= lo));
+            const unsigned m = __ballot_sync(0xffffffffu, sel);
+            if (sel) out[pos + __popc(m & below)] = j;
             pos += __popc(m);
+        }
+    } else {
+        for (int j0b = 0; j0b < N; j0b += 128) {  // four 32-wide slices per pass: loads batched
+            bool sel[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = j0b + 32 * q + lane;
+                const float x = j < N ? row[j] : -INFINITY;
+                sel[q] = j < N && (x > hi || (take_band && x >= lo));
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const unsigned m = __ballot_sync(0xffffffffu, sel[q]);
+                if (sel[q]) out[pos + __popc(m & below)] = j0b + 32 * q + lane;
+                pos += __popc(m);
+            }
         }
     }
 }
@@ -427,78 +518,130 @@ __global__ void __launch_bounds__(WARPS * 32) score_topk_kernel(ScoreArgs a) {
     for (int r = warp; r < R; r += kWarps) {
         const int i = i0 + r;
         if (i >= N) break;
-        select_row<D, 8>(sc + (size_t)r * N, a, bh, hrow, i, qnorm[r], kmax_all, qsum_w + warp * D,
-                         cand_s + warp * kCandCap, cand_j + warp * kCandCap, lane);
+        float* row = sc + (size_t)r * N;
+        if (N <= 256) {
+            uint32_t key[8];
+            load_row_keys<8>(row, N, lane, key);
+            select_row<D, 8>(row, key, a, bh, hrow, i, qnorm[r], kmax_all, qsum_w + warp * D,
+                             cand_s + warp * kCandCap, cand_j + warp * kCandCap, lane);
+        } else {  // only when a caller without room for the score matrix takes this kernel for long rows
+            uint32_t none[1];
+            select_row<D, 0>(row, none, a, bh, hrow, i, qnorm[r], kmax_all, qsum_w + warp * D,
+                             cand_s + warp * kCandCap, cand_j + warp * kCandCap, lane);
+        }
     }
 }
 
 // ------------------------------------------- large N: scores through memory
 // When few query rows fit the fused kernel's shared memory (N above ~1100 at
 // D = 128), the scores go to the workspace instead: a register-tiled fp32
-// GEMM (128 x 128 score tiles, the full depth D in shared memory, each thread
-// 8 x 8 scores on rows ty + 16 r and columns tx + 16 c; products accumulated
-// in increasing d as in the fused kernel, so the scores are the same), then
-// one warp per row runs the same selection on the row read back.
+// GEMM of the cube means, then one warp per row runs the same selection on
+// the row read back (from L2: the [B, heads, N, N] scores of a call are tens
+// of MB).
+//
+// GEMM: 128 x 128 score tiles, 256 threads, each 8 x 8 scores (rows
+// 4 ty + {0..3} and 64 + 4 ty + {0..3}, columns likewise from tx); the depth
+// runs in slices of 16 channels through double-buffered shared memory, the
+// next slice's global loads in flight during the current slice's FMAs.
+// Slices are stored channel-major (As[k][m]), so a thread's 8 rows are two
+// float4 reads; a loading thread takes 8 consecutive channels (32 bytes) of
+// one row and writes them transposed, a warp's 32 rows to 32 banks.  Each
+// score accumulates its D products in increasing channel order.
 constexpr int kGemmTile = 128;
+constexpr int kGemmK = 16;
 
 template <int D>
-__global__ void __launch_bounds__(256) score_gemm_kernel(ScoreArgs a, float* __restrict__ scores) {
-    constexpr int LD = D + 4;  // padded row (floats)
-    extern __shared__ __align__(16) float gsm[];
-    float* As = gsm;                   // [kGemmTile][LD] query means
-    float* Bs = gsm + kGemmTile * LD;  // [kGemmTile][LD] key means
+__global__ void __launch_bounds__(256, 2) score_gemm_kernel(ScoreArgs a, float* __restrict__ scores) {
+    constexpr int KT = D / kGemmK;
+    __shared__ __align__(16) float As[2][kGemmK][kGemmTile];
+    __shared__ __align__(16) float Bs[2][kGemmK][kGemmTile];
     const int N = a.N;
     const int i0 = blockIdx.x * kGemmTile, j0 = blockIdx.y * kGemmTile;
     const size_t bh = blockIdx.z;
-    const size_t hrow = bh * (size_t)N * D;
+    const float* Ag = a.qm + bh * (size_t)N * D;
+    const float* Bg = a.km + bh * (size_t)N * D;
     const int tid = threadIdx.x;
-    for (int e = tid; e < kGemmTile * (D / 4); e += 256) {
-        const int r = e / (D / 4), d4 = e - r * (D / 4);
-        float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
-        if (i0 + r < N) va = *reinterpret_cast<const float4*>(a.qm + hrow + (size_t)(i0 + r) * D + 4 * d4);
-        if (j0 + r < N) vb = *reinterpret_cast<const float4*>(a.km + hrow + (size_t)(j0 + r) * D + 4 * d4);
-        *reinterpret_cast<float4*>(As + r * LD + 4 * d4) = va;
-        *reinterpret_cast<float4*>(Bs + r * LD + 4 * d4) = vb;
-    }
-    __syncthreads();
+    const int lrow = tid & (kGemmTile - 1);  // loader: one row, channels lk .. lk + 7 of the slice
+    const int lk = (tid >> 7) * 8;
+    const bool a_in = i0 + lrow < N, b_in = j0 + lrow < N;
+    const float* ag = Ag + (size_t)(a_in ? i0 + lrow : 0) * D + lk;
+    const float* bg = Bg + (size_t)(b_in ? j0 + lrow : 0) * D + lk;
+    float4 pa[2], pb[2];
+    auto gload = [&](int kt) {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        pa[0] = a_in ? *reinterpret_cast<const float4*>(ag + kt * kGemmK) : z;
+        pa[1] = a_in ? *reinterpret_cast<const float4*>(ag + kt * kGemmK + 4) : z;
+        pb[0] = b_in ? *reinterpret_cast<const float4*>(bg + kt * kGemmK) : z;
+        pb[1] = b_in ? *reinterpret_cast<const float4*>(bg + kt * kGemmK + 4) : z;
+    };
+    auto sstore = [&](int buf) {
+        const float av[8] = {pa[0].x, pa[0].y, pa[0].z, pa[0].w, pa[1].x, pa[1].y, pa[1].z, pa[1].w};
+        const float bv[8] = {pb[0].x, pb[0].y, pb[0].z, pb[0].w, pb[1].x, pb[1].y, pb[1].z, pb[1].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            As[buf][lk + e][lrow] = av[e];
+            Bs[buf][lk + e][lrow] = bv[e];
+        }
+    };
     const int ty = tid >> 4, tx = tid & 15;
     float acc[8][8];
 #pragma unroll
     for (int r = 0; r < 8; ++r)
 #pragma unroll
         for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
-#pragma unroll 2
-    for (int d = 0; d < D; d += 4) {
-        float4 av[8], bv[8];
+    gload(0);
+    sstore(0);
+    __syncthreads();
+#pragma unroll 1
+    for (int kt = 0; kt < KT; ++kt) {
+        const int buf = kt & 1;
+        if (kt + 1 < KT) gload(kt + 1);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) av[r] = *reinterpret_cast<const float4*>(As + (ty + 16 * r) * LD + d);
+        for (int k = 0; k < kGemmK; ++k) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][4 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][64 + 4 * ty]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][64 + 4 * tx]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) bv[c] = *reinterpret_cast<const float4*>(Bs + (tx + 16 * c) * LD + d);
+            for (int r = 0; r < 8; ++r)
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                acc[r][c] = fmaf(av[r].x, bv[c].x, acc[r][c]);
-                acc[r][c] = fmaf(av[r].y, bv[c].y, acc[r][c]);
-                acc[r][c] = fmaf(av[r].z, bv[c].z, acc[r][c]);
-                acc[r][c] = fmaf(av[r].w, bv[c].w, acc[r][c]);
-            }
+                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+        }
+        if (kt + 1 < KT) sstore(buf ^ 1);  // buffer buf ^ 1 was last read before the previous barrier
+        __syncthreads();
     }
+    const bool vec = (N & 3) == 0;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-        const int i = i0 + ty + 16 * r;
+        const int i = i0 + (r < 4 ? 4 * ty + r : 64 + 4 * ty + r - 4);
         if (i >= N) continue;
         float* dst = scores + (bh * N + i) * (size_t)N;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const int j = j0 + tx + 16 * c;
-            if (j < N) dst[j] = a.sm_scale * acc[r][c];
+        for (int h = 0; h < 2; ++h) {
+            const int j = j0 + 64 * h + 4 * tx;
+            const float v0 = a.sm_scale * acc[r][4 * h], v1 = a.sm_scale * acc[r][4 * h + 1];
+            const float v2 = a.sm_scale * acc[r][4 * h + 2], v3 = a.sm_scale * acc[r][4 * h + 3];
+            if (vec && j + 3 < N) {
+                *reinterpret_cast<float4*>(dst + j) = make_float4(v0, v1, v2, v3);
+            } else {
+                if (j < N) dst[j] = v0;
+                if (j + 1 < N) dst[j + 1] = v1;
+                if (j + 2 < N) dst[j + 2] = v2;
+                if (j + 3 < N) dst[j + 3] = v3;
+            }
         }
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(256) select_kernel(ScoreArgs a, float* __restrict__ scores) {
+// One warp per row; rows of up to 1024 scores are held in registers (KPL
+// slots per lane), loaded before the block's reduction of the key norms so
+// the two overlap.
+template <int KPL>
+constexpr int select_min_blocks() { return KPL <= 24 ? 4 : 3; }
+template <int D, int KPL>
+__global__ void __launch_bounds__(256, select_min_blocks<KPL>()) select_kernel(ScoreArgs a, float* __restrict__ scores) {
     __shared__ double qsum_w[8][D];
     __shared__ double cand_s[8][kCandCap];
     __shared__ int cand_j[8][kCandCap];
@@ -506,6 +649,10 @@ __global__ void __launch_bounds__(256) select_kernel(ScoreArgs a, float* __restr
     const int N = a.N;
     const size_t bh = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int i = blockIdx.x * 8 + warp;
+    float* row = scores + (bh * N + (i < N ? i : N - 1)) * (size_t)N;
+    uint32_t key[keys_in_regs(KPL) ? KPL : 1];
+    if constexpr (keys_in_regs(KPL)) load_row_keys<KPL>(row, N, lane, key);
     float kmax = 0.f;  // largest key-mean norm of this head
     for (int j = tid; j < N; j += 256) kmax = fmaxf(kmax, a.kn[bh * N + j]);
 #pragma unroll
@@ -515,10 +662,32 @@ __global__ void __launch_bounds__(256) select_kernel(ScoreArgs a, float* __restr
     float kmax_all = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) kmax_all = fmaxf(kmax_all, red[w]);
-    const int i = blockIdx.x * 8 + warp;
     if (i >= N) return;
-    select_row<D, 16>(scores + (bh * N + i) * (size_t)N, a, bh, bh * (size_t)N * D, i, a.qn[bh * N + i],
-                      kmax_all, qsum_w[warp], cand_s[warp], cand_j[warp], lane);
+    select_row<D, KPL>(row, key, a, bh, bh * (size_t)N * D, i, a.qn[bh * N + i], kmax_all, qsum_w[warp],
+                       cand_s[warp], cand_j[warp], lane);
+}
+
+// The select_kernel instance for rows of N scores: register slots per lane
+// ceil(N / 32) rounded up to a multiple of 4 up to 32 and of 8 up to 64;
+// longer rows are searched in memory.
+template <int D>
+using SelectFn = void (*)(ScoreArgs, float*);
+template <int D>
+SelectFn<D> select_kernel_for(int N) {
+    const int c = (N + 31) / 32;
+    if (c <= 4) return select_kernel<D, 4>;
+    if (c <= 8) return select_kernel<D, 8>;
+    if (c <= 12) return select_kernel<D, 12>;
+    if (c <= 16) return select_kernel<D, 16>;
+    if (c <= 20) return select_kernel<D, 20>;
+    if (c <= 24) return select_kernel<D, 24>;
+    if (c <= 28) return select_kernel<D, 28>;
+    if (c <= 32) return select_kernel<D, 32>;
+    if (c <= 40) return select_kernel<D, 40>;
+    if (c <= 48) return select_kernel<D, 48>;
+    if (c <= 56) return select_kernel<D, 56>;
+    if (c <= 64) return select_kernel<D, 64>;
+    return select_kernel<D, 0>;
 }
 
 // --------------------------------------------------------------- validator
@@ -603,7 +772,7 @@ int coarse_rows_per_block(int ncubes, int D) {
 bool coarse_split_default(int ncubes, int D) { return ncubes >= 256 || coarse_rows_per_block(ncubes, D) < 32; }
 
 size_t coarse_smem_bytes(int N, int D, bool split) {
-    if (split) return (size_t)2 * kGemmTile * (D + 4) * sizeof(float);
+    if (split) return 0;  // the score GEMM and the selection use static shared memory only
     const int R = coarse_rows_per_block(N, D);
     return score_layout(R, N, D, score_warps(R)).total;
 }
@@ -641,14 +810,11 @@ cudaError_t launch_coarse(const void* qt, const void* kt, const int32_t* vbs, in
     a.sm_scale = sm_scale;
     if (split) {
         float* scores = po.norm + 2 * (size_t)B * heads * ncubes;
-        const size_t gsmem = (size_t)2 * kGemmTile * (D + 4) * sizeof(float);
         const int tiles = (ncubes + kGemmTile - 1) / kGemmTile;
         const dim3 gg(tiles, tiles, B * heads);
         auto gemm = D == 128 ? score_gemm_kernel<128> : score_gemm_kernel<64>;
-        e = cudaFuncSetAttribute(gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsmem);
-        if (e != cudaSuccess) return e;
-        gemm<<<gg, 256, gsmem, stream>>>(a, scores);
-        auto sel = D == 128 ? select_kernel<128> : select_kernel<64>;
+        gemm<<<gg, 256, 0, stream>>>(a, scores);
+        auto sel = D == 128 ? select_kernel_for<128>(ncubes) : select_kernel_for<64>(ncubes);
         sel<<<dim3((ncubes + 7) / 8, B * heads), 256, 0, stream>>>(a, scores);
         note_launches(2);
         return cudaGetLastError();
