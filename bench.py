@@ -1,9 +1,11 @@
 #!/usr/bin/env python
 """Benchmark of the VSA hot path on the Wan2.2 attention shape.
 
-One step = one pass of the whole hot path over one batch of synthetic input:
-tile q, k, v (21 x 30 x 52 latent grid, 40 heads, D = 128) -> coarse select
-(topk = 78 of 624 cubes) -> block-sparse attention -> untile.
+One step = one pass of the whole hot path over one batch of synthetic input
+(21 x 30 x 52 latent grid, 40 heads, D = 128): tile k and v and mean-pool the
+cubes of q and k -> coarse select (topk = 78 of 624 cubes) -> query-cube
+pairing -> block-sparse attention reading q and writing the output in raster
+order (the tiling of q and the untiling of the output are part of that pass).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -11,7 +13,7 @@ Prints one JSON line (rank 0).  `value` is effective TFLOPS over the whole
 step, using the fine-stage effective FLOP count 4 * S_pad * k * 64 * D * H * B
 (the work the selected blocks need, not the dense work avoided); the fine
 kernel's own time and roofline fraction are reported beside it.  Inputs
-(q, k, v: 3 x 335 MB, plus 1.2 GB of tiled intermediates) exceed the 126 MB
+(q, k, v: 3 x 335 MB, plus 0.8 GB of tiled intermediates) exceed the 126 MB
 L2, so no explicit flush is used between steps.
 
 --impl reference times the CPU oracle (the only other implementation there is)
@@ -249,10 +251,9 @@ def stage_bytes(wl):
     cubes = wl.B * wl.heads * wl.ncubes
     pooled = 16 * cubes * wl.D + 8 * cubes              # means + residuals of q, k (fp32), norms
     return {
-        "tile_qk_pool": 2 * (real + tiled) + pooled,        # read raster rows, write every slot + statistics
+        "tile_k_pool_qk": 2 * real + tiled + pooled,        # read raster q, k; write tiled k + statistics
         "tile_v": real + tiled,                              # side stream, beside the coarse selection
         "coarse_select": 8 * cubes * wl.D + 8 * cubes + 4 * cubes * wl.topk,  # read means, norms; write idx
-        "untile": 2 * real,                                  # read real slots, write raster rows
     }
 
 
@@ -279,10 +280,10 @@ def config_of(wl):
 
 
 def step_bytes(wl):
-    """Bytes of the step's big tensors: q, k, v and out untiled; q, k, v and out tiled."""
+    """Bytes of the step's big tensors: q, k, v and out raster; k and v tiled."""
     untiled = wl.B * wl.T * wl.H * wl.W * wl.heads * wl.D * 2
     tiled = wl.B * wl.s_pad * wl.heads * wl.D * 2
-    return 4 * untiled + 4 * tiled
+    return 4 * untiled + 2 * tiled
 
 
 # --------------------------------------------------------- blocks128
@@ -435,8 +436,8 @@ def run_ours(args, wl, inputs, rank, world, dist):
     q, k, v = (dev_bf16(inputs[n]) for n in ("q", "k", "v"))
     grid = wl.grid
     N = wl.ncubes
-    qt = torch.empty((wl.B, wl.s_pad, wl.heads, wl.D), dtype=torch.bfloat16, device=dev)
-    kt, vt, ot = torch.empty_like(qt), torch.empty_like(qt), torch.empty_like(qt)
+    kt = torch.empty((wl.B, wl.s_pad, wl.heads, wl.D), dtype=torch.bfloat16, device=dev)
+    vt = torch.empty_like(kt)
     vbs = torch.empty((N,), dtype=torch.int32, device=dev)
     vbs2 = torch.empty_like(vbs)
     idx = torch.empty((wl.B, wl.heads, N, wl.topk), dtype=torch.int32, device=dev)
@@ -462,9 +463,10 @@ def run_ours(args, wl, inputs, rank, world, dist):
         oout = out if oout is None else oout
         if marks is not None:
             marks[0].record(stream)
-        # q and k are tiled and pooled in one pass; the selection starts from
-        # the pooled statistics the tiling left in the workspace.
-        vsa.tile_pool(qin, kin, grid, qt=qt, kt=kt, vbs=vbs, workspace=ws)
+        # k is tiled and q, k pooled in one pass (q needs no tiled copy: the
+        # fine stage reads it in raster order); the selection starts from the
+        # pooled statistics the pass left in the workspace.
+        vsa.tile_pool(qin, kin, grid, kt=kt, vbs=vbs, workspace=ws, want_qt=False)
         ev_qk.record(stream)
         side.wait_event(ev_qk)
         with torch.cuda.stream(side):
@@ -483,12 +485,10 @@ def run_ours(args, wl, inputs, rank, world, dist):
         if marks is not None:
             marks[3].record(stream)
         stream.wait_event(ev_v)
-        vsa.sparse_attn_fwd(qt, kt, vt, idx, vbs, wl.sm_scale, out=ot, lse=lse, pairs=pairs)
+        # Raster q in, raster output out: no tiling of q, no untiling pass.
+        vsa.sparse_attn_fwd_raster(qin, kt, vt, idx, vbs, grid, wl.sm_scale, out=oout, lse=lse, pairs=pairs)
         if marks is not None:
             marks[4].record(stream)
-        vsa.untile(ot, grid, out=oout)
-        if marks is not None:
-            marks[5].record(stream)
 
     clk = ClockSampler(torch.cuda.current_device())
     with clk:
@@ -517,16 +517,17 @@ def run_ours(args, wl, inputs, rank, world, dist):
     ms_total = max_over_ranks(start.elapsed_time(end), dist, dev)
     ms_step = ms_total / args.steps
     stage = {name: [marks[s][i].elapsed_time(marks[s][i + 1]) for s in range(args.steps)]
-             for i, name in enumerate(["tile_qk_pool", "coarse_select", "pair_cubes", "sparse_attn_fwd", "untile"])}
+             for i, name in enumerate(["tile_k_pool_qk", "coarse_select", "pair_cubes", "sparse_attn_fwd"])}
     stage["tile_v"] = [marks[s][6].elapsed_time(marks[s][7]) for s in range(args.steps)]  # side stream, beside coarse
     if vsa.device_error(reset=True):
         raise RuntimeError("device error word set during the timed run")
 
-    if args.no_e2e:
-        nxt = time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream)
-        return ms_step, stage, clk.summary(), None, 0, 0, launches, nxt
-    e2e_ms, h2d, d2h = e2e_leg(step, inputs, q, k, v, out, args, stream, dist, dev)
-    # The next rows are timed last, after the end-to-end leg, on the step's tensors.
+    e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else e2e_leg(step, inputs, q, k, v, out, args, stream, dist, dev)
+    # The next rows are timed last, after the end-to-end leg, on the step's
+    # tensors (plus a tiled q and a tiled output buffer, which the step itself
+    # does not need).
+    qt, _ = vsa.tile(q, grid, vbs=vbs2)
+    ot = torch.empty_like(qt)
     nxt = time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream)
     return ms_step, stage, clk.summary(), e2e_ms, h2d, d2h, launches, nxt
 

@@ -66,6 +66,9 @@ def _declare(lib):
     lib.vsa_tile_pool.argtypes = [ctypes.POINTER(VsaGrid), _p, _p, _p, _p, _p, _p, _p]
     lib.vsa_coarse_select_pooled.restype = ctypes.c_int
     lib.vsa_coarse_select_pooled.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _p, _p, _p]
+    lib.vsa_sparse_attn_fwd_raster.restype = ctypes.c_int
+    lib.vsa_sparse_attn_fwd_raster.argtypes = [ctypes.POINTER(VsaGrid), _p, _p, _p, _p, _p, _p, _p, _i32,
+                                               ctypes.c_float, _p, _p, _p]
     lib.vsa_sparse_attn_fwd.restype = ctypes.c_int
     lib.vsa_sparse_attn_fwd.argtypes = [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_float,
                                         _p, _p, _p]
@@ -228,11 +231,13 @@ def coarse_select(qt, kt, vbs, topk: int, sm_scale: float = 0.0, workspace=None,
     return out
 
 
-def tile_pool(q, k, grid, qt=None, kt=None, vbs=None, workspace=None, stream=None):
+def tile_pool(q, k, grid, qt=None, kt=None, vbs=None, workspace=None, want_qt=True, stream=None):
     """Tile q and k and pool their cubes in one pass (vsa_tile_pool).
 
     Returns (qt, kt, vbs, workspace); pass vbs and workspace to
-    coarse_select_pooled for the same top-k as coarse_select(qt, kt, vbs, ...)."""
+    coarse_select_pooled for the same top-k as coarse_select(qt, kt, vbs, ...).
+    want_qt=False skips the tiled copy of q (qt is then None), for
+    sparse_attn_fwd_raster, which reads the raster q."""
     torch = _torch()
     _need(q, torch.bfloat16, "q")
     _need(k, torch.bfloat16, "k")
@@ -244,7 +249,7 @@ def tile_pool(q, k, grid, qt=None, kt=None, vbs=None, workspace=None, stream=Non
         raise ValueError("q shape does not match the grid")
     N = num_cubes(grid)
     shape = (B, 64 * N, heads, D)
-    if qt is None:
+    if qt is None and want_qt:
         qt = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
     if kt is None:
         kt = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
@@ -254,6 +259,8 @@ def tile_pool(q, k, grid, qt=None, kt=None, vbs=None, workspace=None, stream=Non
     if workspace is None:
         workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=q.device)
     for t, n in ((qt, "qt"), (kt, "kt")):
+        if t is None:
+            continue
         _need(t, torch.bfloat16, n)
         if tuple(t.shape) != shape:
             raise ValueError(f"{n} must be {shape}")
@@ -261,8 +268,9 @@ def tile_pool(q, k, grid, qt=None, kt=None, vbs=None, workspace=None, stream=Non
     _need(workspace, torch.uint8, "workspace")
     if workspace.numel() < nbytes:
         raise ValueError(f"workspace needs {nbytes} bytes")
-    _check(library().vsa_tile_pool(ctypes.byref(g), q.data_ptr(), k.data_ptr(), qt.data_ptr(), kt.data_ptr(),
-                                   vbs.data_ptr(), workspace.data_ptr(), _stream(stream)), "vsa_tile_pool")
+    _check(library().vsa_tile_pool(ctypes.byref(g), q.data_ptr(), k.data_ptr(), None if qt is None else qt.data_ptr(),
+                                   kt.data_ptr(), vbs.data_ptr(), workspace.data_ptr(), _stream(stream)),
+           "vsa_tile_pool")
     return qt, kt, vbs, workspace
 
 
@@ -371,6 +379,54 @@ def sparse_attn_fwd(qt, kt, vt, topk_idx, vbs, sm_scale: float = 0.0, out=None, 
                                                float(sm_scale), ptr(coarse_out), ptr(gate_c), ptr(gate_f),
                                                out.data_ptr(), ptr(lse), _stream(stream)),
            "vsa_sparse_attn_fwd")
+    return out, lse
+
+
+def sparse_attn_fwd_raster(q, kt, vt, topk_idx, vbs, grid, sm_scale: float = 0.0, out=None, lse=None,
+                           want_lse: bool = True, pairs=None, counts=None, stream=None):
+    """Block-sparse attention on raster q -> (out raster bf16 [B, T*H*W, heads, D],
+    lse fp32 [B, heads, 64*N] cube-major or None); kt, vt tiled
+    (vsa_sparse_attn_fwd_raster).  out equals untile(sparse_attn_fwd(tile(q), ...))."""
+    torch = _torch()
+    _need(q, torch.bfloat16, "q")
+    _need(kt, torch.bfloat16, "kt")
+    _need(vt, torch.bfloat16, "vt")
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(vbs, torch.int32, "vbs")
+    B, S, heads, D = q.shape
+    g = _grid(grid, heads, D)
+    N = num_cubes(grid)
+    if (g.B, g.T * g.H * g.W) != (B, S):
+        raise ValueError("q shape does not match the grid")
+    if tuple(kt.shape) != (B, 64 * N, heads, D) or vt.shape != kt.shape:
+        raise ValueError("kt/vt must be tiled [B, 64*N, heads, D] of the grid")
+    if topk_idx.dim() != 4 or tuple(topk_idx.shape[:3]) != (B, heads, N):
+        raise ValueError("topk_idx must be [B, heads, N, topk]")
+    topk = topk_idx.shape[3]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if out.shape != q.shape:
+        raise ValueError("out must match q")
+    if want_lse and lse is None:
+        lse = torch.empty((B, heads, 64 * N), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+        if tuple(lse.shape) != (B, heads, 64 * N):
+            raise ValueError("lse must be [B, heads, 64*N]")
+    if pairs is not None:
+        _need(pairs, torch.int32, "pairs")
+        if tuple(pairs.shape) != (B, heads, (N + 1) // 2):
+            raise ValueError("pairs must be [B, heads, (N + 1) // 2]")
+    if counts is not None:
+        _need(counts, torch.int32, "counts")
+        if tuple(counts.shape) != (B, heads, N):
+            raise ValueError("counts must be [B, heads, N]")
+    _check(library().vsa_sparse_attn_fwd_raster(
+        ctypes.byref(g), q.data_ptr(), kt.data_ptr(), vt.data_ptr(), topk_idx.data_ptr(),
+        None if counts is None else counts.data_ptr(), vbs.data_ptr(),
+        None if pairs is None else pairs.data_ptr(), int(topk), float(sm_scale), out.data_ptr(),
+        None if lse is None else lse.data_ptr(), _stream(stream)), "vsa_sparse_attn_fwd_raster")
     return out, lse
 
 
@@ -546,13 +602,13 @@ def debug_wait_timeout(limit_ns: int, stream=None) -> int:
 
 
 def pipeline(q, k, v, grid, topk: int, sm_scale: float = 0.0, stream=None):
-    """Whole hot path on raster inputs: tile -> coarse select -> (pairing) -> sparse attention -> untile.
+    """Whole hot path on raster inputs: tile k (q, k pooled in the same pass) and v -> coarse select ->
+    pairing -> sparse attention on raster q, written in raster order (no separate untile).
 
     Returns (out raster bf16, lse fp32 [B, heads, 64*N] in cube-major order, topk_idx)."""
-    qt, kt, vbs, ws = tile_pool(q, k, grid, stream=stream)
+    _, kt, vbs, ws = tile_pool(q, k, grid, want_qt=False, stream=stream)
     vt, _ = tile(v, grid, vbs=_torch().empty_like(vbs), stream=stream)
     B, _, heads, D = q.shape
     idx = coarse_select_pooled(ws, vbs, B, heads, D, topk, sm_scale, stream=stream)
     pairs = pair_cubes(idx, stream=stream)
-    ot, lse = sparse_attn_fwd(qt, kt, vt, idx, vbs, sm_scale, pairs=pairs, stream=stream)
-    return untile(ot, grid, stream=stream), lse, idx
+    return (*sparse_attn_fwd_raster(q, kt, vt, idx, vbs, grid, sm_scale, pairs=pairs, stream=stream), idx)

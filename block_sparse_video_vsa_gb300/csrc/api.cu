@@ -145,13 +145,13 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
 
 vsa_status vsa_tile_pool(const vsa_grid* g, const void* q, const void* k, void* qt, void* kt, int32_t* vbs,
                          void* workspace, vsa_stream_t stream) {
-    if (!grid_ok(g) || !q || !k || !qt || !kt || !workspace) return VSA_ERR_INVALID_ARG;
+    if (!grid_ok(g) || !q || !k || !workspace) return VSA_ERR_INVALID_ARG;
     if (g->D != 64 && g->D != 128) return VSA_ERR_UNSUPPORTED;
     const int64_t N = cubes_of(g);
     if (N > 4096 || !sizes_fit(g->B, N * 64, g->heads, g->D) || (int64_t)g->T * g->H * g->W >= ((int64_t)1 << 31))
         return VSA_ERR_UNSUPPORTED;
     if ((int64_t)g->B * N > 2147483647 || g->heads > 65535) return VSA_ERR_UNSUPPORTED;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(qt) || !aligned16(kt) || !aligned16(workspace) ||
+    if (!aligned16(q) || !aligned16(k) || (qt && !aligned16(qt)) || (kt && !aligned16(kt)) || !aligned16(workspace) ||
         (vbs && (reinterpret_cast<uintptr_t>(vbs) & 3u)))
         return VSA_ERR_ALIGNMENT;
     return from_cuda(launch_tile_pool(*g, (int)N, q, k, qt, kt, vbs, workspace, static_cast<cudaStream_t>(stream)));
@@ -185,10 +185,17 @@ namespace {
 vsa_status fine_entry(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx, const int32_t* counts,
                       const int32_t* vbs, const uint32_t* pairs, int32_t B, int32_t ncubes, int32_t heads, int32_t D,
                       int32_t topk, float sm_scale, const float* coarse_out, const void* gate_c, const void* gate_f,
-                      void* out, float* lse, float* max_prob, vsa_stream_t stream) {
+                      void* out, float* lse, float* max_prob, vsa_stream_t stream, const vsa_grid* raster = nullptr) {
     if (!qt || !kt || !vt || !topk_idx || !vbs || !out) return VSA_ERR_INVALID_ARG;
     const bool gated = coarse_out || gate_c || gate_f;
     if (gated && (!coarse_out || !gate_c || !gate_f)) return VSA_ERR_INVALID_ARG;
+    if (raster) {
+        // q and out in raster order of this grid; k, v, topk_idx on its cubes.
+        if (!grid_ok(raster) || gated) return VSA_ERR_INVALID_ARG;
+        if (raster->B != B || raster->heads != heads || raster->D != D || cubes_of(raster) != ncubes)
+            return VSA_ERR_INVALID_ARG;
+        if ((int64_t)B * raster->T * raster->H * raster->W >= ((int64_t)1 << 31)) return VSA_ERR_UNSUPPORTED;
+    }
     if (B <= 0 || ncubes <= 0 || heads <= 0 || topk <= 0 || topk > ncubes) return VSA_ERR_INVALID_ARG;
     if (!(sm_scale == sm_scale)) return VSA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return VSA_ERR_UNSUPPORTED;
@@ -210,7 +217,7 @@ vsa_status fine_entry(const void* qt, const void* kt, const void* vt, const int3
     if (fine_smem_bytes() > ctx.max_smem_optin) return VSA_ERR_UNSUPPORTED;
     if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)D);
     return from_cuda(launch_fine(qt, kt, vt, topk_idx, counts, vbs, pairs, B, ncubes, heads, D, topk, sm_scale,
-                                 coarse_out, gate_c, gate_f, out, lse, max_prob, ctx.err, ctx.num_sms,
+                                 coarse_out, gate_c, gate_f, out, lse, max_prob, raster, ctx.err, ctx.num_sms,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -236,6 +243,17 @@ vsa_status vsa_sparse_attn_fwd_peak(const void* qt, const void* kt, const void* 
                       nullptr, out, lse, max_prob, stream);
 }
 
+
+vsa_status vsa_sparse_attn_fwd_raster(const vsa_grid* g, const void* q, const void* kt, const void* vt,
+                                      const int32_t* topk_idx, const int32_t* counts, const int32_t* vbs,
+                                      const uint32_t* pairs, int32_t topk, float sm_scale, void* out, float* lse,
+                                      vsa_stream_t stream) {
+    if (!grid_ok(g)) return VSA_ERR_INVALID_ARG;
+    const int64_t N = cubes_of(g);
+    if (N > 2147483647) return VSA_ERR_UNSUPPORTED;
+    return fine_entry(q, kt, vt, topk_idx, counts, vbs, pairs, g->B, (int32_t)N, g->heads, g->D, topk, sm_scale,
+                      nullptr, nullptr, nullptr, out, lse, nullptr, stream, g);
+}
 
 vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                                   const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int32_t B,

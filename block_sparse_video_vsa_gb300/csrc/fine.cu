@@ -138,7 +138,7 @@ struct FineParams {
     const int32_t* vbs;
     const uint32_t* pairs;  // [B * heads][npairs]: i | (j << 16), j = 0xFFFF single; or null: (2u, 2u + 1)
     const int32_t* counts;  // [B * heads * N] entries of each topk_idx row in use (<= topk), or null: all
-    const uint4* q;      // tiled q rows (for staging Q into TMEM)
+    const uint4* q;      // q rows (for staging Q into TMEM): tiled, or raster when tokens > 0
     const float* oc;     // coarse-stage output [B * heads][N][D], or null: no gated combine
     const uint4* gc;     // gates of the coarse and fine terms, bf16 in the layout of out
     const uint4* gf;
@@ -150,7 +150,39 @@ struct FineParams {
     int npairs;          // ceil(N / 2)
     int num_units;       // B * heads * npairs
     float scale_log2;    // sm_scale * log2(e)
+    // Raster mode (tokens > 0): q is read and out written in raster token
+    // order [B, tokens, heads, D] of a T x H x W grid (nh x nw cubes per
+    // frame layer); lse stays cube-major.
+    long long tokens;
+    int gT, gH, gW, gnh, gnw;
 };
+
+// Raster token of slot s of cube c (the real tokens of the cube's clipped
+// 4 x 4 x 4 sub-box fill its first slots in (t, h, w) order), or -1 for a
+// padding slot.
+__device__ __forceinline__ int raster_token(const FineParams& p, int c, int s) {
+    const int cw = c % p.gnw;
+    const int c1 = c / p.gnw;
+    const int ch = c1 % p.gnh;
+    const int ct = c1 / p.gnh;
+    const int et = min(4, p.gT - 4 * ct), eh = min(4, p.gH - 4 * ch), ew = min(4, p.gW - 4 * cw);
+    const int hw = eh * ew;
+    if (s >= et * hw) return -1;
+    const int lt = s / hw;
+    const int rem = s - lt * hw;
+    const int lh = rem / ew;
+    return ((4 * ct + lt) * p.gH + 4 * ch + lh) * p.gW + 4 * cw + (rem - lh * ew);
+}
+
+// Global row (token of the [B, S, heads, D] layout) of slot s of cube i in
+// batch b: tiled, or raster (-1 for a padding slot, which has no raster row).
+__device__ __forceinline__ long long token_row(const FineParams& p, int b, int i, int s) {
+    if (p.tokens > 0) {
+        const int n = raster_token(p, i, s);
+        return n < 0 ? -1 : (long long)b * p.tokens + n;
+    }
+    return ((long long)b * p.N + i) * kCubeTokens + s;
+}
 
 __device__ __forceinline__ void unit_coords(int u, const FineParams& p, int& b, int& h, int& pair) {
     pair = u % p.npairs;
@@ -270,10 +302,8 @@ __device__ __forceinline__ void stage_q(const FineParams& p, int u, int r, uint3
     int b, h;
     const int i = row_cube(p, u, r, b, h);
     const uint4* src = nullptr;
-    if (i >= 0) {
-        const size_t row = (size_t)b * p.N * kCubeTokens + (size_t)i * kCubeTokens + (r & 63);
-        src = p.q + (row * p.heads + h) * (size_t)(kD / 8);
-    }
+    const long long row = i >= 0 ? token_row(p, b, i, r & 63) : -1;
+    if (row >= 0) src = p.q + ((size_t)row * p.heads + h) * (size_t)(kD / 8);
 #pragma unroll
     for (int c0 = 0; c0 < kD / 2; c0 += 32) {
         uint32_t w[32];
@@ -298,8 +328,9 @@ __device__ __forceinline__ void prefetch_q(const FineParams& p, int u, int r) {
     int b, h;
     const int i = row_cube(p, u, r, b, h);
     if (i < 0) return;
-    const size_t row = (size_t)b * p.N * kCubeTokens + (size_t)i * kCubeTokens + (r & 63);
-    const uint4* src = p.q + (row * p.heads + h) * (size_t)(kD / 8);
+    const long long row = token_row(p, b, i, r & 63);
+    if (row < 0) return;
+    const uint4* src = p.q + ((size_t)row * p.heads + h) * (size_t)(kD / 8);
 #pragma unroll
     for (int c = 0; c < kD * 2; c += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + c / 16));
 }
@@ -780,7 +811,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = row_cube(p, u, r, b, h);
             const bool wr = ok && i >= 0;
             const size_t row = wr ? (size_t)b * s_pad + (size_t)i * kCubeTokens + (r & 63) : 0;
-            uint4* dst = reinterpret_cast<uint4*>(p.out) + (row * p.heads + h) * (size_t)(D / 8) + G * (dh / 8);
+            // Output row: the tiled row, or in raster mode the slot's token
+            // (padding slots have none and write nothing).
+            const long long orow = wr ? token_row(p, b, i, r & 63) : -1;
+            const bool wo = orow >= 0;
+            uint4* dst = reinterpret_cast<uint4*>(p.out) + ((size_t)(wo ? orow : 0) * p.heads + h) * (size_t)(D / 8) +
+                         G * (dh / 8);
             // Gated: the coarse term g_c * O_c of this thread's columns and the
             // fine gate g_f, loaded before the wait for the unit's last P.V.
             float ct[kGated ? dh : 1];
@@ -838,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     pw[q >> 1] = pack_bf16x2(f[0], f[1]);
                 }
-                if (wr) {
+                if (wo) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
                         __stcs(dst + c0 / 8 + v, make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]));
@@ -908,8 +944,8 @@ int fine_max_cubes() { return kMaxCubes; }
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                         const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int B, int ncubes,
                         int heads, int D, int topk, float sm_scale, const float* coarse_out, const void* gate_c,
-                        const void* gate_f, void* out, float* lse, float* max_prob, unsigned int* err,
-                        int num_sms, cudaStream_t stream) {
+                        const void* gate_f, void* out, float* lse, float* max_prob, const vsa_grid* raster,
+                        unsigned int* err, int num_sms, cudaStream_t stream) {
     CUtensorMap mk, mv;
     const int rows = B * ncubes * kCubeTokens;
     if (!make_map(&mk, kt, rows, heads, D, true) || !make_map(&mv, vt, rows, heads, D, true))
@@ -935,6 +971,17 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     p.npairs = (ncubes + 1) / 2;
     p.num_units = B * heads * p.npairs;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.tokens = 0;
+    p.gT = p.gH = p.gW = p.gnh = p.gnw = 1;
+    if (raster) {
+        if (coarse_out) return cudaErrorInvalidValue;  // gates and coarse term are laid out tiled
+        p.tokens = (long long)raster->T * raster->H * raster->W;
+        p.gT = raster->T;
+        p.gH = raster->H;
+        p.gW = raster->W;
+        p.gnh = (raster->H + 3) / 4;
+        p.gnw = (raster->W + 3) / 4;
+    }
     // The exact row maximum behind max_prob is tracked only in the peak
     // instantiation (it costs about 1% of the ungated kernel's time); the peak
     // entry point runs ungated.

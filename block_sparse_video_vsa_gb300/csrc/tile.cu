@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kThreads) untile_kernel(const int4* __restrict
 // Tiling of q and k fused with the coarse stage's cube mean-pool: one pass
 // over the raster q and k writes the tiled tensors and the pooled statistics
 // (pool_sum.cuh), so the selection does not read the tiled q and k again.
+// A null qt or kt skips that tiled copy (the statistics are still written).
 // grid (B * ncubes, 2 [q, k]); every 8-channel column of the cube's token
 // rows belongs to one thread, which copies its 64 slots eight at a time and
 // sums the first vbs of them in slot order, the order pool_kernel sums the
@@ -152,7 +153,8 @@ __global__ void __launch_bounds__(kPoolThreadsMax) tile_pool_kernel(const uint4*
     const int vb = vb_s;
     const size_t s_pad = (size_t)ncubes * kCubeTokens;
     const uint4* xb = (which == 0 ? q : k) + (size_t)b * (size_t)tokens * row_vecs;
-    uint4* xtb = (which == 0 ? qt : kt) + ((size_t)b * s_pad + (size_t)c * kCubeTokens) * row_vecs;
+    uint4* const dst = which == 0 ? qt : kt;  // null: statistics only, no tiled copy
+    uint4* xtb = dst ? dst + ((size_t)b * s_pad + (size_t)c * kCubeTokens) * row_vecs : nullptr;
     for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) {
         float hi[8], lo[8];
 #pragma unroll
@@ -165,8 +167,10 @@ __global__ void __launch_bounds__(kPoolThreadsMax) tile_pool_kernel(const uint4*
                 const int n = src_tok[s0 + u];
                 w[u] = n >= 0 ? __ldcs(xb + (size_t)n * row_vecs + v) : make_uint4(0u, 0u, 0u, 0u);
             }
+            if (xtb) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) __stcs(xtb + (size_t)(s0 + u) * row_vecs + v, w[u]);
+                for (int u = 0; u < 8; ++u) __stcs(xtb + (size_t)(s0 + u) * row_vecs + v, w[u]);
+            }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
                 if (s0 + u < vb) accumulate8(w[u], hi, lo);

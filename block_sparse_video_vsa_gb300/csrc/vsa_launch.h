@@ -42,8 +42,8 @@ int fine_max_cubes();
 cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const int32_t* topk_idx,
                         const int32_t* counts, const int32_t* vbs, const uint32_t* pairs, int B, int ncubes,
                         int heads, int D, int topk, float sm_scale, const float* coarse_out, const void* gate_c,
-                        const void* gate_f, void* out, float* lse, float* max_prob, unsigned int* err,
-                        int num_sms, cudaStream_t stream);
+                        const void* gate_f, void* out, float* lse, float* max_prob, const vsa_grid* raster,
+                        unsigned int* err, int num_sms, cudaStream_t stream);
 
 // coarse_attn.cu
 size_t coarse_attn_workspace_bytes(int B, int heads, int ncubes, int D);

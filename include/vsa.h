@@ -8,7 +8,8 @@
  *   2. vsa_coarse_select   cube mean-pool of Q and K, cube-to-cube scores and
  *                          the top-k key/value cubes per query cube;
  *      (vsa_tile_pool + vsa_coarse_select_pooled: steps 1 and 2 with one
- *                          read of q and k; same results)
+ *                          read of q and k; vsa_sparse_attn_fwd_raster:
+ *                          step 3 on raster q and out; same results)
  *   3. vsa_sparse_attn_fwd non-causal block-sparse attention over the selected
  *                          cubes, padded tokens masked (bf16 out + fp32 LSE);
  *      (vsa_pair_cubes     optional schedule for step 3: which query cubes
@@ -168,7 +169,9 @@ vsa_status vsa_coarse_select(const void* qt, const void* kt, const int32_t* vbs,
  * vsa_coarse_select; no counterpart of its own on the pages: it fuses two of
  * their steps.
  *   q, k      : raster bf16 [B, T*H*W, heads, D]        (read)
- *   qt, kt    : tiled bf16 [B, 64*ncubes, heads, D]    (written as vsa_tile)
+ *   qt, kt    : tiled bf16 [B, 64*ncubes, heads, D]    (written as vsa_tile),
+ *               or NULL: that tiled copy is skipped (the statistics are
+ *               still computed; vsa_sparse_attn_fwd_raster reads raster q)
  *   vbs       : int32 [ncubes] or NULL                  (written as vsa_tile)
  *   workspace : vsa_coarse_workspace_bytes(B, heads, ncubes, D) bytes,
  *               16-byte aligned; its pooled-statistics head is written
@@ -297,6 +300,25 @@ vsa_status vsa_sparse_attn_fwd_ex(const void* qt, const void* kt, const void* vt
                                   const int32_t* vbs, const uint32_t* pairs, int32_t B,
                                   int32_t ncubes, int32_t heads, int32_t D, int32_t topk,
                                   float sm_scale, void* out, float* lse, vsa_stream_t stream);
+
+/*
+ * vsa_sparse_attn_fwd_ex with q read and the output written in raster token
+ * order, so the tiling of q and the untiling of the output (steps 1 and 4
+ * for those tensors) are not separate passes: same arithmetic, so `out`
+ * equals vsa_untile of vsa_sparse_attn_fwd_ex's output bit for bit, and lse
+ * is the same.  No counterpart of its own on the pages: it fuses the
+ * permutation of [STA] Implementation into step 3.
+ *   g        : the grid (B, T, H, W, heads, D); ncubes = vsa_num_cubes(g)
+ *   q        : raster bf16 [B, T*H*W, heads, D]
+ *   kt, vt   : tiled bf16 [B, 64*ncubes, heads, D] (vsa_tile / vsa_tile_pool)
+ *   topk_idx, counts, vbs, pairs, topk, sm_scale, lse: as vsa_sparse_attn_fwd_ex
+ *   out      : raster bf16 [B, T*H*W, heads, D] (written in full)
+ * Limits and errors as vsa_sparse_attn_fwd_ex, and B * T * H * W < 2^31.
+ */
+vsa_status vsa_sparse_attn_fwd_raster(const vsa_grid* g, const void* q, const void* kt, const void* vt,
+                                      const int32_t* topk_idx, const int32_t* counts, const int32_t* vbs,
+                                      const uint32_t* pairs, int32_t topk, float sm_scale, void* out, float* lse,
+                                      vsa_stream_t stream);
 
 /*
  * vsa_sparse_attn_fwd_ex that also returns each row's peakedness ([INT8-WAN]
