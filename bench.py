@@ -50,9 +50,9 @@ WORKLOAD = "wan"
 # was taken from: if fine.cu no longer hashes to `source_sha256`, the traffic is reported
 # as null.
 FINE_TRAFFIC = {
-    "bytes_per_launch": (248.616448e6 + 69.268992e6) * 40 / 8,
+    "bytes_per_launch": (233.370112e6 + 56.521216e6) * 40 / 8,
     "capture": "profiles/fine_fwd_kernel_wan.md",
-    "source_sha256": "44a48d3b787e04f3baab5a4c55a8735929e36a67452d91c811afb17921d14bda",
+    "source_sha256": "06239ee0868e8ddf1a9dcc8cba5a60b63b4fa4c37061c018d3988a1b3b40017b",
 }
 # The same for the 128-token-block workload, from a capture of one whole
 # 12-head launch (no scaling).
