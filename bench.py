@@ -791,7 +791,7 @@ def main():
                      "frac": fine_tflops / burst,
                      "traffic": fine_traffic() if wl.heads == 40 else None,
                      "peak_kind": f"{peak_kind} dense bf16 burst",
-                     "kernel": "fine_fwd_kernel (vsa_sparse_attn_fwd)"},
+                     "kernel": "fine_fwd_kernel (vsa_sparse_attn_fwd_raster)"},
         "e2e": None if e2e_ms is None else {
             "value": whole_job_throughput(world, flops, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
