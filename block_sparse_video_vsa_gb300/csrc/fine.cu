@@ -52,6 +52,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "vsa_common.cuh"
 
 namespace vsa {
@@ -122,6 +124,8 @@ struct __align__(16) Misc {
     uint64_t list_empty[2];
     uint64_t drain[2];    // per MMA-issuing warp
     int list_count[2];
+    int list_unit[2];     // dynamic schedule: the list's unit, or -1: no more units
+    int list_next[2];     // dynamic schedule: the unit after it (whose Q the stager stages), or -1
     float xm[2][2][128];  // [unit parity][group][row]: running max at the unit's end
     float xl[2][2][128];  // [unit parity][group][row]: sum at the unit's end
     float xt[2][2][128];  // [unit parity][group][row]: exact row maximum (log2 units)
@@ -149,6 +153,7 @@ struct FineParams {
     int B, N, heads, D, topk;
     int npairs;          // ceil(N / 2)
     int num_units;       // B * heads * npairs
+    int slot;            // dynamic schedule: this launch's unit counter (g_unit_next[slot])
     float scale_log2;    // sm_scale * log2(e)
     // Raster mode (tokens > 0): q is read and out written in raster token
     // order [B, tokens, heads, D] of a T x H x W grid (nh x nw cubes per
@@ -378,7 +383,31 @@ __device__ __forceinline__ void exp64(const float* x, float c2, float mb, uint32
     l += (s01.x + s01.y) + (s23.x + s23.y);
 }
 
-template <int kD, bool kGated, bool kPeak>
+// Unit schedules.  Static: CTA c takes units c, c + grid, c + 2 grid, ...
+// Dynamic (for rows of variable length, where the static deal leaves SMs
+// idle): CTA c starts with unit c, and warp 0 claims each further unit as
+// gridDim.x + atomicAdd(&g_unit_next[slot], 1), one unit ahead (the softmax
+// group that stages the next unit's Q needs its index), so CTAs that drew
+// short units take more of them; lists then carry their unit and the next
+// one, and a list with unit -1 ends every role's loop.  Each launch takes its
+// own slot (a host-side ticket modulo kUnitSlots: concurrent launches on
+// other streams use other slots); the last CTA to finish puts the slot's
+// counters back to zero for the launch that takes it next.
+constexpr int kUnitSlots = 256;
+__device__ unsigned int g_unit_next[kUnitSlots];
+__device__ unsigned int g_cta_done[kUnitSlots];
+
+// A claim is drawn by lane 0 (claim_draw) and read by the warp later
+// (claim_take), so the atomic's round trip overlaps other work.
+__device__ __forceinline__ unsigned int claim_draw(const FineParams& p, int lane) {
+    return lane == 0 ? atomicAdd(&g_unit_next[p.slot], 1u) : 0u;
+}
+__device__ __forceinline__ int claim_take(const FineParams& p, unsigned int drawn) {
+    const int v = (int)(gridDim.x + __shfl_sync(0xffffffffu, drawn, 0));
+    return v < p.num_units ? v : -1;
+}
+
+template <int kD, bool kGated, bool kPeak, bool kDyn>
 __global__ void __launch_bounds__(kThreads, 1)
     fine_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     FineParams p) {
@@ -397,6 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nchunks = D / 64;
     const int s_pad = p.N * kCubeTokens;
     const int my_units = blockIdx.x < p.num_units ? (p.num_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    // Loop bound of every role: the static schedule's unit count, or for the
+    // dynamic one a bound the end list always cuts short.  (Written as bounded
+    // loops under a guard: open-ended loops compiled to a form that took 5-8%
+    // longer at the Wan2.2 shape, measured same-box.)
+    const int bound = kDyn ? p.num_units : my_units;
 
     // ---------------------------------------------------------------- setup
     if (threadIdx.x == 0) {
@@ -453,17 +487,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol = l2_policy_evict_last();
         uint32_t g = 0;
         bool ok = true;
-        for (int ul = 0; ul < my_units && ok; ++ul) {
-            const int u = blockIdx.x + ul * gridDim.x;
+        int u_dyn = blockIdx.x;  // dynamic: grid <= units, so every CTA has a first unit
+        int u_next = kDyn ? claim_take(p, claim_draw(p, lane)) : -1;
+        for (int ul = 0; ul < (kDyn ? bound + 1 : bound) && ok; ++ul) {
+            const int u = kDyn ? u_dyn : (int)(blockIdx.x + ul * gridDim.x);
             const int lb = ul & 1;
             if (ul >= 2)
                 ok = mbar_wait_bounded(smem_u32(&ms.list_empty[lb]), ((ul >> 1) + 1) & 1, abort_flag, p.err,
                                        kWaitLimitNs);
             if (!ok) break;
+            unsigned int drawn = 0u;
+            if constexpr (kDyn) {
+                if (u < 0) {  // no unit left: a list with unit -1 tells every role to stop
+                    if (lane == 0) {
+                        ms.list_count[lb] = 0;
+                        ms.list_unit[lb] = -1;
+                        ms.list_next[lb] = -1;
+                        mbar_arrive(smem_u32(&ms.list_full[lb]));
+                    }
+                    break;
+                }
+                // The unit after u_next, drawn now and read after this unit's loads.
+                if (u_next >= 0) drawn = claim_draw(p, lane);
+            }
             uint32_t* list = lists + lb * kMaxUnion;
             const int count = build_union(p, u, list, bitmaps, bitmaps + kBitmapWords, lane);
             if (lane == 0) {
                 ms.list_count[lb] = count;
+                if constexpr (kDyn) {
+                    ms.list_unit[lb] = u;
+                    ms.list_next[lb] = u_next;
+                }
                 mbar_arrive(smem_u32(&ms.list_full[lb]));
             }
             int b, h, pair;
@@ -484,6 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
+            if constexpr (kDyn) {
+                u_dyn = u_next;
+                u_next = u_dyn >= 0 ? claim_take(p, drawn) : -1;
+            }
         }
         if (lane == 0) drain_ring<kKStages>(ms.k_full, g, p.err);
         __syncwarp();
@@ -492,11 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol = l2_policy_evict_last();
         uint32_t g = 0;
         bool ok = true;
-        for (int ul = 0; ul < my_units && ok; ++ul) {
-            const int u = blockIdx.x + ul * gridDim.x;
+        for (int ul = 0; ul < bound && ok; ++ul) {
             const int lb = ul & 1;
             ok = mbar_wait_bounded(smem_u32(&ms.list_full[lb]), (ul >> 1) & 1, abort_flag, p.err, kWaitLimitNs);
             if (!ok) break;
+            const int u = kDyn ? ms.list_unit[lb] : (int)(blockIdx.x + ul * gridDim.x);
+            if (kDyn && u < 0) break;
             const uint32_t* list = lists + lb * kMaxUnion;
             const int count = ms.list_count[lb];
             int b, h, pair;
@@ -532,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // through the softmax's barriers.  Descriptors are precomputed; each
         // MMA adds a constant to the start-address field of the low word (no
         // carry: shared addresses are below 256 KB).
-        if (my_units > 0) {
+        if (bound > 0) {
             const uint32_t hi = (uint32_t)(smem_desc_sw128(0, 16, 1024) >> 32);  // SBO, version, swizzle
             bool ok = true;
             // Count of the list of local unit ul (waits for the list), warp-uniform.
@@ -540,6 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait_bounded(smem_u32(&ms.list_full[ul & 1]), (ul >> 1) & 1, abort_flag, p.err,
                                        kWaitLimitNs))
                     return -1;
+                if constexpr (kDyn) {  // -1 also when no unit is left
+                    if (__shfl_sync(0xffffffffu, ms.list_unit[ul & 1], 0) < 0) return -1;
+                }
                 return __shfl_sync(0xffffffffu, ms.list_count[ul & 1], 0);
             };
             uint32_t g = 0;  // global step at the start of the unit
@@ -547,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
                 const uint32_t lo_k = (uint32_t)smem_desc_sw128(sbase + kOffK, 16, 1024);
                 constexpr int ksteps_qk = D / 16;
-                for (int ul = 0; ul < my_units && ok; ++ul) {
+                for (int ul = 0; ul < bound && ok; ++ul) {
                     const int cnt = list_count(ul);
                     if (cnt < 0) break;
                     const int nst = (cnt + 1) >> 1;
@@ -581,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 const uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
                 const uint32_t lo_v = (uint32_t)smem_desc_sw128(sbase + kOffV, kChunkRows128, 1024);
-                for (int ul = 0; ul < my_units && ok; ++ul) {
+                for (int ul = 0; ul < bound && ok; ++ul) {
                     const int cnt = list_count(ul);
                     if (cnt < 0) break;
                     const int nst = (cnt + 1) >> 1;
@@ -643,16 +705,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         uint32_t g = 0;   // global step at the start of the current unit
         uint32_t jg = 0;  // steps this group has taken (phase of s_full[G])
-        if (G == 0 && my_units > 0) {
+        if (G == 0 && bound > 0) {
             stage_q<D>(p, blockIdx.x, r, t_lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ms.q_full));
         }
 #pragma unroll 1
-        for (int ul = 0; ul < my_units; ++ul) {
-            const int u = blockIdx.x + ul * gridDim.x;
+        for (int ul = 0; ul < bound; ++ul) {
             const int lb = ul & 1;
+            int u = (int)(blockIdx.x + ul * gridDim.x);
+            if constexpr (kDyn) {
+                // The unit comes with the list; it is read here and again just
+                // before the list buffer is released, not held across the steps.
+                if (ok) ok = mbar_wait_bounded(smem_u32(&ms.list_full[lb]), (ul >> 1) & 1, abort_flag, p.err,
+                                               kWaitLimitNs);
+                if (!ok || ms.list_unit[lb] < 0) break;
+                u = ms.list_unit[lb];
+            }
             if constexpr (kGated) {
                 // The epilogue reads this thread's half row of both gates (one
                 // 128-byte line each for D = 128): start bringing them into L2.
@@ -665,15 +735,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(p.gf + gi));
                 }
             }
-            if (ok) ok = mbar_wait_bounded(smem_u32(&ms.list_full[lb]), (ul >> 1) & 1, abort_flag, p.err,
-                                           kWaitLimitNs);
+            if constexpr (!kDyn) {
+                if (ok) ok = mbar_wait_bounded(smem_u32(&ms.list_full[lb]), (ul >> 1) & 1, abort_flag, p.err,
+                                               kWaitLimitNs);
+            }
             const uint32_t* list = lists + lb * kMaxUnion;
             const int count = ok ? ms.list_count[lb] : 0;
             const int nst = (count + 1) >> 1;
             const uint32_t g0 = g;
             // The group that takes the next unit's first step stages its Q.
-            const bool stager = (((g0 + nst) & 1) == (uint32_t)G) && ul + 1 < my_units;
-            if (stager) prefetch_q<D>(p, u + gridDim.x, r);
+            const bool stager = (((g0 + nst) & 1) == (uint32_t)G) &&
+                                (kDyn ? ms.list_next[lb] >= 0 : ul + 1 < my_units);
+            if (stager) prefetch_q<D>(p, kDyn ? ms.list_next[lb] : u + (int)gridDim.x, r);
             float m = ninf, l = 0.f;
             float mx = ninf;  // exact row maximum of this group's steps (m lags it by up to the threshold)
             bool first = true;
@@ -778,12 +851,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) ok = mbar_wait_bounded(smem_u32(&ms.q_empty), ul & 1, abort_flag, p.err, kWaitLimitNs);
                 if (ok) {
                     tc_fence_after();
-                    stage_q<D>(p, u + gridDim.x, r, t_lane);
+                    stage_q<D>(p, kDyn ? *reinterpret_cast<volatile int*>(&ms.list_next[lb]) : u + (int)gridDim.x,
+                               r, t_lane);
                     tc_fence_before();
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&ms.q_full));
             }
+            if constexpr (kDyn) u = *reinterpret_cast<volatile int*>(&ms.list_unit[lb]);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ms.list_empty[lb]));
             // ------------------------------------------------ unit epilogue
@@ -798,15 +873,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_true = kPeak ? fmaxf(mx, ms.xt[lb][G ^ 1][r]) : ninf;
             const float m0 = G ? mo : m, l0 = G ? lo : l;
             const float m1 = G ? m : mo, l1 = G ? l : lo;
+            // Which group holds the unit's even steps (step t: group (g0 + t) & 1)
+            // depends on the steps the CTA ran before the unit (with the dynamic
+            // schedule, on the run): the merge takes the even-step group's
+            // partial result first, so the bits depend on the unit alone.
+            const int ge = (int)(g0 & 1u);  // group of the even steps
+            const float m_e = ge ? m1 : m0, l_e = ge ? l1 : l0;
+            const float m_o = ge ? m0 : m1, l_o = ge ? l0 : l1;
             // A group that took no step of this unit holds no O for it.
-            const bool had0 = nst > 0 && (((g0 & 1) == 0) || nst >= 2);
-            const bool had1 = nst > 0 && (((g0 & 1) == 1) || nst >= 2);
-            const float mt = fmaxf(m0, m1);
-            const float a0 = (m0 == ninf) ? 0.f : ex2_approx(m0 - mt);
-            const float a1 = (m1 == ninf) ? 0.f : ex2_approx(m1 - mt);
-            const float lt = a0 * l0 + a1 * l1;
+            const bool had_e = nst > 0, had_o = nst >= 2;
+            const float mt = fmaxf(m_e, m_o);
+            const float a_e = (m_e == ninf) ? 0.f : ex2_approx(m_e - mt);
+            const float a_o = (m_o == ninf) ? 0.f : ex2_approx(m_o - mt);
+            const float lt = __fmaf_rn(a_e, l_e, __fmul_rn(a_o, l_o));
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            const float s0 = a0 * inv, s1 = a1 * inv;
+            const float s_e = a_e * inv, s_o = a_o * inv;
+            const uint32_t o_e = ge ? kTmemO1 : kTmemO0, o_o = ge ? kTmemO0 : kTmemO1;
             int b, h;
             const int i = row_cube(p, u, r, b, h);
             const bool wr = ok && i >= 0;
@@ -852,10 +934,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c0 = 0; c0 < dh; c0 += 32) {
                 uint32_t oa[32], ob[32];
-                // Loaded whatever had0/had1 say (values of a group without a step
+                // Loaded whatever had_e/had_o say (values of a group without a step
                 // are never used): defined on every path, as the allocator needs.
-                tmem_ld32(t_lane + kTmemO0 + G * dh + c0, oa);
-                tmem_ld32(t_lane + kTmemO1 + G * dh + c0, ob);
+                tmem_ld32(t_lane + o_e + G * dh + c0, oa);
+                tmem_ld32(t_lane + o_o + G * dh + c0, ob);
                 tmem_wait_ld();
                 uint32_t pw[16];
 #pragma unroll
@@ -863,9 +945,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float f[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const float va = (ok && had0) ? __uint_as_float(oa[q + e]) : 0.f;
-                        const float vb = (ok && had1) ? __uint_as_float(ob[q + e]) : 0.f;
-                        f[e] = fmaf(s0, va, s1 * vb);
+                        const float va = (ok && had_e) ? __uint_as_float(oa[q + e]) : 0.f;
+                        const float vb = (ok && had_o) ? __uint_as_float(ob[q + e]) : 0.f;
+                        f[e] = __fmaf_rn(s_e, va, __fmul_rn(s_o, vb));
                     }
                     if constexpr (kGated) {
                         const uint32_t gw = gfw[(c0 + q) >> 1];
@@ -900,6 +982,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, 512);
+    if (kDyn && threadIdx.x == 0) {
+        // Every claim of this CTA precedes its count here; the last CTA to
+        // count puts the slot back to zero for the next launch that takes it.
+        __threadfence();
+        if (atomicAdd(&g_cta_done[p.slot], 1u) == gridDim.x - 1) {
+            g_unit_next[p.slot] = 0;
+            g_cta_done[p.slot] = 0;
+            __threadfence();
+        }
+    }
 }
 
 }  // namespace
@@ -970,6 +1062,8 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     p.topk = topk;
     p.npairs = (ncubes + 1) / 2;
     p.num_units = B * heads * p.npairs;
+    static std::atomic<unsigned int> ticket{0};
+    p.slot = (int)(ticket.fetch_add(1u, std::memory_order_relaxed) % (unsigned int)kUnitSlots);
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.tokens = 0;
     p.gT = p.gH = p.gW = p.gnh = p.gnw = 1;
@@ -986,9 +1080,15 @@ cudaError_t launch_fine(const void* qt, const void* kt, const void* vt, const in
     // instantiation (it costs about 1% of the ungated kernel's time); the peak
     // entry point runs ungated.
     if (max_prob && coarse_out) return cudaErrorInvalidValue;
-    auto kernel = coarse_out ? (D == 64 ? fine_fwd_kernel<64, true, false> : fine_fwd_kernel<128, true, false>)
-                  : max_prob ? (D == 64 ? fine_fwd_kernel<64, false, true> : fine_fwd_kernel<128, false, true>)
-                             : (D == 64 ? fine_fwd_kernel<64, false, false> : fine_fwd_kernel<128, false, false>);
+    // Rows of variable length (counts) take the dynamic unit schedule; the
+    // fixed-length call keeps the static one (no load imbalance to win back,
+    // and the static form is the faster one there).
+    const bool dyn = counts != nullptr && !coarse_out && !max_prob;
+    auto kernel =
+        coarse_out ? (D == 64 ? fine_fwd_kernel<64, true, false, false> : fine_fwd_kernel<128, true, false, false>)
+        : max_prob ? (D == 64 ? fine_fwd_kernel<64, false, true, false> : fine_fwd_kernel<128, false, true, false>)
+        : dyn      ? (D == 64 ? fine_fwd_kernel<64, false, false, true> : fine_fwd_kernel<128, false, false, true>)
+                   : (D == 64 ? fine_fwd_kernel<64, false, false, false> : fine_fwd_kernel<128, false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     // The setmaxnreg split is sized for a launch of exactly kLaunchRegs

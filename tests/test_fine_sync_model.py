@@ -20,8 +20,11 @@ K into a 3-slot ring, warp 1 issues Q.K^T into the one S buffer, warp 2 loads
 V into a 3-slot ring, warp 3 issues P.V into the O of the step's group, and
 two softmax groups of four warps (one per TMEM lane quarter) take the even
 and the odd steps, stage the next unit's Q, and merge their results in a
-per-unit epilogue through a named barrier per lane quarter.  Planted
-protocol mistakes must be caught.
+per-unit epilogue through a named barrier per lane quarter.  Both unit
+schedules are modelled: static (every role knows the CTA's unit count) and
+dynamic (units are claimed one ahead at run time, so each list says whether
+another unit follows, and a final list, the end marker, stops every role).
+Planted protocol mistakes must be caught.
 """
 import random
 
@@ -43,7 +46,8 @@ class MBar:
 
 
 class Cta:
-    def __init__(self, shared_s_full=False):
+    def __init__(self, shared_s_full=False, dynamic=True):
+        self.dynamic = dynamic
         self.mb = {}
         for i in range(3):
             for n in ("k_full", "k_empty", "v_full", "v_empty"):
@@ -61,6 +65,7 @@ class Cta:
             self.mb[n] = MBar(1)
         self.mb["o_free"] = MBar(8)
         self.count = [0, 0]
+        self.info = [None, None]  # per list buffer: (steps, another unit follows) or END
         self.queues = {}
 
     def commit(self, issuer, name, rng):
@@ -76,13 +81,22 @@ def check(cond, what):
     return ("check", cond, what)
 
 
+END = "end"
+
+
 def producer_k(c, units):
     g = 0
-    for ul, nst in enumerate(units):
+    for ul in range(len(units) + (1 if c.dynamic else 0)):
         lb = ul & 1
         if ul >= 2:
             yield wait(f"list_empty{lb}", (ul >> 1) - 1)
+        if ul == len(units):  # dynamic: no unit left, the end marker
+            c.info[lb] = END
+            c.mb[f"list_full{lb}"].arrive()
+            return
+        nst = units[ul]
         c.count[lb] = nst
+        c.info[lb] = (nst, ul + 1 < len(units))
         c.mb[f"list_full{lb}"].arrive()
         for _ in range(nst):
             if g >= 3:
@@ -92,12 +106,19 @@ def producer_k(c, units):
             yield ("step",)
 
 
+def unit_range(c, units):
+    return range(len(units) + 1) if c.dynamic else range(len(units))
+
+
 def producer_v(c, units):
     g = 0
-    for ul, nst in enumerate(units):
+    for ul in unit_range(c, units):
         lb = ul & 1
         yield wait(f"list_full{lb}", ul >> 1)
-        assert c.count[lb] == nst
+        if c.info[lb] == END:
+            return
+        nst = c.info[lb][0]
+        assert c.count[lb] == nst == units[ul]
         for _ in range(nst):
             if g >= 3:
                 yield wait(f"v_empty{g % 3}", g // 3 - 1)
@@ -109,9 +130,12 @@ def producer_v(c, units):
 
 def mma_qk(c, units, rng):
     g = 0
-    for ul, nst in enumerate(units):
+    for ul in unit_range(c, units):
         lb = ul & 1
         yield wait(f"list_full{lb}", ul >> 1)
+        if c.info[lb] == END:
+            return
+        nst = c.info[lb][0]
         yield wait("q_full", ul)
         for t in range(nst):
             gs = g + t
@@ -127,9 +151,12 @@ def mma_qk(c, units, rng):
 
 def mma_pv(c, units, rng, gate_empty=True):
     g = 0
-    for ul, nst in enumerate(units):
+    for ul in unit_range(c, units):
         lb = ul & 1
         yield wait(f"list_full{lb}", ul >> 1)
+        if c.info[lb] == END:
+            return
+        nst = c.info[lb][0]
         if ul >= 1 and (nst > 0 or gate_empty):
             yield wait("o_free", ul - 1)
         for t in range(nst):
@@ -148,11 +175,16 @@ def softmax(c, units, warp, rng, p_waits_own=False):
     G = (warp - 4) >> 2
     bar = ("nbar", 1 + quarter)
     g = jg = 0
-    if G == 0 and units:
-        c.mb["q_full"].arrive()  # the first unit's Q
-    for ul, nst in enumerate(units):
+    if G == 0:
+        c.mb["q_full"].arrive()  # the first unit's Q (every CTA has a first unit)
+    for ul in unit_range(c, units):
         lb = ul & 1
         yield wait(f"list_full{lb}", ul >> 1)
+        if c.info[lb] == END:
+            return
+        nst, has_next = c.info[lb]
+        if not c.dynamic:
+            has_next = ul + 1 < len(units)  # the static schedule knows its unit count
         first = True
         for t in range((g + G) & 1, nst, 2):
             gs = g + t
@@ -171,7 +203,7 @@ def softmax(c, units, warp, rng, p_waits_own=False):
                             f"O rescaled before P.V({gs - 2}) completed")
             c.mb["p_full"].arrive()
             first = False
-        if ((g + nst) & 1) == G and ul + 1 < len(units):  # stage the next unit's Q
+        if ((g + nst) & 1) == G and has_next:  # stage the next unit's Q
             yield wait("q_empty", ul)
             c.mb["q_full"].arrive()
         c.mb[f"list_empty{lb}"].arrive()
@@ -184,9 +216,9 @@ def softmax(c, units, warp, rng, p_waits_own=False):
         g += nst
 
 
-def run(units, seed, gate_empty=True, shared_s_full=False, p_waits_own=False):
+def run(units, seed, gate_empty=True, shared_s_full=False, p_waits_own=False, dynamic=True):
     rng = random.Random(seed)
-    c = Cta(shared_s_full)
+    c = Cta(shared_s_full, dynamic)
     warps = {0: producer_k(c, units), 1: mma_qk(c, units, rng), 2: producer_v(c, units),
              3: mma_pv(c, units, rng, gate_empty)}
     for w in range(4, 12):
@@ -248,15 +280,17 @@ def unit_sequences(n, seed):
     return [[rng.choice([0, 1, 2, 3, 4, 5, 39, 40]) for _ in range(rng.randint(1, 7))] for _ in range(n)]
 
 
-def test_kernel_protocol_never_deadlocks_or_passes_early():
+@pytest.mark.parametrize("dynamic", [False, True])
+def test_kernel_protocol_never_deadlocks_or_passes_early(dynamic):
     for i, units in enumerate(unit_sequences(400, 1)):
-        assert run(units, seed=i) == "ok", units
+        assert run(units, seed=i, dynamic=dynamic) == "ok", units
 
 
 @pytest.mark.parametrize("units", [[0], [0, 0, 3], [1], [1, 0, 1], [2, 40, 0, 41], [0, 0, 0], [3, 0, 0, 2]])
 def test_kernel_protocol_edge_units(units):
     for seed in range(50):
-        assert run(units, seed) == "ok"
+        assert run(units, seed, dynamic=False) == "ok"
+        assert run(units, seed, dynamic=True) == "ok"
 
 
 @pytest.mark.parametrize("mistake", ["gate_empty", "shared_s_full", "p_waits_own"])
@@ -267,5 +301,6 @@ def test_model_catches_planted_mistakes(mistake):
     write that waits for the group's own previous P.V instead of the other
     group's (P is single-buffered) must each be caught."""
     kw = {"gate_empty": False} if mistake == "gate_empty" else {mistake: True}
-    bad = [run(units, seed=i, **kw) for i, units in enumerate(unit_sequences(200, 2))]
-    assert any(r != "ok" for r in bad)
+    for dynamic in (False, True):
+        bad = [run(units, seed=i, dynamic=dynamic, **kw) for i, units in enumerate(unit_sequences(200, 2))]
+        assert any(r != "ok" for r in bad)

@@ -120,6 +120,21 @@ def test_deterministic():
     assert np.array_equal(a, b) and np.array_equal(la, lb)
 
 
+def test_deterministic_with_counts():
+    """Rows of variable length take the dynamic unit schedule (which CTA runs
+    a unit varies from run to run): the bits must not."""
+    wl = synth.WORKLOADS["mid"]
+    _, _, qt, kt, vt, vbs = tiled_inputs(wl)
+    idx = oracle.coarse(qt, kt, vbs, wl.topk, wl.sm_scale)
+    ridx, counts = ragged_counts(idx, 21)
+    runs = [gpu_fine(qt, kt, vt, ridx, vbs, wl.sm_scale, paired=paired, counts=counts)
+            for paired in (False, True) for _ in range(3)]
+    for a, la in runs[1:3]:
+        assert np.array_equal(a, runs[0][0]) and np.array_equal(la, runs[0][1])
+    for a, la in runs[4:]:
+        assert np.array_equal(a, runs[3][0]) and np.array_equal(la, runs[3][1])
+
+
 # ---------------------------------------------- per-row counts (variable length)
 def ragged_counts(idx, seed, fill=-1):
     """Random counts in [0, topk] (0 and topk always present); entries past a
