@@ -14,8 +14,9 @@
 // pairing (2u, 2u + 1) then puts exactly one block in each tile.
 //
 // GB300 design: pooling is a streaming read of q and k (one pass, 16-byte
-// loads, fp32 sums in token order); selection is one warp per query block:
-// scores in fp32 against every key block, the softmax weights, and the
+// loads, fp32 sums in token order); selection is one warp per query block,
+// the head's key-block means staged once per CTA in shared memory: scores in
+// fp32 against every key block, the softmax weights, and the
 // threshold found by a 32-step bitwise search over order-preserving integer
 // keys of the scores (the largest key t whose blocks with key >= t hold at
 // least tau of the mass), so no sort is needed; blocks tied at that key are
@@ -29,7 +30,7 @@ namespace vsa {
 namespace {
 
 constexpr int kBlockTokens = 128;
-constexpr int kSelWarps = 8;
+constexpr int kSelWarps = 32;  // query blocks per CTA (one warp each): the staged key means serve 32 rows
 constexpr int kMaxBlocks = 256;  // key blocks per row: cube table rows of up to 512 entries
 constexpr int kPerLane = kMaxBlocks / 32;
 
@@ -52,12 +53,12 @@ __global__ void __launch_bounds__(256) block_pool_kernel(const uint4* __restrict
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int r = 0; r < kBlockTokens; r += 8) {
-            uint4 w[8];
+        for (int r = 0; r < kBlockTokens; r += 16) {  // sixteen loads in flight, summed in token order
+            uint4 w[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) w[u] = __ldcs(base + (size_t)(r + u) * row_vecs + v);
+            for (int u = 0; u < 16; ++u) w[u] = __ldcs(base + (size_t)(r + u) * row_vecs + v);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < 16; ++u) {
                 const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -87,37 +88,106 @@ __device__ __forceinline__ float warp_max(float x) {
     return x;
 }
 
-// grid (ceil(nb / kSelWarps), heads, B): one warp per query block.
+// grid (ceil(nb / kSelWarps), heads, B): one warp per query block for the
+// selection.  The CTA stages the head's key-block means (rows padded to D + 4
+// floats: a float4 read by 32 lanes of 32 rows is 4 conflict-free phases) and
+// its 32 query-block means in shared memory, forms the 32 x nb score tile with
+// each thread holding 4 query rows x 2 key blocks (float4 reads, every score
+// summed channel by channel in order), and parks it in shared memory, from
+// where each warp takes its row.
+constexpr int kScoreLd = kMaxBlocks + 4;
+
+template <int D>
+__host__ __device__ constexpr size_t select_smem_bytes() {
+    return ((size_t)kMaxBlocks * (D + 4) + (size_t)kSelWarps * D + (size_t)kSelWarps * kScoreLd) * sizeof(float);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kSelWarps * 32) block_select_kernel(const float* __restrict__ means, int B, int nb,
                                                                       int heads, float scale_log2, float tau,
                                                                       int32_t* __restrict__ cube_idx,
                                                                       int32_t* __restrict__ cube_counts) {
-    constexpr int C = D / 32;
+    static_assert(kSelWarps == 32 && kMaxBlocks == 256, "the score tile covers 32 rows x 256 key blocks");
+    constexpr int LD = D + 4;
+    constexpr int kV = D / 4;  // float4 vectors per row
+    extern __shared__ __align__(16) float sel_smem[];
+    float* ks = sel_smem;                             // [kMaxBlocks][LD] key-block means
+    float* qs = ks + (size_t)kMaxBlocks * LD;         // [kSelWarps][D] query-block means
+    float* ss = qs + (size_t)kSelWarps * D;           // [kSelWarps][kScoreLd] scores
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int i = blockIdx.x * kSelWarps + warp;
+    const int i0 = blockIdx.x * kSelWarps;
+    const int i = i0 + warp;
     const int h = blockIdx.y;
     const int b = blockIdx.z;
-    if (i >= nb) return;  // no block-wide barrier below
     const size_t plane = (size_t)B * heads * nb * D;
     const size_t hoff = ((size_t)b * heads + h) * nb * D;
-    float qv[C];
+    // Key means: eight 16-byte loads per thread in flight (at most 8 each).
 #pragma unroll
-    for (int c = 0; c < C; ++c) qv[c] = means[hoff + (size_t)i * D + lane + 32 * c];
-    // Scores: lane t holds key blocks j = t + 32 s (s < kPerLane).
+    for (int e0 = 0; e0 < kMaxBlocks * kV; e0 += 8 * kSelWarps * 32) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e0 + u * kSelWarps * 32 + threadIdx.x;
+            if (e < nb * kV) v[u] = *reinterpret_cast<const float4*>(means + plane + hoff + (size_t)e * 4);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e0 + u * kSelWarps * 32 + threadIdx.x;
+            if (e < nb * kV) {
+                const int j = e / kV, c = e - j * kV;
+                *reinterpret_cast<float4*>(ks + j * LD + 4 * c) = v[u];
+            }
+        }
+    }
+    // Query means of the CTA's rows (zeros past nb).
+    for (int e = threadIdx.x; e < kSelWarps * kV; e += kSelWarps * 32) {
+        const int r = e / kV, c = e - r * kV;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i0 + r < nb) v = *reinterpret_cast<const float4*>(means + hoff + (size_t)(i0 + r) * D + 4 * c);
+        *reinterpret_cast<float4*>(qs + r * D + 4 * c) = v;
+    }
+    __syncthreads();
+    {
+        // Tile: rows 4 (warp & 7) .. + 3; key blocks lane + 32 (2 (warp >> 3) + {0, 1}).
+        const int r0 = 4 * (warp & 7);
+        const int j0 = lane + 64 * (warp >> 3), j1 = j0 + 32;
+        const float* k0 = ks + (j0 < nb ? j0 : 0) * LD;
+        const float* k1 = ks + (j1 < nb ? j1 : 0) * LD;
+        float acc[4][2];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < kV; ++c) {
+            const float4 a0 = *reinterpret_cast<const float4*>(k0 + 4 * c);
+            const float4 a1 = *reinterpret_cast<const float4*>(k1 + 4 * c);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float4 q = *reinterpret_cast<const float4*>(qs + (r0 + r) * D + 4 * c);
+                acc[r][0] = fmaf(q.x, a0.x, acc[r][0]);
+                acc[r][0] = fmaf(q.y, a0.y, acc[r][0]);
+                acc[r][0] = fmaf(q.z, a0.z, acc[r][0]);
+                acc[r][0] = fmaf(q.w, a0.w, acc[r][0]);
+                acc[r][1] = fmaf(q.x, a1.x, acc[r][1]);
+                acc[r][1] = fmaf(q.y, a1.y, acc[r][1]);
+                acc[r][1] = fmaf(q.z, a1.z, acc[r][1]);
+                acc[r][1] = fmaf(q.w, a1.w, acc[r][1]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            ss[(r0 + r) * kScoreLd + j0] = acc[r][0];
+            ss[(r0 + r) * kScoreLd + j1] = acc[r][1];
+        }
+    }
+    __syncthreads();
+    if (i >= nb) return;  // no block-wide barrier below
+    // Row i's scores: lane t holds key blocks j = t + 32 s (s < kPerLane).
     float sc[kPerLane];
 #pragma unroll
-    for (int s = 0; s < kPerLane; ++s) sc[s] = -INFINITY;
-    for (int j = 0; j < nb; ++j) {
-        const float* kr = means + plane + hoff + (size_t)j * D;
-        float part = 0.f;
-#pragma unroll
-        for (int c = 0; c < C; ++c) part = fmaf(qv[c], kr[lane + 32 * c], part);
-        part = warp_sum(part);
-#pragma unroll
-        for (int s = 0; s < kPerLane; ++s)
-            if (j == lane + 32 * s) sc[s] = part;
+    for (int s2 = 0; s2 < kPerLane; ++s2) {
+        const int j = lane + 32 * s2;
+        sc[s2] = j < nb ? ss[warp * kScoreLd + j] : -INFINITY;
     }
     // Softmax weights of the row (exp2 with log2(e) folded into the scale).
     float smax = -INFINITY;
@@ -211,7 +281,10 @@ cudaError_t launch_block_select(const void* q, const void* k, int B, int S, int 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kernel = D == 128 ? block_select_kernel<128> : block_select_kernel<64>;
-    kernel<<<dim3((nb + kSelWarps - 1) / kSelWarps, heads, B), kSelWarps * 32, 0, stream>>>(
+    const size_t smem = D == 128 ? select_smem_bytes<128>() : select_smem_bytes<64>();
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<dim3((nb + kSelWarps - 1) / kSelWarps, heads, B), kSelWarps * 32, smem, stream>>>(
         means, B, nb, heads, sm_scale * 1.4426950408889634f, tau, cube_idx, cube_counts);
     note_launches(1);
     return cudaGetLastError();

@@ -341,3 +341,29 @@ def test_named_entry_points_match_the_binding_bit_for_bit():
         assert status == 0
         assert torch.equal(out.view(torch.int16), ref_o.view(torch.int16)), paired
         assert torch.equal(lse, ref_lse), paired
+
+
+def test_dynamic_schedule_concurrent_streams():
+    """Dynamic-schedule launches (rows with counts) on two streams at once
+    take different unit-counter slots: each gives the bits it gives alone."""
+    wl = synth.WORKLOADS["mid"]
+    _, _, qt, kt, vt, vbs = tiled_inputs(wl)
+    idx = oracle.coarse(qt, kt, vbs, wl.topk, wl.sm_scale)
+    ridx, counts = ragged_counts(idx, 31)
+    ref_a, ref_la = gpu_fine(qt, kt, vt, ridx, vbs, wl.sm_scale, counts=counts)
+    ridx2, counts2 = ragged_counts(idx, 32)
+    ref_b, ref_lb = gpu_fine(qt, kt, vt, ridx2, vbs, wl.sm_scale, counts=counts2)
+    q, k, v, vb = to_dev(qt), to_dev(kt), to_dev(vt), i32_dev(vbs)
+    args = [(i32_dev(ridx), i32_dev(counts)), (i32_dev(ridx2), i32_dev(counts2))]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(8):
+        for s, (ix, cn) in zip(streams, args):
+            with torch.cuda.stream(s):
+                outs.append(vsa.sparse_attn_fwd(q, k, v, ix, vb, wl.sm_scale, counts=cn, stream=s))
+    torch.cuda.synchronize()
+    assert vsa.device_error(reset=True) == 0
+    for n, (o, l) in enumerate(outs):
+        ref, ref_l = (ref_a, ref_la) if n % 2 == 0 else (ref_b, ref_lb)
+        assert np.array_equal(to_bits(o), ref) and np.array_equal(l.cpu().numpy(), ref_l)
