@@ -50,16 +50,16 @@ WORKLOAD = "wan"
 # was taken from: if fine.cu no longer hashes to `source_sha256`, the traffic is reported
 # as null.
 FINE_TRAFFIC = {
-    "bytes_per_launch": (233.370112e6 + 56.521216e6) * 40 / 8,
+    "bytes_per_launch": (233.117696e6 + 55.445504e6) * 40 / 8,
     "capture": "profiles/fine_fwd_kernel_wan.md",
-    "source_sha256": "06239ee0868e8ddf1a9dcc8cba5a60b63b4fa4c37061c018d3988a1b3b40017b",
+    "source_sha256": "6e7173ac74a9415274dd98393d31250459216f88c902b2f30282065ec3321514",
 }
 # The same for the 128-token-block workload, from a capture of one whole
 # 12-head launch (no scaling).
 FINE_TRAFFIC_BLOCKS = {
-    "bytes_per_launch": 339.878144e6 + 90.351360e6,
+    "bytes_per_launch": 309.088768e6 + 86.803200e6,
     "capture": "profiles/fine_fwd_kernel_blocks128.md",
-    "source_sha256": "44a48d3b787e04f3baab5a4c55a8735929e36a67452d91c811afb17921d14bda",
+    "source_sha256": "6e7173ac74a9415274dd98393d31250459216f88c902b2f30282065ec3321514",
 }
 
 
