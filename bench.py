@@ -553,11 +553,11 @@ def e2e_leg(step, inputs, q, k, v, out, args, stream, dist, dev):
     douts = [out, torch.empty_like(out)]
     s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
     # Up to 30 steps per run: the first upload (about 5 ms for 1 GB at the
-    # ~210 GB/s host link) fills the pipeline once per run.  Three runs; the
+    # ~210 GB/s host link) fills the pipeline once per run.  Five runs; the
     # median is reported with every run's figure (a run now and then holds
     # one stall of tens of ms while copies and kernels overlap).
     e2e_steps = max(3, min(args.steps, 30))
-    e2e_repeats = 3
+    e2e_repeats = 5
 
     def e2e_run(n, first=None, compute=True):
         up = [torch.cuda.Event() for _ in range(2)]
