@@ -231,13 +231,14 @@ def coarse_select(qt, kt, vbs, topk: int, sm_scale: float = 0.0, workspace=None,
     return out
 
 
-def tile_pool(q, k, grid, qt=None, kt=None, vbs=None, workspace=None, want_qt=True, stream=None):
+def tile_pool(q, k, grid, qt=None, kt=None, vbs=None, workspace=None, want_qt=True, want_kt=True, stream=None):
     """Tile q and k and pool their cubes in one pass (vsa_tile_pool).
 
     Returns (qt, kt, vbs, workspace); pass vbs and workspace to
     coarse_select_pooled for the same top-k as coarse_select(qt, kt, vbs, ...).
     want_qt=False skips the tiled copy of q (qt is then None), for
-    sparse_attn_fwd_raster, which reads the raster q."""
+    sparse_attn_fwd_raster, which reads the raster q; want_kt=False likewise
+    skips the tiled copy of k (kt is then None: the statistics alone)."""
     torch = _torch()
     _need(q, torch.bfloat16, "q")
     _need(k, torch.bfloat16, "k")
@@ -251,7 +252,7 @@ def tile_pool(q, k, grid, qt=None, kt=None, vbs=None, workspace=None, want_qt=Tr
     shape = (B, 64 * N, heads, D)
     if qt is None and want_qt:
         qt = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
-    if kt is None:
+    if kt is None and want_kt:
         kt = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
     if vbs is None:
         vbs = torch.empty((N,), dtype=torch.int32, device=q.device)
@@ -269,8 +270,8 @@ def tile_pool(q, k, grid, qt=None, kt=None, vbs=None, workspace=None, want_qt=Tr
     if workspace.numel() < nbytes:
         raise ValueError(f"workspace needs {nbytes} bytes")
     _check(library().vsa_tile_pool(ctypes.byref(g), q.data_ptr(), k.data_ptr(), None if qt is None else qt.data_ptr(),
-                                   kt.data_ptr(), vbs.data_ptr(), workspace.data_ptr(), _stream(stream)),
-           "vsa_tile_pool")
+                                   None if kt is None else kt.data_ptr(), vbs.data_ptr(), workspace.data_ptr(),
+                                   _stream(stream)), "vsa_tile_pool")
     return qt, kt, vbs, workspace
 
 

@@ -67,7 +67,8 @@ def test_raster_with_counts_and_empty_rows():
 
 
 def test_tile_pool_without_qt():
-    """want_qt=False: kt, vbs and the pooled statistics as with the copy."""
+    """want_qt=False (and want_kt=False): kt, vbs and the pooled statistics as
+    with the copies."""
     wl = synth.WORKLOADS["mid"]
     d = synth.make_inputs(wl)
     q, k = to_dev(d["q"]), to_dev(d["k"])
@@ -77,6 +78,10 @@ def test_tile_pool_without_qt():
     assert qt2 is None
     head = 16 * wl.heads * wl.ncubes * wl.D + 8 * wl.heads * wl.ncubes
     assert torch.equal(kt, kt2) and torch.equal(vbs, vbs2) and torch.equal(ws[:head], ws2[:head])
+    qt3, kt3, vbs3, ws3 = vsa.tile_pool(q, k, wl.grid, want_qt=False, want_kt=False)  # statistics alone
+    torch.cuda.synchronize()
+    assert qt3 is None and kt3 is None
+    assert torch.equal(vbs, vbs3) and torch.equal(ws[:head], ws3[:head])
 
 
 def test_wan_full_size():
