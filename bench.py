@@ -51,14 +51,14 @@ WORKLOAD = "wan"
 # as null.
 FINE_TRAFFIC = {
     "bytes_per_launch": (233.117696e6 + 55.445504e6) * 40 / 8,
-    "capture": "profiles/fine_fwd_kernel_wan.md",
+    "capture": "ncu, fine_fwd_kernel on the Wan2.2 grid with 8 heads (one launch), scaled x5",
     "source_sha256": "6e7173ac74a9415274dd98393d31250459216f88c902b2f30282065ec3321514",
 }
 # The same for the 128-token-block workload, from a capture of one whole
 # 12-head launch (no scaling).
 FINE_TRAFFIC_BLOCKS = {
     "bytes_per_launch": 309.088768e6 + 86.803200e6,
-    "capture": "profiles/fine_fwd_kernel_blocks128.md",
+    "capture": "ncu, fine_fwd_kernel on the 128-token-block workload (one whole launch)",
     "source_sha256": "6e7173ac74a9415274dd98393d31250459216f88c902b2f30282065ec3321514",
 }
 
