@@ -286,6 +286,31 @@ def step_bytes(wl):
     return 4 * untiled + 2 * tiled
 
 
+def executed_tensor_flops(idx, pairs, D: int) -> float:
+    """Tensor-core FLOPs the paired fine kernel issues for a selection.
+
+    A unit (query cubes i and j, 128 query rows) walks the union U of the two
+    selections two key cubes per step: each step runs Q.K^T over 128 rows x
+    128 keys, and P.V over the step's keys (64 per cube), so a unit costs
+    ceil(|U| / 2) * 2*128*128*D + |U| * 2*128*64*D FLOPs.  idx: [B, heads, N,
+    k] int32 (every entry in [0, N)); pairs: [B, heads, ceil(N / 2)] as
+    i | (j << 16), j = 0xFFFF for a single cube."""
+    idx = np.asarray(idx)
+    pr = np.asarray(pairs).astype(np.int64) & 0xFFFFFFFF
+    B, H, N, k = idx.shape
+    steps = cubes = 0
+    for b in range(B):
+        for h in range(H):
+            sel = np.zeros((N + 1, N), dtype=bool)  # row N: no cube
+            sel[np.repeat(np.arange(N), k), idx[b, h].reshape(-1)] = True
+            i0 = np.minimum(pr[b, h] & 0xFFFF, N)
+            i1 = np.minimum(pr[b, h] >> 16, N)
+            u = (sel[i0] | sel[i1]).sum(axis=1)
+            steps += int(((u + 1) // 2).sum())
+            cubes += int(u.sum())
+    return float(steps) * 2 * 128 * 128 * D + float(cubes) * 2 * 128 * 64 * D
+
+
 # --------------------------------------------------------- blocks128
 def blocks_flops(counts, D: int) -> float:
     """Effective fine-stage FLOPs of a cube table: 4 * 64 * 64 * D per (query
@@ -530,7 +555,11 @@ def run_ours(args, wl, inputs, rank, world, dist):
     qt, _ = vsa.tile(q, grid, vbs=vbs2)
     ot = torch.empty_like(qt)
     nxt = time_next_rows(vsa, torch, wl, qt, kt, vt, idx, vbs, pairs, ot, lse, stream)
-    return ms_step, stage, clk.summary(), (e2e_ms, h2d, d2h, copy_ms), launches, nxt
+    try:  # the tensor-core work the step's fine launch issued (host-side count, outside every timing)
+        executed = executed_tensor_flops(idx.cpu().numpy(), pairs.cpu().numpy(), wl.D)
+    except Exception:  # context only: never let it cost the result line
+        executed = None
+    return ms_step, stage, clk.summary(), (e2e_ms, h2d, d2h, copy_ms), launches, nxt, executed
 
 
 def e2e_leg(step, inputs, q, k, v, out, args, stream, dist, dev):
@@ -767,8 +796,8 @@ def main():
         dist.barrier()
 
     inputs = synth.make_inputs(wl)
-    ms_step, stage, clocks, (e2e_ms, h2d, d2h, copy_ms), launches, nxt = run_ours(args, wl, inputs, rank, world,
-                                                                                  dist)
+    ms_step, stage, clocks, (e2e_ms, h2d, d2h, copy_ms), launches, nxt, executed = run_ours(args, wl, inputs, rank,
+                                                                                            world, dist)
 
     burst, sustained, hbm, peak_kind = load_peaks()
     flops = wl.fine_flops()
@@ -782,7 +811,14 @@ def main():
         "fine_kernel": {
             "ms_per_call_mean": fine_ms, "ms_per_call_median": statistics.median(stage["sparse_attn_fwd"]),
             "effective_tflops": fine_tflops, "frac_of_burst_peak": fine_tflops / burst,
-            "frac_of_sustained_peak": fine_tflops / sustained},
+            "frac_of_sustained_peak": fine_tflops / sustained,
+            # The pair tiles also compute the keys of the other cube's selection
+            # (the union walk): the tensor-core work issued, its rate, and the
+            # selected share of it.
+            "executed_tensor_flops": executed,
+            "executed_tflops": None if executed is None else executed / (fine_ms * 1e-3) / 1e12,
+            "executed_frac_of_burst_peak": None if executed is None else executed / (fine_ms * 1e-3) / 1e12 / burst,
+            "selected_share_of_executed": None if executed is None else flops / executed},
         "stages_ms_median": {k: statistics.median(v) for k, v in stage.items()},
         "stages_hbm_gbs": {k: b / (statistics.median(stage[k]) * 1e-3) / 1e9
                            for k, b in stage_bytes(wl).items()},
