@@ -26,6 +26,7 @@ __all__ = [
     "sparse_attn_fwd", "validate_indices", "device_error", "debug_wait_timeout", "pipeline",
     "coarse_attn", "coarse_attn_workspace_bytes", "pair_cubes", "pair_workspace_bytes", "kernel_launches",
     "table_from_csr", "block_select", "block_select_workspace_bytes", "sparse_attn_fwd_peak", "all_cubes",
+    "PipelineGraph",
 ]
 
 _STATUS = {0: "VSA_OK", 1: "VSA_ERR_INVALID_ARG", 2: "VSA_ERR_UNSUPPORTED", 3: "VSA_ERR_ALIGNMENT",
@@ -613,3 +614,38 @@ def pipeline(q, k, v, grid, topk: int, sm_scale: float = 0.0, stream=None):
     idx = coarse_select_pooled(ws, vbs, B, heads, D, topk, sm_scale, stream=stream)
     pairs = pair_cubes(idx, stream=stream)
     return (*sparse_attn_fwd_raster(q, kt, vt, idx, vbs, grid, sm_scale, pairs=pairs, stream=stream), idx)
+
+
+class PipelineGraph:
+    """pipeline() captured once as a CUDA graph for fixed shapes, then
+    replayed: for repeated calls on inputs of one shape (serving), with no
+    per-call launch or argument marshalling.
+
+    The graph owns its inputs (copies of q, k, v made at construction) and its
+    outputs (out, lse, topk_idx: pipeline()'s return values, overwritten by
+    every replay).  Calling it copies any given inputs into the graph's
+    buffers on the current stream, replays the graph there and returns the
+    output tensors.  The kernels and their arguments (tensor maps included)
+    are fixed at capture, so the buffers must not be reallocated."""
+
+    def __init__(self, q, k, v, grid, topk: int, sm_scale: float = 0.0):
+        torch = _torch()
+        self.q, self.k, self.v = (x.detach().clone() for x in (q, k, v))
+        dev = self.q.device
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):  # a first run outside the capture sets kernel attributes, loads modules
+            pipeline(self.q, self.k, self.v, grid, topk, sm_scale)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.out, self.lse, self.topk_idx = pipeline(self.q, self.k, self.v, grid, topk, sm_scale)
+
+    def __call__(self, q=None, k=None, v=None):
+        for dst, src in ((self.q, q), (self.k, k), (self.v, v)):
+            if src is not None:
+                if src.shape != dst.shape or src.dtype != dst.dtype:
+                    raise ValueError("inputs must keep the shape and dtype the graph was captured with")
+                dst.copy_(src)
+        self.graph.replay()
+        return self.out, self.lse, self.topk_idx
