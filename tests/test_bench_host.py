@@ -52,3 +52,39 @@ def test_selected_share_is_one_for_identical_selections():
     idx = np.tile(np.arange(k, dtype=np.int32), (1, 1, N, 1))
     pairs = np.array([[[2 * u | ((2 * u + 1) << 16) for u in range(N // 2)]]], dtype=np.int32)
     assert bench.executed_tensor_flops(idx, pairs, D) == 4.0 * 64 * k * 64 * D * N
+
+
+def test_result_line_keeps_the_contract(monkeypatch, capsys):
+    """main() assembles the one JSON line with every key the contract names,
+    from a stubbed device run (the GPU legs are measured on the GPU machine)."""
+    import json
+
+    def fake_run_ours(args, wl, inputs, rank, world, dist):
+        stage = {n: [1.0, 1.2] for n in ["tile_k_pool_qk", "coarse_select", "pair_cubes", "sparse_attn_fwd",
+                                         "tile_v"]}
+        clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+        return 2.0, stage, clocks, (None, 0, 0, None), 10, {}, 3.0e11
+
+    monkeypatch.setattr(bench, "run_ours", fake_run_ours)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--heads", "2", "--steps", "2", "--no-cpu-baseline", "--no-e2e"])
+    assert bench.main() == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"):
+        assert key in line, key
+    assert line["n_gpus"] == 1 and line["steps"] == 2 and line["warmup"] >= 3 and line["ms_per_step"] == 2.0
+    assert line["higher_is_better"] is True and line["scaling"] == "weak" and line["dtype"] == "bf16"
+    assert "workload" in line["config"]
+    roof = line["roofline"]
+    assert set(("bound", "achieved", "peak", "unit", "frac", "traffic")) <= set(roof)
+    assert roof["bound"] == "tensor" and roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"])
+    assert roof["traffic"] is None  # taken from a 40-head capture: none for another head count
+    fk = line["fine_kernel"]
+    assert fk["executed_tensor_flops"] == 3.0e11
+    assert fk["selected_share_of_executed"] == pytest.approx(bench_flops(line) / 3.0e11)
+
+
+def bench_flops(line):
+    """The line's effective fine-stage FLOPs, back from its rate and time."""
+    fk = line["fine_kernel"]
+    return fk["effective_tflops"] * 1e12 * fk["ms_per_call_mean"] * 1e-3
